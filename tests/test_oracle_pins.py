@@ -1,0 +1,415 @@
+"""Pins for the CPU oracle (no GPU).
+
+The pages print no equations and no worked example of the decode step, so the
+oracle is pinned to things other than itself: closed forms (RMSNorm of a constant
+vector, RoPE as a complex rotation, single-key attention), textbook/library routines
+(torch rms_norm, scaled_dot_product_attention with GQA, silu, stable sort), an
+independently written float64 NumPy twin, and structural invariants (cached decode
+equals a full causal recompute; paged equals contiguous; page permutations and
+batch composition change nothing; MoE with one expert is the dense MLP).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import synth
+from oracle.twin import Twin, bf16_bits_to_f64, round_to_bf16
+
+TINY = synth.TINY
+TINY_MOE = synth.ModelConfig("tiny-moe", n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=2,
+                             head_dim=64, ffn_dim=0, vocab=512, n_experts=8, top_k=2,
+                             expert_ffn_dim=128, max_positions=512)
+
+
+def bits(t):
+    return synth.bf16_bits(t)
+
+
+# ---------------------------------------------------------------- BF16 rounding
+def test_bf16_round_to_nearest_even_cases():
+    one = 1.0
+    ulp = 2.0 ** -7  # BF16 spacing at 1.0 (8 significant bits)
+    cases = {
+        one: 0x3F80,
+        one + ulp / 2: 0x3F80,          # tie -> even (1.0)
+        one + 3 * ulp / 2: 0x3F82,      # tie -> even (1 + 2 ulp)
+        one + ulp / 2 + 2 ** -20: 0x3F81,  # just above the tie -> up
+        -2.0: 0xC000,
+        0.0: 0x0000,
+    }
+    for x, want in cases.items():
+        assert oracle.lib().or_f32_to_bf16(x) == want, x
+
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal(4000) * np.exp(rng.uniform(-20, 20, 4000))).astype(np.float32)
+    got = oracle.f32_to_bf16_bits(x)
+    want = bits(torch.from_numpy(x).to(torch.bfloat16))
+    assert np.array_equal(got, want)
+    assert np.array_equal(bits(torch.from_numpy(x).to(torch.bfloat16)),
+                          (round_to_bf16(x).astype(np.float32).view(np.uint32) >> 16)
+                          .astype(np.uint16))
+
+
+# ---------------------------------------------------------------- RMSNorm
+def test_rmsnorm_constant_vector_closed_form():
+    n, eps = 256, 1e-5
+    g = torch.ones(n, dtype=torch.bfloat16)
+    for c in (3.0, -0.25, 1e-3):
+        out = oracle.rmsnorm(np.full(n, c, np.float32), bits(g), eps)
+        want = c / math.sqrt(c * c + eps)
+        np.testing.assert_allclose(out, want, rtol=1e-6)
+
+
+def test_rmsnorm_matches_torch_and_uses_gain():
+    rng = np.random.default_rng(1)
+    n, eps = 2048, 1e-5
+    x = rng.standard_normal(n).astype(np.float32) * 0.3
+    g = (1 + 0.1 * torch.from_numpy(rng.standard_normal(n).astype(np.float32))).to(torch.bfloat16)
+    out = oracle.rmsnorm(x, bits(g), eps)
+    want = F.rms_norm(torch.from_numpy(x).double(), (n,), g.double(), eps).numpy()
+    np.testing.assert_allclose(out, want, rtol=2e-6, atol=1e-6)
+    ms = float(np.mean(x.astype(np.float64) ** 2))
+    assert np.sqrt(np.mean((out / g.float().numpy()) ** 2)) == pytest.approx(
+        math.sqrt(ms / (ms + eps)), abs=1e-6)
+
+
+# ---------------------------------------------------------------- RoPE
+def test_rope_position_zero_is_identity():
+    v = np.random.default_rng(2).standard_normal(128).astype(np.float32)
+    assert np.array_equal(oracle.rope(v, 0, 1e4), v)
+
+
+def test_rope_single_pair_is_rotation_by_pos_radians():
+    # hd = 2: one pair, inv_freq = theta^0 = 1, so position p rotates by p radians
+    for p in (1, 2, 7):
+        out = oracle.rope(np.array([1.0, 0.0], np.float32), p, 1e4)
+        np.testing.assert_allclose(out, [math.cos(p), math.sin(p)], atol=1e-6)
+
+
+def test_rope_is_complex_rotation_and_keeps_pair_norms():
+    rng = np.random.default_rng(3)
+    hd, theta = 128, 1e4
+    v = rng.standard_normal(hd).astype(np.float32)
+    for pos in (1, 17, 4095, 8191):
+        out = oracle.rope(v, pos, theta)
+        i = np.arange(hd // 2)
+        z = (v[:64] + 1j * v[64:]) * np.exp(1j * pos * theta ** (-2.0 * i / hd))
+        np.testing.assert_allclose(out, np.concatenate([z.real, z.imag]), atol=2e-5)
+        np.testing.assert_allclose(np.hypot(out[:64], out[64:]), np.hypot(v[:64], v[64:]),
+                                   rtol=1e-5)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal(64).astype(np.float32)
+    k = rng.standard_normal(64).astype(np.float32)
+    a = np.dot(oracle.rope(q, 40, 1e4), oracle.rope(k, 33, 1e4))
+    b = np.dot(oracle.rope(q, 1007, 1e4), oracle.rope(k, 1000, 1e4))
+    assert a == pytest.approx(b, rel=1e-4, abs=1e-4)
+
+
+# ---------------------------------------------------------------- attention
+def test_attention_single_key_returns_v_exactly():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal(128).astype(np.float32)
+    K = rng.standard_normal((1, 128)).astype(np.float32)
+    V = rng.standard_normal((1, 128)).astype(np.float32)
+    assert np.array_equal(oracle.attend(q, K, V), V[0])
+
+
+def test_attention_uniform_scores_give_mean_and_onehot_selects():
+    rng = np.random.default_rng(6)
+    K = rng.standard_normal((37, 64)).astype(np.float32)
+    V = rng.standard_normal((37, 64)).astype(np.float32)
+    np.testing.assert_allclose(oracle.attend(np.zeros(64, np.float32), K, V), V.mean(0),
+                               rtol=1e-5, atol=1e-6)
+    K2 = np.zeros((37, 64), np.float32)
+    K2[11, 0] = 1.0
+    q = np.zeros(64, np.float32)
+    q[0] = 1e4  # score 1e4/8 for key 11, 0 for the others
+    np.testing.assert_allclose(oracle.attend(q, K2, V), V[11], rtol=1e-6)
+
+
+def test_attention_matches_torch_sdpa():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal(128).astype(np.float32)
+    K = rng.standard_normal((300, 128)).astype(np.float32)
+    V = rng.standard_normal((300, 128)).astype(np.float32)
+    want = F.scaled_dot_product_attention(torch.from_numpy(q).double()[None, None, None],
+                                          torch.from_numpy(K).double()[None, None],
+                                          torch.from_numpy(V).double()[None, None])[0, 0, 0]
+    np.testing.assert_allclose(oracle.attend(q, K, V), want.numpy(), rtol=1e-5, atol=1e-6)
+
+
+def test_matvec_matches_float64_matmul():
+    rng = np.random.default_rng(8)
+    W = torch.from_numpy(rng.standard_normal((64, 2048)).astype(np.float32) * 0.02).to(torch.bfloat16)
+    x = rng.standard_normal(2048).astype(np.float32)
+    np.testing.assert_allclose(oracle.matvec(bits(W), x), W.double().numpy() @ x,
+                               rtol=1e-4, atol=1e-5)
+
+
+# ---------------------------------------------------------------- routing / argmax
+def test_route_matches_brute_force_sort():
+    rng = np.random.default_rng(9)
+    for _ in range(20):
+        lg = rng.standard_normal(64).astype(np.float32)
+        ids, w = oracle.route(lg, 8)
+        p = np.exp(lg.astype(np.float64) - lg.max())
+        p /= p.sum()
+        order = sorted(range(64), key=lambda e: (-p[e], e))[:8]
+        assert ids.tolist() == order
+        np.testing.assert_allclose(w, p[order] / p[order].sum(), rtol=1e-5)
+        assert w.sum() == pytest.approx(1.0, abs=1e-6)
+
+
+def test_route_ties_take_lower_index_and_uniform_gives_equal_weights():
+    ids, w = oracle.route(np.zeros(64, np.float32), 8)
+    assert ids.tolist() == list(range(8))
+    np.testing.assert_allclose(w, 1 / 8, rtol=1e-6)
+    ids, w = oracle.route(np.zeros(8, np.float32), 8)  # k = E: all experts, mean
+    np.testing.assert_allclose(w, 1 / 8, rtol=1e-6)
+
+
+def test_argmax_ties_lowest_index():
+    v = np.array([0.5, 2.0, -1.0, 2.0, 2.0], np.float32)
+    assert oracle.argmax(v) == 1
+    assert oracle.argmax(np.zeros(10, np.float32)) == 0
+
+
+# ---------------------------------------------------------------- whole model helpers
+def _model(cfg, seed, gain_noise=0.0):
+    W = synth.make_weights(cfg, seed, gain_noise=gain_noise)
+    return W, oracle.OracleModel(cfg, W)
+
+
+def _decode_sequence(om, cfg, tokens, num_pages=8, perm_seed=0, window=None):
+    """Teacher-forced decode of one sequence through the paged cache; returns the
+    logits of every step and the final pool."""
+    T = len(tokens)
+    rng = np.random.default_rng(perm_seed)
+    pages = (T + cfg.page_size - 1) // cfg.page_size
+    pt = synth.random_page_tables(rng, num_pages, [pages], max_pages=pages + 1)
+    kv = np.zeros(synth.kv_pool_shape(cfg, num_pages), np.uint16)
+    out = []
+    for t in range(T):
+        lg, _ = om.decode_step(kv, [tokens[t]], [t], pt, [t + 1], nthreads=2)
+        out.append(lg[0])
+    return np.stack(out), kv, pt
+
+
+def _torch_reference_forward(cfg, W, tokens):
+    """Full causal forward in float64 from torch library routines (rms_norm, sdpa
+    with GQA and a causal/window mask, silu); RoPE as a complex rotation; the K/V
+    the cache would hold rounded to BF16."""
+    f = lambda t: t.double()  # noqa: E731
+    T, hd = len(tokens), cfg.head_dim
+    tok = torch.tensor(tokens)
+    x = f(W["embed"])[tok]
+    i = torch.arange(hd // 2, dtype=torch.float64)
+    ang = torch.arange(T, dtype=torch.float64)[:, None] * cfg.rope_theta ** (-2.0 * i / hd)
+    rot = torch.polar(torch.ones_like(ang), ang)
+    rot = torch.complex(rot.real.float().double(), rot.imag.float().double())
+
+    def rope(v):  # [T, H, hd]
+        z = torch.complex(v[..., : hd // 2], v[..., hd // 2:]) * rot[:, None, :]
+        return torch.cat([z.real, z.imag], -1)
+
+    def bf(v):
+        return v.float().to(torch.bfloat16).double()
+
+    pos = torch.arange(T)
+    for l, L in enumerate(W["layers"]):
+        xn = F.rms_norm(x, (cfg.d_model,), f(L["attn_norm"]), cfg.rms_eps)
+        q = rope((xn @ f(L["wq"]).T).view(T, cfg.n_q_heads, hd))
+        k = bf(rope((xn @ f(L["wk"]).T).view(T, cfg.n_kv_heads, hd)))
+        v = bf((xn @ f(L["wv"]).T).view(T, cfg.n_kv_heads, hd))
+        mask = pos[None, :] <= pos[:, None]
+        if cfg.sliding_window > 0 and cfg.layer_is_sliding()[l]:
+            mask &= pos[None, :] > pos[:, None] - cfg.sliding_window
+        o = F.scaled_dot_product_attention(q.transpose(0, 1), k.transpose(0, 1),
+                                           v.transpose(0, 1), attn_mask=mask, enable_gqa=True)
+        x = x + o.transpose(0, 1).reshape(T, -1) @ f(L["wo"]).T
+        xn = F.rms_norm(x, (cfg.d_model,), f(L["mlp_norm"]), cfg.rms_eps)
+        if cfg.is_moe:
+            r = torch.softmax(xn @ f(L["router"]).T, -1)
+            top = torch.topk(r, cfg.top_k, dim=-1, sorted=True)
+            wts = top.values / top.values.sum(-1, keepdim=True)
+            mo = torch.zeros_like(x)
+            for t in range(T):
+                for e, we in zip(top.indices[t].tolist(), wts[t].tolist()):
+                    h = F.silu(xn[t] @ f(L["exp_gate"][e]).T) * (xn[t] @ f(L["exp_up"][e]).T)
+                    mo[t] += we * (h @ f(L["exp_down"][e]).T)
+            x = x + mo
+        else:
+            h = F.silu(xn @ f(L["w_gate"]).T) * (xn @ f(L["w_up"]).T)
+            x = x + h @ f(L["w_down"]).T
+    xn = F.rms_norm(x, (cfg.d_model,), f(W["final_norm"]), cfg.rms_eps)
+    return (xn @ f(W["lm_head"]).T).numpy()
+
+
+@pytest.fixture(scope="module")
+def tiny_run():
+    cfg = TINY
+    W, om = _model(cfg, 0, gain_noise=0.02)
+    rng = np.random.default_rng(0)
+    tokens = synth.random_tokens(rng, cfg.vocab, 48).tolist()
+    logits, kv, pt = _decode_sequence(om, cfg, tokens, num_pages=8, perm_seed=1)
+    return cfg, W, om, tokens, logits, kv, pt
+
+
+def test_cached_decode_equals_full_recompute(tiny_run):
+    cfg, W, om, tokens, logits, _, _ = tiny_run
+    full = om.forward_full(tokens, nthreads=2)
+    np.testing.assert_allclose(logits, full, rtol=0, atol=1e-5)
+
+
+def test_oracle_matches_float64_twin(tiny_run):
+    cfg, W, om, tokens, logits, _, _ = tiny_run
+    tw = Twin(cfg, W)
+    cache = tw.new_cache()
+    for t in (0, 1, 15, 16, 17, 31, 47):
+        while cache[0]["k"].shape[0] < t:
+            tw.step(cache, tokens[cache[0]["k"].shape[0]], cache[0]["k"].shape[0])
+        np.testing.assert_allclose(logits[t], tw.step(cache, tokens[t], t), rtol=0, atol=1e-4)
+
+
+def test_oracle_matches_torch_library_forward(tiny_run):
+    cfg, W, om, tokens, logits, _, _ = tiny_run
+    ref = _torch_reference_forward(cfg, W, tokens)
+    np.testing.assert_allclose(logits, ref, rtol=0, atol=1e-4)
+
+
+def test_norm_gains_are_used(tiny_run):
+    cfg, W, om, tokens, logits, _, _ = tiny_run
+    W1 = synth.make_weights(cfg, 0, gain_noise=0.0)
+    lg1, _, _ = _decode_sequence(oracle.OracleModel(cfg, W1), cfg, tokens[:4], perm_seed=1)
+    assert np.abs(lg1 - logits[:4]).max() > 1e-3
+
+
+def test_paged_equals_contiguous_and_permutation_invariant(tiny_run):
+    cfg, W, om, tokens, logits, _, _ = tiny_run
+    T = 20
+    # contiguous: pages 0,1 in order; permuted: a 16-page pool, two other permutations
+    ref = None
+    for num_pages, seed in ((2, None), (16, 5), (16, 9)):
+        kv = np.zeros(synth.kv_pool_shape(cfg, num_pages), np.uint16)
+        if seed is None:
+            pt = np.array([[0, 1]], np.int32)
+        else:
+            pt = synth.random_page_tables(np.random.default_rng(seed), num_pages, [2], 2)
+        out = [om.decode_step(kv, [tokens[t]], [t], pt, [t + 1], nthreads=2)[0][0]
+               for t in range(T)]
+        out = np.stack(out)
+        if ref is None:
+            ref = out
+        assert np.array_equal(out, ref)
+    assert np.array_equal(ref, logits[:T])
+
+
+def test_kv_append_writes_exactly_one_slot_per_layer_head(tiny_run):
+    cfg, W, om, tokens, _, _, _ = tiny_run
+    num_pages = 6
+    kv = np.full(synth.kv_pool_shape(cfg, num_pages), 0xABCD, np.uint16)
+    pt = np.array([[4, 1, 3]], np.int32)
+    pos = 21  # page index 1 -> physical page 1, slot 5
+    before = kv.copy()
+    om.decode_step(kv, [tokens[0]], [pos], pt, [pos + 1], nthreads=2)
+    changed = np.argwhere(np.any(kv != before, axis=-1))
+    want = {(l, 1, kvi, g, 5) for l in range(cfg.n_layers) for kvi in (0, 1)
+            for g in range(cfg.n_kv_heads)}
+    assert {tuple(c) for c in changed.tolist()} == want
+
+
+def test_batch_rows_are_independent(tiny_run):
+    cfg, W, om, tokens, _, _, _ = tiny_run
+    rng = np.random.default_rng(11)
+    num_pages = 24
+    lens = [5, 37, 20]
+    pt = synth.random_page_tables(rng, num_pages, [(n + 15) // 16 + 1 for n in lens], 4)
+    kv = np.zeros(synth.kv_pool_shape(cfg, num_pages), np.uint16)
+    kv[:] = synth.bf16_bits(torch.randn(kv.shape, generator=torch.Generator().manual_seed(3))
+                            .to(torch.bfloat16))
+    kv0 = kv.copy()
+    toks = [7, 99, 4000]
+    lg_b, nt_b = om.decode_step(kv, toks, lens, pt, [n + 1 for n in lens], nthreads=2)
+    for b in range(3):
+        kv1 = kv0.copy()
+        lg1, nt1 = om.decode_step(kv1, toks[b:b + 1], lens[b:b + 1], pt[b:b + 1],
+                                  [lens[b] + 1], nthreads=2)
+        assert np.array_equal(lg1[0], lg_b[b]) and nt1[0] == nt_b[b]
+    assert np.array_equal(nt_b, np.argmax(lg_b, axis=1))
+
+
+def test_sliding_window_wider_than_context_is_full_attention(tiny_run):
+    cfg, W, om, tokens, logits, _, _ = tiny_run
+    cfg_w = cfg.with_(sliding_window=1000)
+    om_w = oracle.OracleModel(cfg_w, W)
+    lg, _, _ = _decode_sequence(om_w, cfg_w, tokens, perm_seed=1)
+    assert np.array_equal(lg, logits)
+
+
+def test_sliding_window_matches_twin_and_torch():
+    cfg = TINY.with_(sliding_window=8)
+    W, om = _model(cfg, 2)
+    tokens = synth.random_tokens(np.random.default_rng(2), cfg.vocab, 30).tolist()
+    lg, _, _ = _decode_sequence(om, cfg, tokens, perm_seed=3)
+    np.testing.assert_allclose(lg, _torch_reference_forward(cfg, W, tokens), atol=1e-4, rtol=0)
+    full = oracle.OracleModel(TINY, W)
+    lg_full, _, _ = _decode_sequence(full, TINY, tokens, perm_seed=3)
+    assert np.abs(lg_full[-1] - lg[-1]).max() > 1e-3  # the window changed something
+    tw = Twin(cfg, W)
+    cache = tw.new_cache()
+    for t in range(30):
+        out = tw.step(cache, tokens[t], t)
+    np.testing.assert_allclose(lg[-1], out, atol=1e-4, rtol=0)
+
+
+def test_moe_with_one_expert_is_dense_swiglu():
+    dense_cfg = TINY.with_(vocab=512)
+    W = synth.make_weights(dense_cfg, 4)
+    moe_cfg = dense_cfg.with_(name="moe1", ffn_dim=0, n_experts=1, top_k=1,
+                              expert_ffn_dim=dense_cfg.ffn_dim)
+    Wm = {k: v for k, v in W.items() if k != "layers"}
+    Wm["layers"] = []
+    for L in W["layers"]:
+        M = {k: v for k, v in L.items() if k not in ("w_gate", "w_up", "w_down")}
+        M["router"] = synth.normal_bf16((1, dense_cfg.d_model), 0.02, 1)
+        M["exp_gate"], M["exp_up"], M["exp_down"] = (L["w_gate"][None], L["w_up"][None],
+                                                     L["w_down"][None])
+        Wm["layers"].append(M)
+    toks = [3, 50, 7, 400]
+    a, _, _ = _decode_sequence(oracle.OracleModel(dense_cfg, W), dense_cfg, toks)
+    b, _, _ = _decode_sequence(oracle.OracleModel(moe_cfg, Wm), moe_cfg, toks)
+    assert np.array_equal(a, b)
+
+
+def test_moe_matches_twin_and_torch():
+    cfg = TINY_MOE
+    W, om = _model(cfg, 5)
+    tokens = synth.random_tokens(np.random.default_rng(5), cfg.vocab, 20).tolist()
+    lg, _, _ = _decode_sequence(om, cfg, tokens, perm_seed=4)
+    np.testing.assert_allclose(lg, _torch_reference_forward(cfg, W, tokens), atol=1e-4, rtol=0)
+    tw = Twin(cfg, W)
+    cache = tw.new_cache()
+    for t in range(20):
+        out = tw.step(cache, tokens[t], t)
+    np.testing.assert_allclose(lg[-1], out, atol=1e-4, rtol=0)
+
+
+def test_oracle_rejects_bad_inputs(tiny_run):
+    cfg, W, om, tokens, _, _, _ = tiny_run
+    kv = np.zeros(synth.kv_pool_shape(cfg, 4), np.uint16)
+    pt = np.array([[0, 1]], np.int32)
+    with pytest.raises(ValueError):
+        om.decode_step(kv, [cfg.vocab], [0], pt, [1])       # token out of range
+    with pytest.raises(ValueError):
+        om.decode_step(kv, [1], [3], pt, [3])               # seq_len != pos + 1
+    with pytest.raises(ValueError):
+        om.decode_step(kv, [1], [3], np.array([[9, 1]], np.int32), [4])  # bad page id
