@@ -1,0 +1,215 @@
+/*
+ * mk.h -- C ABI of the persistent decode megakernel (sm_103a).
+ *
+ * One call, mk_decode_step, runs one autoregressive decode step of a pre-norm
+ * transformer LM for 1..8 sequences as ONE persistent CUDA kernel: RMSNorm, QKV
+ * projection, RoPE, paged-KV GQA attention (optionally sliding-window), output
+ * projection + residual, SwiGLU MLP or softmax-top-k MoE, final norm, LM head and
+ * greedy argmax. Work is a task graph of GEMV row tiles and attention key splits,
+ * ordered by dependency counters instead of grid-wide barriers.
+ *
+ * Source of the operation (pages, by title and section):
+ *   "Cohere, Megakernel sunum sistemini acik kaynak yapti", section
+ *     "Megakernel ne demek": the whole decode pass in a single persistent CUDA
+ *     kernel; work split into a graph of GEMM pieces and attention sections; no
+ *     full-grid synchronisation barriers between operations.
+ *   same page, section "Sinirlar acikca yazilmis": decode only, BF16 only, batch
+ *     1..8, greedy sampling; continuous batching, ragged lengths, paged KV cache,
+ *     sliding-window attention, prefix cache.
+ *   "Kog AI: standart GPU'larda 3,000 token/s", sections on memory bandwidth and on
+ *     the monokernel: decode at low batch is bound by HBM bandwidth; LM-head
+ *     sampling stays on the GPU; prefetch overlaps the non-GEMM sections.
+ *
+ * Conventions
+ *   - Every pointer passed to mk_decode_step and stored in mk_weights is CUDA
+ *     device memory on the handle's device (PyTorch may allocate it). Host
+ *     pointers are accepted only where a comment says "host".
+ *   - All weights are BF16, row-major [out][in] (the nn.Linear convention); MoE
+ *     experts are stacked [E][out][in]. Weights are BORROWED: they must stay
+ *     valid and unchanged for the life of the handle.
+ *   - The KV pool is OWNED by the handle (mk_kv_alloc / mk_kv_free).
+ *   - Everything is asynchronous on the caller's stream (a cudaStream_t passed
+ *     as void*; NULL = the legacy default stream). A handle is not thread-safe,
+ *     and only one mk_decode_step may be in flight per handle at a time (its
+ *     counters and scratch are per handle).
+ *   - Errors found on the host return at once. Errors found on the device (a bad
+ *     page id, a step input out of range, a dependency wait that timed out) are
+ *     latched in a device status word and reported by mk_status_sync; the kernel
+ *     then winds down without faulting the GPU. After such an error, call
+ *     mk_status_reset before the next step.
+ */
+#ifndef MK_H_
+#define MK_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MK_API __attribute__((visibility("default")))
+#else
+#define MK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mk_status {
+    MK_OK = 0,
+    MK_ERR_INVALID_ARG = 1,        /* bad argument (host check) or bad step input (device) */
+    MK_ERR_UNSUPPORTED_DEVICE = 2, /* not an sm_103 GPU, or no cooperative launch */
+    MK_ERR_OOM = 3,                /* device allocation failed / KV pool too large */
+    MK_ERR_LAUNCH = 4,             /* kernel launch refused (e.g. CTAs not co-resident) */
+    MK_ERR_BAD_PAGE = 5,           /* a page-table entry used by the step is out of range */
+    MK_ERR_TIMEOUT = 6,            /* a dependency wait passed its time limit */
+    MK_ERR_INTERNAL = 7,           /* CUDA runtime error or broken invariant */
+    MK_ERR_NO_DEVICE = 8           /* no CUDA device visible */
+} mk_status;
+
+/* Model descriptor (copied by mk_create). */
+typedef struct mk_model_desc {
+    int32_t n_layers;
+    int32_t d_model;        /* multiple of 64 */
+    int32_t n_q_heads;
+    int32_t n_kv_heads;     /* n_q_heads / n_kv_heads <= 8 */
+    int32_t head_dim;       /* 64 or 128 */
+    int32_t ffn_dim;        /* dense SwiGLU width (multiple of 64); unused when n_experts > 0 */
+    int32_t vocab;
+    int32_t n_experts;      /* 0 = dense SwiGLU MLP; else softmax-top-k MoE */
+    int32_t top_k;
+    int32_t expert_ffn_dim; /* multiple of 64 */
+    float rms_eps;          /* RMSNorm epsilon, e.g. 1e-5 */
+    float rope_theta;       /* rotate-half RoPE base, e.g. 1e4 */
+    int32_t sliding_window; /* 0 = none; else a sliding layer attends to the last W keys */
+    const uint8_t *layer_is_sliding; /* host, [n_layers], nonzero = sliding; may be NULL */
+    int32_t max_batch;      /* 1..8 */
+    int32_t page_size;      /* must be 16 */
+    int32_t max_positions;  /* positions[b] must stay below this (RoPE table size) */
+} mk_model_desc;
+
+typedef struct mk_layer_weights {
+    const void *attn_norm;  /* [d] */
+    const void *wq;         /* [n_q_heads*head_dim][d] */
+    const void *wk;         /* [n_kv_heads*head_dim][d] */
+    const void *wv;         /* [n_kv_heads*head_dim][d] */
+    const void *wo;         /* [d][n_q_heads*head_dim] */
+    const void *mlp_norm;   /* [d] */
+    const void *w_gate;     /* dense: [ffn][d] */
+    const void *w_up;       /* dense: [ffn][d] */
+    const void *w_down;     /* dense: [d][ffn] */
+    const void *router;     /* MoE: [E][d] */
+    const void *exp_gate;   /* MoE: [E][expert_ffn][d] */
+    const void *exp_up;     /* MoE: [E][expert_ffn][d] */
+    const void *exp_down;   /* MoE: [E][d][expert_ffn] */
+} mk_layer_weights;
+
+typedef struct mk_weights {
+    const void *embed;      /* [vocab][d] */
+    const void *final_norm; /* [d] */
+    const void *lm_head;    /* [vocab][d] (untied) */
+    const mk_layer_weights *layers; /* host array [n_layers] of device pointers */
+} mk_weights;
+
+typedef struct mk_handle mk_handle;
+
+/* Paged KV pool, BF16, layout [n_layers][num_pages][2 (K=0,V=1)][n_kv_heads][16][head_dim].
+ * Strides are in elements. Page ids are global across layers: page p of layer l
+ * starts at base + l*layer_stride + p*page_stride. K rows are stored after RoPE. */
+typedef struct mk_kv_pool {
+    void *base;             /* device; owned by the handle */
+    int32_t num_pages;
+    int64_t layer_stride, page_stride, kv_stride, head_stride, slot_stride;
+    int64_t bytes;
+} mk_kv_pool;
+
+/* Creates a handle on `device`: checks the GPU (sm_103, cooperative launch),
+ * copies the descriptor, records the weight pointers, uploads the RoPE table
+ * (cos/sin computed on the host in double), and allocates the step scratch
+ * (activations, attention partials, dependency counters, status word).
+ * Returns MK_ERR_INVALID_ARG for an unsupported shape, MK_ERR_NO_DEVICE /
+ * MK_ERR_UNSUPPORTED_DEVICE for the GPU checks, MK_ERR_OOM if scratch cannot be
+ * allocated. On error *out is NULL and nothing is leaked. */
+MK_API mk_status mk_create(const mk_model_desc *desc, const mk_weights *weights, int device,
+                    mk_handle **out);
+
+/* Allocates the handle's paged KV pool of num_pages pages (one pool per handle; a
+ * second call fails with MK_ERR_INVALID_ARG until mk_kv_free). The memory is not
+ * initialised. Returns MK_ERR_OOM if the allocation fails. */
+MK_API mk_status mk_kv_alloc(mk_handle *h, int32_t num_pages, mk_kv_pool *out);
+MK_API mk_status mk_kv_free(mk_handle *h, mk_kv_pool *pool);
+
+/* One decode step for `batch` sequences (1 <= batch <= max_batch), enqueued on
+ * `stream` as a single cooperative kernel launch.
+ *   tokens[batch]       input token of each sequence (0 <= token < vocab)
+ *   positions[batch]    tokens already cached = position of the input token
+ *   page_table[batch][max_pages_per_seq]  entry i = page holding positions
+ *                       [16i, 16i+16); every entry the step reads (the attended
+ *                       range and the page of positions[b]) must be a valid page
+ *   seq_lens[batch]     must equal positions[b] + 1 (keys attended incl. self)
+ *   next_tokens[batch]  out: greedy argmax (lowest index on ties)
+ *   logits              out: [batch][vocab] fp32, or NULL to skip
+ * The step appends K/V of the input token at positions[b] of every layer, then
+ * attends over keys [lo, positions[b]] (lo = 0, or positions[b]-W+1 clamped at 0
+ * on sliding layers). Output buffers must not overlap the inputs. Page ids may
+ * repeat across rows only for read-only shared prefixes (no row may append into
+ * a page another row reads in the same step).
+ * Returns host-side argument errors directly; device-side errors are latched
+ * (see mk_status_sync). */
+MK_API mk_status mk_decode_step(mk_handle *h, const int32_t *tokens, const int32_t *positions,
+                         const int32_t *page_table, int32_t max_pages_per_seq,
+                         const int32_t *seq_lens, int32_t batch, int32_t *next_tokens,
+                         float *logits, void *stream);
+
+/* Waits for `stream`, then reads the device status word. Returns MK_OK or the
+ * latched device error; *failing_task (may be NULL) receives the id of the task
+ * that latched it (layer*16 + stage, or -1). */
+MK_API mk_status mk_status_sync(mk_handle *h, void *stream, int32_t *failing_task);
+
+/* Clears a latched device error and re-zeroes the dependency counters (synchronous). */
+MK_API mk_status mk_status_reset(mk_handle *h);
+
+/* Options (host-side; take effect from the next step):
+ *   MK_OPT_TIMEOUT_NS   limit for every device-side wait, in ns (default 1e9)
+ *   MK_OPT_SKIP_PUBLISH test hook: the task with this id never publishes its
+ *                       completion, so its waiters time out (-1 = off) */
+typedef enum mk_option { MK_OPT_TIMEOUT_NS = 1, MK_OPT_SKIP_PUBLISH = 2 } mk_option;
+MK_API mk_status mk_set_option(mk_handle *h, mk_option opt, int64_t value);
+
+/* Read-only facts about a handle (for schedulers and benchmarks). */
+typedef struct mk_info {
+    int32_t num_ctas;          /* persistent CTAs per launch (one per SM) */
+    int32_t threads_per_cta;
+    int32_t smem_bytes;        /* dynamic shared memory per CTA */
+    int32_t ring_stages;       /* shared-memory ring depth */
+    int64_t weight_bytes;      /* bytes of weights one dense step streams (all layers + head) */
+    int64_t scratch_bytes;     /* device scratch owned by the handle */
+} mk_info;
+MK_API mk_status mk_get_info(const mk_handle *h, mk_info *out);
+
+/* Introspection for stage-by-stage verification. After a step has completed (sync
+ * the stream first), these device buffers hold the activations of the LAST layer the
+ * step ran; they are overwritten by the next step. Layouts (fp32, row b at b*width):
+ *   MK_BUF_X     residual stream after the last layer (input of the final norm),
+ *                [max_batch][d_model], permuted columns (below)
+ *   MK_BUF_QKV   q|k|v projections of the last layer, BEFORE RoPE, natural order,
+ *                [max_batch][(n_q_heads + 2 n_kv_heads) * head_dim]
+ *   MK_BUF_ATTN  attention output of the last layer (input of the O projection),
+ *                [max_batch][n_q_heads * head_dim], permuted columns
+ *   MK_BUF_H     SwiGLU activations of the last layer (input of the down projection),
+ *                [max_batch][ffn_dim], permuted columns
+ * Permuted columns: logical column k is stored at
+ *   (k & ~63) | ((k & 7) >> 1) << 4 | ((k & 63) >> 3) << 1 | (k & 1).
+ * *dev_ptr receives the device address (read-only use), *bytes its size. */
+typedef enum mk_buffer { MK_BUF_X = 1, MK_BUF_QKV = 2, MK_BUF_ATTN = 3, MK_BUF_H = 4 } mk_buffer;
+MK_API mk_status mk_debug_buffer(const mk_handle *h, int32_t which, void **dev_ptr,
+                                 int64_t *bytes);
+
+MK_API const char *mk_status_string(mk_status s);
+
+/* Frees everything the handle owns (scratch, KV pool, RoPE table). Synchronises
+ * the device first. NULL is allowed. */
+MK_API void mk_destroy(mk_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H_ */

@@ -1,0 +1,497 @@
+// mk_api.cu -- host runtime behind include/mk.h: validation, scratch and KV-pool
+// allocation, the KV tensor map, RoPE table, and the cooperative launch of the
+// persistent decode-step kernel (mk_kernel.cuh).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "mk.h"
+#include "mk_kernel.cuh"
+
+using mk::bf16;
+
+struct mk_handle {
+    int device = 0;
+    mk_model_desc desc{};
+    std::vector<uint8_t> sliding;
+    mk::Plan plan{};
+    void* block = nullptr;          // scratch arena
+    size_t block_bytes = 0;
+    mk::LayerPlan* d_layers = nullptr;
+    float* d_gains = nullptr;
+    float2* d_rope = nullptr;
+    void* d_kvmap = nullptr;        // CUtensorMap (128 B, 64-B aligned)
+    void* kv = nullptr;
+    mk_kv_pool pool{};
+    uint32_t epoch = 0;
+    uint32_t attn_total = 0;
+    long long timeout_ns = 1000000000LL;
+    int skip_publish = -1;
+    int num_ctas = 0;
+    int hd = 0;
+    int64_t weight_bytes = 0;
+    size_t counters_words = 0, arrivals_words = 0;
+};
+
+namespace {
+
+struct DeviceGuard {  // restores the caller's current device
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+inline int perm_col_host(int k) {
+    return (k & ~63) | (((k & 7) >> 1) << 4) | (((k & 63) >> 3) << 1) | (k & 1);
+}
+
+mk_status validate_desc(const mk_model_desc* d) {
+    if (!d) return MK_ERR_INVALID_ARG;
+    if (d->n_layers < 1 || d->n_layers > mk::kMaxLayers) return MK_ERR_INVALID_ARG;
+    if (d->d_model < 64 || d->d_model % 64) return MK_ERR_INVALID_ARG;
+    if (d->head_dim != 64 && d->head_dim != 128) return MK_ERR_INVALID_ARG;
+    if (d->n_q_heads < 1 || d->n_kv_heads < 1 || d->n_q_heads % d->n_kv_heads)
+        return MK_ERR_INVALID_ARG;
+    const int G = d->n_q_heads / d->n_kv_heads;
+    if (G > 8 || G * d->head_dim > 512) return MK_ERR_INVALID_ARG;
+    if ((d->n_q_heads * d->head_dim) % 64) return MK_ERR_INVALID_ARG;
+    if (d->vocab < 1) return MK_ERR_INVALID_ARG;
+    if (d->n_experts != 0) return MK_ERR_INVALID_ARG;  // MoE stages: not in this build yet
+    if (d->ffn_dim < 64 || d->ffn_dim % 64) return MK_ERR_INVALID_ARG;
+    if (!(d->rms_eps > 0.f) || !(d->rope_theta > 0.f)) return MK_ERR_INVALID_ARG;
+    if (d->sliding_window < 0) return MK_ERR_INVALID_ARG;
+    if (d->max_batch < 1 || d->max_batch > mk::kMaxBatch) return MK_ERR_INVALID_ARG;
+    if (d->page_size != mk::kPage) return MK_ERR_INVALID_ARG;
+    if (d->max_positions < 1) return MK_ERR_INVALID_ARG;
+    return MK_OK;
+}
+
+mk_status validate_weights(const mk_model_desc* d, const mk_weights* w) {
+    if (!w || !w->embed || !w->final_norm || !w->lm_head || !w->layers) return MK_ERR_INVALID_ARG;
+    for (int l = 0; l < d->n_layers; ++l) {
+        const mk_layer_weights& L = w->layers[l];
+        if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.mlp_norm || !L.w_gate ||
+            !L.w_up || !L.w_down)
+            return MK_ERR_INVALID_ARG;
+    }
+    return MK_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <int HD>
+cudaError_t set_kernel_attrs() {
+    return cudaFuncSetAttribute(mk::decode_step_kernel<HD>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, mk::kSmemBytes);
+}
+
+template <int HD>
+cudaError_t occupancy(int* blocks) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mk::decode_step_kernel<HD>,
+                                                         mk::kThreads, mk::kSmemBytes);
+}
+
+void free_handle(mk_handle* h) {
+    if (!h) return;
+    if (h->kv) cudaFree(h->kv);
+    if (h->d_kvmap) cudaFree(h->d_kvmap);
+    if (h->block) cudaFree(h->block);
+    if (h->d_layers) cudaFree(h->d_layers);
+    if (h->d_gains) cudaFree(h->d_gains);
+    if (h->d_rope) cudaFree(h->d_rope);
+    delete h;
+}
+
+// BF16 gain vector on the device -> fp32, permuted column order, into host vector
+bool fetch_gain(const void* dptr, int d, float* out) {
+    std::vector<uint16_t> tmp(d);
+    if (cudaMemcpy(tmp.data(), dptr, sizeof(uint16_t) * d, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return false;
+    for (int k = 0; k < d; ++k) {
+        uint32_t u = (uint32_t)tmp[k] << 16;
+        float f;
+        std::memcpy(&f, &u, 4);
+        out[perm_col_host(k)] = f;
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mk_status_string(mk_status s) {
+    switch (s) {
+        case MK_OK: return "ok";
+        case MK_ERR_INVALID_ARG: return "invalid argument";
+        case MK_ERR_UNSUPPORTED_DEVICE: return "unsupported device (need sm_103 with cooperative launch)";
+        case MK_ERR_OOM: return "out of device memory";
+        case MK_ERR_LAUNCH: return "kernel launch failed";
+        case MK_ERR_BAD_PAGE: return "page-table entry out of range";
+        case MK_ERR_TIMEOUT: return "device-side dependency wait timed out";
+        case MK_ERR_INTERNAL: return "internal / CUDA runtime error";
+        case MK_ERR_NO_DEVICE: return "no CUDA device";
+    }
+    return "unknown status";
+}
+
+mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int device,
+                    mk_handle** out) {
+    if (!out) return MK_ERR_INVALID_ARG;
+    *out = nullptr;
+    mk_status st = validate_desc(desc);
+    if (st != MK_OK) return st;
+    st = validate_weights(desc, weights);
+    if (st != MK_OK) return st;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+        cudaGetLastError();
+        return MK_ERR_NO_DEVICE;
+    }
+    if (device < 0 || device >= ndev) return MK_ERR_INVALID_ARG;
+    DeviceGuard guard(device);
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MK_ERR_INTERNAL;
+    if (prop.major != 10 || prop.minor != 3 || !prop.cooperativeLaunch)
+        return MK_ERR_UNSUPPORTED_DEVICE;
+    const int hd = desc->head_dim;
+    int blocks = 0;
+    cudaError_t e = hd == 128 ? set_kernel_attrs<128>() : set_kernel_attrs<64>();
+    if (e == cudaSuccess) e = hd == 128 ? occupancy<128>(&blocks) : occupancy<64>(&blocks);
+    if (e != cudaSuccess || blocks < 1) {
+        cudaGetLastError();
+        return MK_ERR_UNSUPPORTED_DEVICE;
+    }
+
+    mk_handle* h = new (std::nothrow) mk_handle();
+    if (!h) return MK_ERR_OOM;
+    h->device = device;
+    h->desc = *desc;
+    h->sliding.assign(desc->n_layers, 0);
+    if (desc->layer_is_sliding)
+        for (int l = 0; l < desc->n_layers; ++l) h->sliding[l] = desc->layer_is_sliding[l] ? 1 : 0;
+    h->desc.layer_is_sliding = nullptr;
+    h->num_ctas = prop.multiProcessorCount;
+    h->hd = hd;
+
+    const int L = desc->n_layers, d = desc->d_model, Hq = desc->n_q_heads, Hkv = desc->n_kv_heads;
+    const int G = Hq / Hkv, F = desc->ffn_dim, V = desc->vocab, maxB = desc->max_batch;
+    const int C = h->num_ctas;
+    const int qkv_rows = (Hq + 2 * Hkv) * hd;
+
+    // ---- scratch arena
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t o_x = take(sizeof(float) * maxB * d);
+    const size_t o_qkv = take(sizeof(float) * maxB * qkv_rows);
+    const size_t o_attn = take(sizeof(float) * maxB * Hq * hd);
+    const size_t o_h = take(sizeof(float) * maxB * F);
+    const size_t o_po = take(sizeof(float) * (size_t)maxB * Hkv * C * G * hd);
+    const size_t o_pml = take(sizeof(float2) * (size_t)maxB * Hkv * C * G);
+    const size_t o_am = take(sizeof(float2) * (size_t)C * maxB);
+    h->counters_words = (size_t)(2 + L * mk::kStagesPerLayer) * mk::kCounterStride;
+    h->arrivals_words = (size_t)(L * maxB * Hkv + 1) * mk::kCounterStride;
+    const size_t o_cnt = take(sizeof(uint32_t) * h->counters_words);
+    const size_t o_arr = take(sizeof(uint32_t) * h->arrivals_words);
+    const size_t o_status = take(sizeof(int) * 4);
+    h->block_bytes = off;
+    if (cudaMalloc(&h->block, h->block_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        free_handle(h);
+        return MK_ERR_OOM;
+    }
+    uint8_t* base = static_cast<uint8_t*>(h->block);
+    if (cudaMemset(h->block, 0, h->block_bytes) != cudaSuccess) { free_handle(h); return MK_ERR_INTERNAL; }
+
+    // ---- norm gains (fp32, permuted), RoPE table, layer table
+    std::vector<float> gains((size_t)(2 * L + 1) * d);
+    for (int l = 0; l < L; ++l) {
+        if (!fetch_gain(weights->layers[l].attn_norm, d, &gains[(size_t)(2 * l) * d]) ||
+            !fetch_gain(weights->layers[l].mlp_norm, d, &gains[(size_t)(2 * l + 1) * d])) {
+            cudaGetLastError();
+            free_handle(h);
+            return MK_ERR_INVALID_ARG;
+        }
+    }
+    if (!fetch_gain(weights->final_norm, d, &gains[(size_t)(2 * L) * d])) {
+        cudaGetLastError();
+        free_handle(h);
+        return MK_ERR_INVALID_ARG;
+    }
+    const int half = hd / 2;
+    std::vector<float2> rope((size_t)desc->max_positions * half);
+    for (int pos = 0; pos < desc->max_positions; ++pos)
+        for (int i = 0; i < half; ++i) {
+            const double inv_freq = std::pow((double)desc->rope_theta, -2.0 * i / (double)hd);
+            const double ang = (double)pos * inv_freq;
+            rope[(size_t)pos * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+    if (cudaMalloc(&h->d_gains, sizeof(float) * gains.size()) != cudaSuccess ||
+        cudaMalloc(&h->d_rope, sizeof(float2) * rope.size()) != cudaSuccess ||
+        cudaMalloc(&h->d_layers, sizeof(mk::LayerPlan) * L) != cudaSuccess) {
+        cudaGetLastError();
+        free_handle(h);
+        return MK_ERR_OOM;
+    }
+    std::vector<mk::LayerPlan> lp(L);
+    int64_t wbytes = 0;
+    for (int l = 0; l < L; ++l) {
+        const mk_layer_weights& W = weights->layers[l];
+        lp[l].wq = (const bf16*)W.wq; lp[l].wk = (const bf16*)W.wk; lp[l].wv = (const bf16*)W.wv;
+        lp[l].wo = (const bf16*)W.wo; lp[l].w_gate = (const bf16*)W.w_gate;
+        lp[l].w_up = (const bf16*)W.w_up; lp[l].w_down = (const bf16*)W.w_down;
+        lp[l].attn_gain = h->d_gains + (size_t)(2 * l) * d;
+        lp[l].mlp_gain = h->d_gains + (size_t)(2 * l + 1) * d;
+        lp[l].sliding = h->sliding[l];
+        wbytes += 2LL * ((int64_t)qkv_rows * d + (int64_t)d * Hq * hd + 3LL * F * d + 2LL * d);
+    }
+    wbytes += 2LL * ((int64_t)V * d + d);
+    h->weight_bytes = wbytes;
+    if (cudaMemcpy(h->d_gains, gains.data(), sizeof(float) * gains.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(h->d_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(h->d_layers, lp.data(), sizeof(mk::LayerPlan) * L, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        free_handle(h);
+        return MK_ERR_INTERNAL;
+    }
+
+    mk::Plan& p = h->plan;
+    p.L = L; p.d = d; p.Hq = Hq; p.Hkv = Hkv; p.hd = hd; p.G = G; p.F = F; p.V = V;
+    p.window = desc->sliding_window; p.max_pos = desc->max_positions; p.maxB = maxB;
+    p.num_pages = 0;
+    p.eps = desc->rms_eps;
+    p.scale = (float)(1.0 / std::sqrt((double)hd));
+    p.C = C;
+    p.qkv_rows = qkv_rows;
+    p.layers = h->d_layers;
+    p.embed = (const bf16*)weights->embed;
+    p.lm_head = (const bf16*)weights->lm_head;
+    p.final_gain = h->d_gains + (size_t)(2 * L) * d;
+    p.rope = h->d_rope;
+    p.x = (float*)(base + o_x);
+    p.qkv = (float*)(base + o_qkv);
+    p.attn = (float*)(base + o_attn);
+    p.h = (float*)(base + o_h);
+    p.part_o = (float*)(base + o_po);
+    p.part_ml = (float2*)(base + o_pml);
+    p.amax_part = (float2*)(base + o_am);
+    p.counters = (uint32_t*)(base + o_cnt);
+    p.arrivals = (uint32_t*)(base + o_arr);
+    p.status = (int*)(base + o_status);
+    p.kv = nullptr;
+    p.kv_map = nullptr;
+    *out = h;
+    return MK_OK;
+}
+
+mk_status mk_kv_alloc(mk_handle* h, int32_t num_pages, mk_kv_pool* out) {
+    if (!h || !out || num_pages < 1) return MK_ERR_INVALID_ARG;
+    if (h->kv) return MK_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    const mk_model_desc& d = h->desc;
+    const int64_t rows = (int64_t)d.n_layers * num_pages * 2 * d.n_kv_heads * mk::kPage;
+    if (rows >= (1LL << 31)) return MK_ERR_OOM;
+    const int64_t elems = rows * h->hd;
+    const int64_t bytes = elems * 2;
+    if (cudaMalloc(&h->kv, (size_t)bytes) != cudaSuccess) {
+        cudaGetLastError();
+        h->kv = nullptr;
+        return MK_ERR_OOM;
+    }
+    // tensor map: the pool as a 2D [rows][head_dim] BF16 tensor, box 64 x 16, 128B swizzle
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void**)&encode, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !encode) {
+        cudaGetLastError();
+        cudaFree(h->kv);
+        h->kv = nullptr;
+        return MK_ERR_INTERNAL;
+    }
+    CUtensorMap map;
+    cuuint64_t gdim[2] = {(cuuint64_t)h->hd, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)h->hd * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)mk::kPage};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->kv, gdim, gstride, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        cudaFree(h->kv);
+        h->kv = nullptr;
+        return MK_ERR_INTERNAL;
+    }
+    if (!h->d_kvmap && cudaMalloc(&h->d_kvmap, sizeof(CUtensorMap)) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->kv);
+        h->kv = nullptr;
+        return MK_ERR_OOM;
+    }
+    if (cudaMemcpy(h->d_kvmap, &map, sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->kv);
+        h->kv = nullptr;
+        return MK_ERR_INTERNAL;
+    }
+    h->plan.kv = (bf16*)h->kv;
+    h->plan.num_pages = num_pages;
+    h->plan.kv_map = h->d_kvmap;
+    mk_kv_pool& P = h->pool;
+    P.base = h->kv;
+    P.num_pages = num_pages;
+    P.slot_stride = h->hd;
+    P.head_stride = (int64_t)mk::kPage * h->hd;
+    P.kv_stride = P.head_stride * d.n_kv_heads;
+    P.page_stride = 2 * P.kv_stride;
+    P.layer_stride = P.page_stride * num_pages;
+    P.bytes = bytes;
+    *out = P;
+    return MK_OK;
+}
+
+mk_status mk_kv_free(mk_handle* h, mk_kv_pool* pool) {
+    if (!h || !h->kv) return MK_ERR_INVALID_ARG;
+    if (pool && pool->base != h->kv) return MK_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    cudaDeviceSynchronize();
+    cudaFree(h->kv);
+    h->kv = nullptr;
+    h->plan.kv = nullptr;
+    h->plan.num_pages = 0;
+    h->pool = mk_kv_pool{};
+    if (pool) *pool = mk_kv_pool{};
+    return MK_OK;
+}
+
+mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* positions,
+                         const int32_t* page_table, int32_t max_pages_per_seq,
+                         const int32_t* seq_lens, int32_t batch, int32_t* next_tokens,
+                         float* logits, void* stream) {
+    if (!h || !tokens || !positions || !page_table || !seq_lens || !next_tokens)
+        return MK_ERR_INVALID_ARG;
+    if (batch < 1 || batch > h->desc.max_batch || max_pages_per_seq < 1) return MK_ERR_INVALID_ARG;
+    if (!h->kv) return MK_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    mk::StepArgs a;
+    a.p = h->plan;
+    a.tokens = tokens;
+    a.positions = positions;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.next_tokens = next_tokens;
+    a.logits = logits;
+    a.max_pages = max_pages_per_seq;
+    a.B = batch;
+    const uint32_t epoch = h->epoch + 1;
+    const uint32_t attn_total = h->attn_total + (uint32_t)batch * (uint32_t)h->desc.n_kv_heads;
+    a.stage_target = epoch * (uint32_t)h->num_ctas;
+    a.embed_target = a.stage_target;
+    a.attn_target = attn_total;
+    a.skip_publish = h->skip_publish;
+    a.timeout_ns = h->timeout_ns;
+    void* args[] = {&a};
+    const void* fn = h->hd == 128 ? (const void*)mk::decode_step_kernel<128>
+                                  : (const void*)mk::decode_step_kernel<64>;
+    cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(h->num_ctas), dim3(mk::kThreads), args,
+                                                mk::kSmemBytes, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_LAUNCH;
+    }
+    h->epoch = epoch;
+    h->attn_total = attn_total;
+    return MK_OK;
+}
+
+mk_status mk_status_sync(mk_handle* h, void* stream, int32_t* failing_task) {
+    if (!h) return MK_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_INTERNAL;
+    }
+    int st[2] = {0, -1};
+    if (cudaMemcpy(st, h->plan.status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_INTERNAL;
+    }
+    if (failing_task) *failing_task = st[0] ? st[1] : -1;
+    return (mk_status)st[0];
+}
+
+mk_status mk_status_reset(mk_handle* h) {
+    if (!h) return MK_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_INTERNAL;
+    }
+    if (cudaMemset(h->plan.counters, 0, sizeof(uint32_t) * h->counters_words) != cudaSuccess ||
+        cudaMemset(h->plan.arrivals, 0, sizeof(uint32_t) * h->arrivals_words) != cudaSuccess ||
+        cudaMemset(h->plan.status, 0, sizeof(int) * 4) != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_INTERNAL;
+    }
+    h->epoch = 0;
+    h->attn_total = 0;
+    return MK_OK;
+}
+
+mk_status mk_set_option(mk_handle* h, mk_option opt, int64_t value) {
+    if (!h) return MK_ERR_INVALID_ARG;
+    switch (opt) {
+        case MK_OPT_TIMEOUT_NS:
+            if (value < 1000) return MK_ERR_INVALID_ARG;
+            h->timeout_ns = value;
+            return MK_OK;
+        case MK_OPT_SKIP_PUBLISH:
+            h->skip_publish = (int)value;
+            return MK_OK;
+    }
+    return MK_ERR_INVALID_ARG;
+}
+
+mk_status mk_get_info(const mk_handle* h, mk_info* out) {
+    if (!h || !out) return MK_ERR_INVALID_ARG;
+    out->num_ctas = h->num_ctas;
+    out->threads_per_cta = mk::kThreads;
+    out->smem_bytes = mk::kSmemBytes;
+    out->ring_stages = mk::kStages;
+    out->weight_bytes = h->weight_bytes;
+    out->scratch_bytes = (int64_t)h->block_bytes;
+    return MK_OK;
+}
+
+mk_status mk_debug_buffer(const mk_handle* h, int32_t which, void** dev_ptr, int64_t* bytes) {
+    if (!h || !dev_ptr || !bytes) return MK_ERR_INVALID_ARG;
+    const mk::Plan& p = h->plan;
+    const int64_t B = p.maxB;
+    switch (which) {
+        case MK_BUF_X: *dev_ptr = p.x; *bytes = 4 * B * p.d; return MK_OK;
+        case MK_BUF_QKV: *dev_ptr = p.qkv; *bytes = 4 * B * p.qkv_rows; return MK_OK;
+        case MK_BUF_ATTN: *dev_ptr = p.attn; *bytes = 4 * B * p.Hq * p.hd; return MK_OK;
+        case MK_BUF_H: *dev_ptr = p.h; *bytes = 4 * B * p.F; return MK_OK;
+    }
+    return MK_ERR_INVALID_ARG;
+}
+
+void mk_destroy(mk_handle* h) {
+    if (!h) return;
+    DeviceGuard guard(h->device);
+    cudaDeviceSynchronize();
+    free_handle(h);
+}
+
+}  // extern "C"

@@ -1,0 +1,1029 @@
+// mk_kernel.cuh -- the persistent decode-step kernel (one launch = one decode step).
+//
+// Design (pages: "Cohere Megakernel", section "Megakernel ne demek"; "Kog Inference
+// Engine", sections on memory bandwidth and the monokernel):
+//   * one CTA per SM, launched cooperatively so every CTA is resident;
+//   * the step is a fixed list of stages per layer -- QKV tiles, attention key
+//     splits (+ last-arriver merge), O-projection tiles, gate/up tiles, down tiles --
+//     then LM-head tiles and the greedy argmax. Each stage's work is cut into row
+//     tiles (GEMV) or page ranges (attention) that are statically assigned to CTAs;
+//   * stages are ordered by per-stage dependency counters (gpu-scope release/acquire)
+//     and per-(sequence, kv-head) arrival counters, never by a grid-wide barrier;
+//   * warp 0 of every CTA is a TMA producer: it walks the CTA's own task list and
+//     streams every weight row and every KV page the CTA will need into a ring of
+//     shared-memory slots, without waiting on any dependency (weights and old KV rows
+//     never depend on this step's activations), so HBM keeps streaming while the
+//     consumer warps wait on counters;
+//   * warps 1..8 consume: BF16 mma.sync GEMV tiles (weights as the 16-row A operand,
+//     the <= 8 batch rows as the 8-column B operand), flash-decode attention with
+//     online softmax, fused epilogues (RoPE + KV append, residual add, SwiGLU,
+//     partial argmax).
+// Every wait is bounded; on an error the kernel latches a status word and winds down
+// (waits become no-ops, in-flight TMA copies are drained) instead of hanging.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include "mk_ptx.cuh"
+
+namespace mk {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kThreads = 32 + kConsumerThreads;   // warp 0 = producer
+constexpr int kStages = 6;                         // shared-memory ring depth
+constexpr int KC = 1024;                           // GEMV k-chunk (columns per ring slot)
+constexpr int kRowPitch = KC * 2 + 16;             // padded row pitch: conflict-free ldmatrix
+constexpr int kSlotBytes = 33 * 1024;              // >= 16 * kRowPitch, multiple of 1024
+constexpr int kScratchBytes = 20 * 1024;
+constexpr int kMaxBatch = 8;
+constexpr int kPage = 16;
+constexpr int kTaskRows = 128;                     // <= 8 row groups of 16 per GEMV task
+constexpr int kMaxLayers = 128;
+constexpr int kCounterStride = 32;                 // u32 words per counter (128 B apart)
+constexpr int kStagesPerLayer = 8;                 // counter slots per layer
+
+// error codes (same values as mk_status)
+constexpr int kErrInvalid = 1, kErrBadPage = 5, kErrTimeout = 6, kErrInternal = 7;
+
+// stage ids (task id = layer * 16 + stage id)
+enum StageId { ST_QKV = 0, ST_ATTN = 1, ST_O = 2, ST_GU = 3, ST_DOWN = 4 };
+enum GemvKind { G_QKV = 0, G_O = 1, G_GU = 2, G_DOWN = 3, G_LM = 4 };
+
+struct LayerPlan {
+    const bf16 *wq, *wk, *wv, *wo, *w_gate, *w_up, *w_down;
+    const float *attn_gain, *mlp_gain;  // fp32, permuted column order
+    int sliding;
+    int pad_;
+};
+
+struct Plan {
+    int L, d, Hq, Hkv, hd, G, F, V, window, max_pos, maxB, num_pages;
+    float eps, scale;                   // scale = 1/sqrt(hd)
+    int C;                              // CTAs in the launch
+    int qkv_rows;                       // (Hq + 2 Hkv) * hd
+    const LayerPlan* layers;            // [L]
+    const bf16* embed;
+    const bf16* lm_head;
+    const float* final_gain;            // fp32, permuted
+    const float2* rope;                 // [max_pos][hd/2] (cos, sin)
+    float* x;                           // [maxB][d]  residual stream, permuted
+    float* qkv;                         // [maxB][qkv_rows] natural order, pre-RoPE
+    float* attn;                        // [maxB][Hq*hd] permuted
+    float* h;                           // [maxB][F] permuted
+    float* part_o;                      // [maxB*Hkv][C][G][hd]
+    float2* part_ml;                    // [maxB*Hkv][C][G] (m, l)
+    float2* amax_part;                  // [C][maxB] (value, index as float bits)
+    uint32_t* counters;                 // stage counters, kCounterStride apart
+    uint32_t* arrivals;                 // [L][maxB*Hkv] + 1 (argmax), kCounterStride apart
+    int* status;                        // [0] code, [1] task
+    bf16* kv;                           // paged pool base
+    const void* kv_map;                 // CUtensorMap of the pool as [rows][hd], 128B swizzle
+};
+
+struct StepArgs {
+    Plan p;
+    const int* tokens;
+    const int* positions;
+    const int* page_table;
+    const int* seq_lens;
+    int* next_tokens;
+    float* logits;                      // may be null
+    int max_pages;
+    int B;
+    uint32_t stage_target;              // epoch * C
+    uint32_t attn_target;               // cumulative (sum of batch sizes) * Hkv
+    uint32_t embed_target;              // epoch * C
+    int skip_publish;                   // task id whose publish is suppressed, or -1
+    long long timeout_ns;
+};
+
+// counter slots
+__device__ __forceinline__ int cnt_embed() { return 0; }
+__device__ __forceinline__ int cnt_stage(int l, int s) { return 1 + l * kStagesPerLayer + s; }
+__device__ __forceinline__ int cnt_lm(int L) { return 1 + L * kStagesPerLayer; }
+
+// column permutation of fp32 activation rows: within each 64-column block, thread t of
+// an mma quad finds its 16 B-operand values (8 column pairs) in 4 consecutive float4s
+__device__ __forceinline__ int perm_col(int k) {
+    return (k & ~63) | (((k & 7) >> 1) << 4) | (((k & 63) >> 3) << 1) | (k & 1);
+}
+
+struct Smem {
+    float rstd[kMaxBatch];
+    float amax_v[kMaxBatch];
+    int amax_i[kMaxBatch];
+    int pos[kMaxBatch];
+    volatile int abort;
+    int bcast;
+    int pad_[6];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    __align__(16) bf16 knew[128];
+    __align__(16) bf16 vnew[128];
+};
+
+constexpr int kSmemBytes = 1024 + kStages * kSlotBytes + kScratchBytes + (int)sizeof(Smem);
+
+struct Ctx {
+    const StepArgs* a;
+    Smem* sm;
+    uint8_t* ring;       // generic pointer, 1024-aligned
+    float* scratch;
+    uint32_t ring_s;     // shared address of the ring
+    uint32_t seq;        // ring sequence number (slot = seq % kStages)
+    int cw, lane, tid;   // consumer warp (0..7), lane, consumer thread id (0..255)
+};
+
+// ------------------------------------------------------------------ errors / waits
+__device__ __forceinline__ void set_error(const Plan& p, Smem* sm, int code, int task) {
+    if (atomicCAS(p.status, 0, code) == 0) p.status[1] = task;
+    sm->abort = 1;
+}
+
+__device__ __forceinline__ bool status_bad(const Plan& p) { return ld_volatile_int(p.status) != 0; }
+
+// wait until counter - target >= 0 (wrapping u32); one thread; false on abort/timeout
+__device__ bool poll_counter(const StepArgs& a, Smem* sm, const uint32_t* c, uint32_t target,
+                             int task) {
+    if (sm->abort) return false;
+    uint64_t t0 = 0;
+    for (int it = 0;; ++it) {
+        uint32_t v = ld_acquire(c);
+        if ((int)(v - target) >= 0) return true;
+        if (sm->abort) return false;
+        if ((it & 7) == 7) {
+            if (status_bad(a.p)) { sm->abort = 1; return false; }
+            uint64_t t = globaltimer();
+            if (t0 == 0) t0 = t;
+            else if ((long long)(t - t0) > a.timeout_ns) {
+                set_error(a.p, sm, kErrTimeout, task);
+                return false;
+            }
+        }
+        if (it > 32) __nanosleep(64);
+    }
+}
+
+// all consumer threads: wait for a stage counter
+__device__ bool consumer_wait(Ctx& c, int slot, uint32_t target, int task) {
+    if (c.tid == 0) poll_counter(*c.a, c.sm, c.a->p.counters + slot * kCounterStride, target, task);
+    consumer_sync();
+    return !c.sm->abort;
+}
+
+__device__ void publish(Ctx& c, int slot, int task) {
+    consumer_sync();
+    if (c.tid == 0 && !c.sm->abort && c.a->skip_publish != task) {
+        __threadfence();
+        red_release_add(c.a->p.counters + slot * kCounterStride, 1u);
+    }
+}
+
+// a consumer warp waits for ring slot `seq` to be full; warp-uniform result
+__device__ bool wait_full(Ctx& c, int task) {
+    const uint32_t slot = c.seq % kStages, parity = (c.seq / kStages) & 1;
+    const uint32_t bar = smem_u32(&c.sm->full[slot]);
+    int ok = 1;
+    if (c.lane == 0) {
+        if (c.sm->abort) ok = 0;
+        else if (!mbar_try_wait(bar, parity)) {
+            uint64_t t0 = globaltimer();
+            for (int it = 0;; ++it) {
+                if (mbar_try_wait(bar, parity)) break;
+                if (c.sm->abort) { ok = 0; break; }
+                if ((it & 7) == 7) {
+                    if (status_bad(c.a->p)) { c.sm->abort = 1; ok = 0; break; }
+                    if ((long long)(globaltimer() - t0) > c.a->timeout_ns) {
+                        set_error(c.a->p, c.sm, kErrTimeout, task);
+                        ok = 0;
+                        break;
+                    }
+                }
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_try_wait(bar, parity);  // every lane acquires the completed phase
+    return ok != 0;
+}
+
+__device__ __forceinline__ void release_slot(Ctx& c) {
+    __syncwarp();
+    if (c.lane == 0 && !c.sm->abort) mbar_arrive(smem_u32(&c.sm->empty[c.seq % kStages]));
+    c.seq++;
+}
+
+// ------------------------------------------------------------------ schedule
+__device__ __forceinline__ void cta_rows(int R, int cta, int C, int& r0, int& r1) {
+    r0 = (int)((long long)cta * R / C);
+    r1 = (int)((long long)(cta + 1) * R / C);
+}
+
+struct GemvStage {
+    int kind, layer, R, K, task_id, cnt_wait, cnt_pub;
+    uint32_t wait_target;
+    const bf16 *w0, *w1, *w2;
+    int split1, split2;          // QKV: row boundaries between wq / wk / wv
+    const float* src;            // B operand source rows [b][K], permuted
+    const float* gain;           // permuted fp32 gain or null (no norm)
+};
+
+__device__ GemvStage make_gemv(const StepArgs& a, int kind, int l) {
+    const Plan& p = a.p;
+    GemvStage s;
+    s.kind = kind;
+    s.layer = l;
+    s.w1 = s.w2 = nullptr;
+    s.split1 = s.split2 = 0;
+    s.gain = nullptr;
+    s.wait_target = a.stage_target;
+    if (kind == G_LM) {
+        s.R = p.V; s.K = p.d; s.w0 = p.lm_head; s.src = p.x; s.gain = p.final_gain;
+        s.task_id = p.L * 16; s.cnt_wait = cnt_stage(p.L - 1, ST_DOWN); s.cnt_pub = cnt_lm(p.L);
+        return s;
+    }
+    const LayerPlan& lp = p.layers[l];
+    switch (kind) {
+        case G_QKV:
+            s.R = p.qkv_rows; s.K = p.d; s.w0 = lp.wq; s.w1 = lp.wk; s.w2 = lp.wv;
+            s.split1 = p.Hq * p.hd; s.split2 = (p.Hq + p.Hkv) * p.hd;
+            s.src = p.x; s.gain = lp.attn_gain; s.task_id = l * 16 + ST_QKV;
+            s.cnt_wait = l == 0 ? cnt_embed() : cnt_stage(l - 1, ST_DOWN);
+            if (l == 0) s.wait_target = a.embed_target;
+            s.cnt_pub = cnt_stage(l, ST_QKV);
+            break;
+        case G_O:
+            s.R = p.d; s.K = p.Hq * p.hd; s.w0 = lp.wo; s.src = p.attn;
+            s.task_id = l * 16 + ST_O; s.cnt_wait = cnt_stage(l, ST_ATTN);
+            s.wait_target = a.attn_target; s.cnt_pub = cnt_stage(l, ST_O);
+            break;
+        case G_GU:
+            s.R = p.F; s.K = p.d; s.w0 = lp.w_gate; s.w1 = lp.w_up; s.src = p.x;
+            s.gain = lp.mlp_gain; s.task_id = l * 16 + ST_GU; s.cnt_wait = cnt_stage(l, ST_O);
+            s.cnt_pub = cnt_stage(l, ST_GU);
+            break;
+        default:  // G_DOWN
+            s.R = p.d; s.K = p.F; s.w0 = lp.w_down; s.src = p.h;
+            s.task_id = l * 16 + ST_DOWN; s.cnt_wait = cnt_stage(l, ST_GU);
+            s.cnt_pub = cnt_stage(l, ST_DOWN);
+            break;
+    }
+    return s;
+}
+
+// rows per task: GU tasks count gate/up row PAIRS (<= 64 pairs = 8 row groups)
+__device__ __forceinline__ int task_rows(int kind) { return kind == G_GU ? kTaskRows / 2 : kTaskRows; }
+
+// weight row `r` of row group `rg` (GU: groups [0, ng/2) are gate, the rest up)
+__device__ __forceinline__ const bf16* gemv_row(const GemvStage& s, int r0, int rg, int ng, int i) {
+    if (s.kind == G_GU) {
+        const int half = ng >> 1;
+        const bool up = rg >= half;
+        const int r = r0 + 16 * (up ? rg - half : rg) + i;
+        return (up ? s.w1 : s.w0) + (size_t)r * s.K;
+    }
+    const int r = r0 + 16 * rg + i;
+    if (s.kind == G_QKV) {
+        if (r < s.split1) return s.w0 + (size_t)r * s.K;
+        if (r < s.split2) return s.w1 + (size_t)(r - s.split1) * s.K;
+        return s.w2 + (size_t)(r - s.split2) * s.K;
+    }
+    return s.w0 + (size_t)r * s.K;
+}
+__device__ __forceinline__ int group_rows(const GemvStage& s, int r0, int r1, int rg, int ng) {
+    const int n = r1 - r0;
+    const int base = 16 * (s.kind == G_GU ? (rg % (ng >> 1)) : rg);
+    return min(16, n - base);
+}
+__device__ __forceinline__ int num_groups(const GemvStage& s, int n) {
+    const int g = (n + 15) >> 4;
+    return s.kind == G_GU ? 2 * g : g;
+}
+
+// ---- attention work partition (identical in producer and consumers) ----
+struct SeqSpan { int lo, pos, p0, np; };  // attended keys [lo, pos], logical pages [p0, p0+np)
+
+__device__ __forceinline__ SeqSpan seq_span(const Plan& p, const Smem* sm, int l, int b) {
+    SeqSpan s;
+    s.pos = sm->pos[b];
+    s.lo = (p.window > 0 && p.layers[l].sliding) ? max(0, s.pos - p.window + 1) : 0;
+    s.p0 = s.lo / kPage;
+    s.np = s.pos / kPage - s.p0 + 1;
+    return s;
+}
+
+// Calls f(b, g, first unit in this bg, count, split, nsplit) for each piece of this CTA.
+// Units are (b, g, page) triples in order; CTA c owns [c U / C, (c+1) U / C) (or unit c
+// when U < C). A piece is this CTA's share of one (b, g); its split index is its rank
+// among the CTAs that share that (b, g).
+template <typename F>
+__device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta, F&& f) {
+    const Plan& p = a.p;
+    long long U = 0;
+    for (int b = 0; b < a.B; ++b) U += (long long)p.Hkv * seq_span(p, sm, l, b).np;
+    const int C = p.C;
+    long long u0, u1;
+    if (U >= C) { u0 = (long long)cta * U / C; u1 = (long long)(cta + 1) * U / C; }
+    else { u0 = cta; u1 = cta < U ? cta + 1 : cta; }
+    if (u0 >= u1) return;
+    auto first_cta = [&](long long s) -> int {
+        return U >= C ? (int)(((s + 1) * C - 1) / U) : (int)s;
+    };
+    long long s = 0;
+    for (int b = 0; b < a.B; ++b) {
+        const SeqSpan sp = seq_span(p, sm, l, b);
+        for (int g = 0; g < p.Hkv; ++g) {
+            const long long e = s + sp.np;
+            const long long lo = max(s, u0), hi = min(e, u1);
+            if (lo < hi) {
+                const int c0 = first_cta(s);
+                const int nsplit = first_cta(e - 1) - c0 + 1;
+                f(b, g, sp, (int)(lo - s), (int)(hi - lo), cta - c0, nsplit);
+            }
+            s = e;
+            if (s >= u1) return;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ producer (1 thread)
+struct Producer {
+    const StepArgs* a;
+    Smem* sm;
+    uint32_t ring_s;
+    uint32_t seq = 0;
+    uint64_t policy;
+
+    __device__ bool acquire_slot(int task) {
+        if (sm->abort) return false;
+        if (seq >= (uint32_t)kStages) {
+            const uint32_t bar = smem_u32(&sm->empty[seq % kStages]);
+            const uint32_t parity = ((seq / kStages) - 1) & 1;
+            if (!mbar_try_wait(bar, parity)) {
+                uint64_t t0 = globaltimer();
+                for (int it = 0;; ++it) {
+                    if (mbar_try_wait(bar, parity)) break;
+                    if (sm->abort) return false;
+                    if ((it & 7) == 7) {
+                        if (status_bad(a->p)) { sm->abort = 1; return false; }
+                        if ((long long)(globaltimer() - t0) > a->timeout_ns) {
+                            set_error(a->p, sm, kErrTimeout, task);
+                            return false;
+                        }
+                    }
+                }
+            }
+        }
+        return true;
+    }
+    __device__ uint32_t slot_addr() const { return ring_s + (seq % kStages) * kSlotBytes; }
+    __device__ uint32_t full_bar() const { return smem_u32(&sm->full[seq % kStages]); }
+
+    __device__ bool gemv(const GemvStage& s, int cta) {
+        int a0, a1;
+        cta_rows(s.R, cta, a->p.C, a0, a1);
+        const int tr = task_rows(s.kind);
+        for (int r0 = a0; r0 < a1; r0 += tr) {
+            const int r1 = min(a1, r0 + tr);
+            const int ng = num_groups(s, r1 - r0);
+            for (int k0 = 0; k0 < s.K; k0 += KC) {
+                const int kc = min(KC, s.K - k0);
+                for (int rg = 0; rg < ng; ++rg) {
+                    if (!acquire_slot(s.task_id)) return false;
+                    const int nr = group_rows(s, r0, r1, rg, ng);
+                    const uint32_t dst = slot_addr(), bar = full_bar();
+                    mbar_arrive_expect_tx(bar, (uint32_t)(nr * kc * 2));
+                    for (int i = 0; i < nr; ++i)
+                        tma_load_1d(dst + i * kRowPitch, gemv_row(s, r0, rg, ng, i) + k0,
+                                    (uint32_t)(kc * 2), bar, policy);
+                    ++seq;
+                }
+            }
+        }
+        return true;
+    }
+
+    template <int HD>
+    __device__ bool attention(int l, int cta) {
+        const Plan& p = a->p;
+        constexpr int PPS = 512 / HD;  // pages per ring slot (K + V of one kv head)
+        bool ok = true;
+        for_each_piece(*a, sm, l, cta, [&](int b, int g, const SeqSpan& sp, int u, int n,
+                                           int split, int nsplit) {
+            if (!ok) return;
+            const int* pt = a->page_table + (size_t)b * a->max_pages;
+            for (int st = 0; st < n; st += PPS) {
+                const int np = min(PPS, n - st);
+                if (!acquire_slot(l * 16 + ST_ATTN)) { ok = false; return; }
+                int pages[PPS];
+                for (int i = 0; i < np; ++i) {
+                    pages[i] = __ldg(pt + sp.p0 + u + st + i);
+                    if (pages[i] < 0 || pages[i] >= p.num_pages) {
+                        set_error(p, sm, kErrBadPage, l * 16 + ST_ATTN);
+                        ok = false;
+                        return;
+                    }
+                }
+                const uint32_t dst = slot_addr(), bar = full_bar();
+                mbar_arrive_expect_tx(bar, (uint32_t)(np * 2 * 2 * kPage * HD));
+                for (int i = 0; i < np; ++i)
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const int row = (((l * p.num_pages + pages[i]) * 2 + kv) * p.Hkv + g) * kPage;
+                        for (int bx = 0; bx < HD / 64; ++bx)
+                            tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, p.kv_map,
+                                        bx * 64, row, bar, policy);
+                    }
+                ++seq;
+            }
+        });
+        return ok;
+    }
+
+    template <int HD>
+    __device__ void run(int cta) {
+        policy = policy_evict_first();
+        prefetch_tmap(a->p.kv_map);
+        const Plan& p = a->p;
+        bool ok = !sm->abort;
+        for (int l = 0; l < p.L && ok; ++l) {
+            ok = ok && gemv(make_gemv(*a, G_QKV, l), cta);
+            ok = ok && attention<HD>(l, cta);
+            ok = ok && gemv(make_gemv(*a, G_O, l), cta);
+            ok = ok && gemv(make_gemv(*a, G_GU, l), cta);
+            ok = ok && gemv(make_gemv(*a, G_DOWN, l), cta);
+        }
+        if (ok) gemv(make_gemv(*a, G_LM, 0), cta);
+        // drain: never leave a copy in flight into shared memory
+        const uint32_t first = seq > (uint32_t)kStages ? seq - kStages : 0;
+        for (uint32_t k = first; k < seq; ++k) {
+            const uint32_t bar = smem_u32(&sm->full[k % kStages]);
+            const uint32_t parity = (k / kStages) & 1;
+            uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(bar, parity))
+                if ((long long)(globaltimer() - t0) > a->timeout_ns) {
+                    set_error(p, sm, kErrInternal, -3);
+                    break;
+                }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ consumer pieces
+__device__ void rms_scale(Ctx& c, const float* src, int K) {
+    // rstd[b] = 1 / sqrt(mean(src[b]^2) + eps); fixed summation order
+    const StepArgs& a = *c.a;
+    float* red = c.scratch;
+    for (int b = 0; b < a.B; ++b) {
+        float ss = 0.f;
+        for (int k = c.tid * 4; k < K; k += kConsumerThreads * 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)b * K + k));
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (c.lane == 0) red[b * kConsumerWarps + c.cw] = ss;
+    }
+    consumer_sync();
+    if (c.tid < a.B) {
+        float ss = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) ss += red[c.tid * kConsumerWarps + w];
+        c.sm->rstd[c.tid] = rsqrtf(ss / (float)K + a.p.eps);
+    }
+    consumer_sync();
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __noinline__ void gemv_task(Ctx& c, const GemvStage& s, int r0, int r1) {
+    const StepArgs& a = *c.a;
+    const Plan& p = a.p;
+    const int ng = num_groups(s, r1 - r0);
+    const int g = c.lane >> 2, t = c.lane & 3;
+    const bool has_b = g < a.B;
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    const float rs = has_b ? c.sm->rstd[g] : 0.f;
+
+    for (int k0 = 0; k0 < s.K; k0 += KC) {
+        const int kc = min(KC, s.K - k0);
+        const int nblk = kc >> 6;
+        // B fragments (activations) for this warp's 64-column blocks cw and cw + 8
+        // [jj][mma i][0,1 = hi b0b1, b2b3; 2,3 = lo b0b1, b2b3]
+        uint32_t bfr[2][4][4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+            const int j = c.cw + 8 * jj;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bfr[jj][i][0] = bfr[jj][i][1] = bfr[jj][i][2] = bfr[jj][i][3] = 0u;
+            if (j < nblk && has_b && !c.sm->abort) {
+                const int col = k0 + 64 * j + 16 * t;
+                const float4* src = reinterpret_cast<const float4*>(s.src + (size_t)g * s.K + col);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float4 v = __ldcg(src + i);
+                    if (s.gain) {
+                        const float4 gg = __ldg(reinterpret_cast<const float4*>(s.gain + col) + i);
+                        v.x *= rs * gg.x; v.y *= rs * gg.y; v.z *= rs * gg.z; v.w *= rs * gg.w;
+                    }
+                    split_bf16x2(v.x, v.y, bfr[jj][i][0], bfr[jj][i][2]);
+                    split_bf16x2(v.z, v.w, bfr[jj][i][1], bfr[jj][i][3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int rg = 0; rg < 8; ++rg) {
+            if (rg < ng) {
+                const bool ok = wait_full(c, s.task_id);
+                if (ok) {
+                    const uint32_t slot = c.ring_s + (c.seq % kStages) * kSlotBytes;
+                    // ldmatrix lane -> (row, chunk): lanes 0-7 rows 0-7 chunk X, 8-15 rows
+                    // 8-15 chunk X, 16-23 rows 0-7 chunk X+1, 24-31 rows 8-15 chunk X+1
+                    const int lrow = (c.lane & 7) + ((c.lane >> 3) & 1) * 8;
+                    const int lch = c.lane >> 4;
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = c.cw + 8 * jj;
+                        if (j < nblk) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int chunk = 8 * j + 2 * i + lch;
+                                uint32_t a0, a1, a2, a3;
+                                ldmatrix_x4(slot + lrow * kRowPitch + chunk * 16, a0, a1, a2, a3);
+                                mma_16816(acc[rg], a0, a1, a2, a3, bfr[jj][i][0], bfr[jj][i][1]);
+                                mma_16816(acc[rg], a0, a1, a2, a3, bfr[jj][i][2], bfr[jj][i][3]);
+                            }
+                        }
+                    }
+                }
+                release_slot(c);
+            }
+        }
+    }
+
+    // cross-warp reduction: red[w][rr][row][col] in rounds of 4 row groups
+    float* red = c.scratch;                       // 8*4*16*8 floats = 16 KB
+    float* yout = c.scratch + 8 * 4 * 16 * 8;     // [8 rg][16][8]
+#pragma unroll
+    for (int round = 0; round < 2; ++round) {
+        if (round * 4 < ng) {
+            consumer_sync();
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int rg = round * 4 + rr;
+                if (rg < ng) {
+                    float* base = red + ((c.cw * 4 + rr) * 16) * 8;
+                    *reinterpret_cast<float2*>(base + g * 8 + 2 * t) = make_float2(acc[rg][0], acc[rg][1]);
+                    *reinterpret_cast<float2*>(base + (g + 8) * 8 + 2 * t) = make_float2(acc[rg][2], acc[rg][3]);
+                }
+            }
+            consumer_sync();
+            for (int e = c.tid; e < 4 * 16 * 8; e += kConsumerThreads) {
+                const int rr = e >> 7, rem = e & 127;
+                const int rg = round * 4 + rr;
+                if (rg < ng) {
+                    float y = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) y += red[(w * 4 + rr) * 128 + rem];
+                    yout[rg * 128 + rem] = y;
+                }
+            }
+        }
+    }
+    consumer_sync();
+    if (c.sm->abort) return;
+
+    // epilogues
+    const int n = r1 - r0;
+    const int B = a.B;
+    switch (s.kind) {
+        case G_QKV:
+            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+                const int r = e / B, b = e % B;
+                p.qkv[(size_t)b * p.qkv_rows + r0 + r] = yout[r * 8 + b];
+            }
+            break;
+        case G_O:
+        case G_DOWN:
+            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+                const int r = e / B, b = e % B;
+                float* xp = p.x + (size_t)b * p.d + perm_col(r0 + r);
+                *xp = __ldcg(xp) + yout[r * 8 + b];
+            }
+            break;
+        case G_GU: {
+            const int half = ng >> 1;
+            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+                const int r = e / B, b = e % B;
+                const float yg = yout[r * 8 + b];
+                const float yu = yout[(half * 16 + r) * 8 + b];
+                p.h[(size_t)b * p.F + perm_col(r0 + r)] = silu(yg) * yu;
+            }
+            break;
+        }
+        default: {  // G_LM: logits + running argmax (warp w handles batch row w)
+            if (a.logits)
+                for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+                    const int r = e / B, b = e % B;
+                    a.logits[(size_t)b * p.V + r0 + r] = yout[r * 8 + b];
+                }
+            if (c.cw < B) {
+                const int b = c.cw;
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+                for (int r = c.lane; r < n; r += 32) {
+                    const float v = yout[r * 8 + b];
+                    if (v > bv) { bv = v; bi = r0 + r; }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                    if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+                }
+                if (c.lane == 0) {
+                    const float cv = c.sm->amax_v[b];
+                    const int ci = c.sm->amax_i[b];
+                    if (bv > cv || (bv == cv && bi < ci)) { c.sm->amax_v[b] = bv; c.sm->amax_i[b] = bi; }
+                }
+            }
+            break;
+        }
+    }
+}
+
+__device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
+    const Plan& p = c.a->p;
+    int a0, a1;
+    cta_rows(s.R, cta, p.C, a0, a1);
+    if (a0 < a1) {
+        consumer_wait(c, s.cnt_wait, s.wait_target, s.task_id);
+        if (s.gain) rms_scale(c, s.src, s.K);
+        const int tr = task_rows(s.kind);
+        for (int r0 = a0; r0 < a1; r0 += tr) gemv_task(c, s, r0, min(a1, r0 + tr));
+    }
+    if (s.kind != G_LM) publish(c, s.cnt_pub, s.task_id);
+}
+
+// ---- attention: one piece (a CTA's share of one (b, kv head)) ----
+template <int HD>
+__device__ __noinline__ void attention_piece(Ctx& c, int l, int b, int g, const SeqSpan& sp, int u, int n,
+                                int split, int nsplit) {
+    const StepArgs& a = *c.a;
+    const Plan& p = a.p;
+    constexpr int NKS = HD / 16;   // k16 steps over the head dim
+    constexpr int NCH = HD / 8;    // 8-dim chunks
+    constexpr int PPS = 512 / HD;  // pages per slot
+    const int G = p.G;
+    const int gq = c.lane >> 2, t = c.lane & 3;
+    const int hq = g * G + gq;
+    const int task = l * 16 + ST_ATTN;
+    const int pos = sp.pos, lo = sp.lo;
+    const bool has_last = (sp.p0 + u + n - 1) == pos / kPage;
+    const float2* rope = p.rope + (size_t)pos * (HD / 2);
+
+    // q (after RoPE) as A fragments: row gq = query head, k = head dims; hi/lo split
+    uint32_t qa[NKS][2], ql[NKS][2];
+    {
+        const float* q = p.qkv + (size_t)b * p.qkv_rows + (size_t)hq * HD;
+#pragma unroll
+        for (int s = 0; s < NKS; ++s)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[2] = {0.f, 0.f};
+                if (gq < G && !c.sm->abort) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int d = 16 * s + 8 * hh + 2 * t + e;
+                        const int i = d % (HD / 2);
+                        const float2 cs = __ldg(rope + i);
+                        const float x0 = __ldcg(q + d);
+                        const float xp = __ldcg(q + (d < HD / 2 ? d + HD / 2 : d - HD / 2));
+                        v[e] = d < HD / 2 ? x0 * cs.x - xp * cs.y : x0 * cs.x + xp * cs.y;
+                    }
+                }
+                split_bf16x2(v[0], v[1], qa[s][hh], ql[s][hh]);
+            }
+    }
+    // the new token's K (after RoPE) and V, rounded to BF16, staged in shared memory
+    if (has_last && c.cw == 0 && !c.sm->abort) {
+        const float* kp = p.qkv + (size_t)b * p.qkv_rows + (size_t)(p.Hq + g) * HD;
+        const float* vp = p.qkv + (size_t)b * p.qkv_rows + (size_t)(p.Hq + p.Hkv + g) * HD;
+        for (int i = c.lane; i < HD / 2; i += 32) {
+            const float2 cs = __ldg(rope + i);
+            const float k0 = __ldcg(kp + i), k1 = __ldcg(kp + i + HD / 2);
+            c.sm->knew[i] = __float2bfloat16_rn(k0 * cs.x - k1 * cs.y);
+            c.sm->knew[i + HD / 2] = __float2bfloat16_rn(k1 * cs.x + k0 * cs.y);
+        }
+        for (int i = c.lane; i < HD; i += 32) c.sm->vnew[i] = __float2bfloat16_rn(__ldcg(vp + i));
+    }
+    if (has_last) consumer_sync();
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float oacc[NCH][2];  // O[head gq][8 i + 2 t + {0, 1}]
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) oacc[i][0] = oacc[i][1] = 0.f;
+
+    for (int st = 0; st < n; st += PPS) {
+        const int np = min(PPS, n - st);
+        const bool ok = wait_full(c, task);
+        const uint32_t slot = c.ring_s + (c.seq % kStages) * kSlotBytes;
+        if (has_last && st + np == n) {
+            // splice the new row into the last page and append it to the pool
+            if (c.cw == 0 && ok) {
+                const int pi = np - 1, row = pos % kPage;
+                const int page = __ldg(a.page_table + (size_t)b * a.max_pages + pos / kPage);
+                if (page >= 0 && page < p.num_pages) {
+                    if (c.lane < 2 * NCH) {
+                        const int kv = c.lane / NCH, ch = c.lane % NCH;
+                        const uint4 val = *reinterpret_cast<const uint4*>((kv ? c.sm->vnew : c.sm->knew) + ch * 8);
+                        const uint32_t box = slot + pi * 64 * HD + kv * 32 * HD + (ch >> 3) * 2048;
+                        const uint32_t dst = box + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(val.x),
+                                     "r"(val.y), "r"(val.z), "r"(val.w) : "memory");
+                        bf16* gdst = p.kv + ((((size_t)l * p.num_pages + page) * 2 + kv) * p.Hkv + g) *
+                                                kPage * HD + (size_t)row * HD + ch * 8;
+                        *reinterpret_cast<uint4*>(gdst) = val;
+                    }
+                } else {
+                    set_error(p, c.sm, kErrBadPage, task);
+                }
+                fence_proxy_async_smem();
+            }
+            consumer_sync();
+        }
+        if (ok && !c.sm->abort) {
+            for (int kb = c.cw; kb < 2 * np; kb += kConsumerWarps) {
+                const int pi = kb >> 1, half = kb & 1;
+                const uint32_t kbase = slot + pi * 64 * HD;
+                const uint32_t vbase = kbase + 32 * HD;
+                const int key0 = (sp.p0 + u + st + pi) * kPage + half * 8 + 2 * t;
+                const bool v0 = key0 >= lo && key0 <= pos;
+                const bool v1 = key0 + 1 >= lo && key0 + 1 <= pos;
+                // S = q K^T for 8 keys (n) x 16 head rows (m)
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+                const int lrow = half * 8 + (c.lane & 7);
+                const int lmi = c.lane >> 3;
+#pragma unroll
+                for (int s2 = 0; s2 < NKS / 2; ++s2) {
+                    const int ch = 4 * s2 + lmi;
+                    uint32_t k0r, k1r, k2r, k3r;
+                    ldmatrix_x4(kbase + (ch >> 3) * 2048 + lrow * 128 + (((ch & 7) ^ (lrow & 7)) << 4),
+                                k0r, k1r, k2r, k3r);
+                    mma_16816(sacc, qa[2 * s2][0], 0u, qa[2 * s2][1], 0u, k0r, k1r);
+                    mma_16816(sacc, ql[2 * s2][0], 0u, ql[2 * s2][1], 0u, k0r, k1r);
+                    mma_16816(sacc, qa[2 * s2 + 1][0], 0u, qa[2 * s2 + 1][1], 0u, k2r, k3r);
+                    mma_16816(sacc, ql[2 * s2 + 1][0], 0u, ql[2 * s2 + 1][1], 0u, k2r, k3r);
+                }
+                const float s0 = v0 ? sacc[0] * p.scale : -INFINITY;
+                const float s1 = v1 ? sacc[1] * p.scale : -INFINITY;
+                float mb = fmaxf(s0, s1);
+                mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+                mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+                const float m_new = fmaxf(m_run, mb);
+                float corr = 1.f, p0 = 0.f, p1 = 0.f;
+                if (m_new != -INFINITY) {
+                    corr = expf(m_run - m_new);
+                    p0 = expf(s0 - m_new);
+                    p1 = expf(s1 - m_new);
+                }
+                m_run = m_new;
+                l_run = l_run * corr + p0 + p1;
+#pragma unroll
+                for (int i = 0; i < NCH; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; }
+                uint32_t pa, pl;
+                split_bf16x2(p0, p1, pa, pl);
+                const uint32_t mask = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int q4 = 0; q4 < NCH / 4; ++q4) {
+                    const int ch = 4 * q4 + lmi;
+                    uint32_t r[4];
+                    ldmatrix_x4_trans(vbase + (ch >> 3) * 2048 + lrow * 128 + (((ch & 7) ^ (lrow & 7)) << 4),
+                                      r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int mi = 0; mi < 4; ++mi) {
+                        mma_1688_top(oacc[4 * q4 + mi][0], oacc[4 * q4 + mi][1], pa, r[mi] & mask);
+                        mma_1688_top(oacc[4 * q4 + mi][0], oacc[4 * q4 + mi][1], pl, r[mi] & mask);
+                    }
+                }
+            }
+        }
+        release_slot(c);
+    }
+
+    // merge the 8 warps' partial softmax states (rows gq < G hold real heads)
+    float* ws_o = c.scratch;                                  // [8][G][HD]
+    float* ws_m = c.scratch + kConsumerWarps * 512;           // [8][8]
+    float* ws_l = ws_m + 64;                                  // [8][8]
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    consumer_sync();
+    if (gq < G) {
+        if (t == 0) { ws_m[c.cw * 8 + gq] = m_run; ws_l[c.cw * 8 + gq] = l_run; }
+#pragma unroll
+        for (int i = 0; i < NCH; ++i)
+            *reinterpret_cast<float2*>(ws_o + (c.cw * G + gq) * HD + 8 * i + 2 * t) =
+                make_float2(oacc[i][0], oacc[i][1]);
+    }
+    consumer_sync();
+    const int bg = b * p.Hkv + g;
+    const size_t pbase = ((size_t)bg * p.C + split) * G;
+    if (!c.sm->abort) {
+        for (int e = c.tid; e < G * HD; e += kConsumerThreads) {
+            const int hl = e / HD, d = e % HD;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ws_m[w * 8 + hl]);
+            float o = 0.f, L = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = ws_m[w * 8 + hl];
+                const float f = mw == -INFINITY ? 0.f : expf(mw - M);
+                o += f * ws_o[(w * G + hl) * HD + d];
+                L += f * ws_l[w * 8 + hl];
+            }
+            p.part_o[(pbase + hl) * HD + d] = o;
+            if (d == 0) p.part_ml[pbase + hl] = make_float2(M, L);
+        }
+    }
+    // arrival: the last of the nsplit pieces merges them all
+    consumer_sync();
+    if (c.tid == 0) {
+        int last = 0;
+        if (!c.sm->abort) {
+            uint32_t* ctr = p.arrivals + ((size_t)l * p.maxB * p.Hkv + bg) * kCounterStride;
+            __threadfence();
+            const uint32_t old = atom_acq_rel_add(ctr, 1u);
+            if (old == (uint32_t)(nsplit - 1)) { last = 1; st_relaxed(ctr, 0u); }
+        }
+        c.sm->bcast = last;
+    }
+    consumer_sync();
+    if (c.sm->bcast) {
+        const size_t base0 = (size_t)bg * p.C * G;
+        for (int e = c.tid; e < G * HD; e += kConsumerThreads) {
+            const int hl = e / HD, d = e % HD;
+            float M = -INFINITY;
+            for (int sidx = 0; sidx < nsplit; ++sidx)
+                M = fmaxf(M, __ldcg(&p.part_ml[base0 + (size_t)sidx * G + hl].x));
+            float o = 0.f, L = 0.f;
+            for (int sidx = 0; sidx < nsplit; ++sidx) {
+                const float2 ml = __ldcg(&p.part_ml[base0 + (size_t)sidx * G + hl]);
+                const float f = expf(ml.x - M);
+                o += f * __ldcg(&p.part_o[(base0 + (size_t)sidx * G + hl) * HD + d]);
+                L += f * ml.y;
+            }
+            p.attn[(size_t)b * p.Hq * HD + perm_col((g * G + hl) * HD + d)] = o / L;
+        }
+        consumer_sync();
+        if (c.tid == 0 && !c.sm->abort && a.skip_publish != task) {
+            __threadfence();
+            red_release_add(p.counters + cnt_stage(l, ST_ATTN) * kCounterStride, 1u);
+        }
+    }
+}
+
+template <int HD>
+__device__ void attention_stage(Ctx& c, int l, int cta) {
+    bool waited = false;
+    for_each_piece(*c.a, c.sm, l, cta, [&](int b, int g, const SeqSpan& sp, int u, int n,
+                                          int split, int nsplit) {
+        if (!waited) {
+            consumer_wait(c, cnt_stage(l, ST_QKV), c.a->stage_target, l * 16 + ST_ATTN);
+            waited = true;
+        }
+        attention_piece<HD>(c, l, b, g, sp, u, n, split, nsplit);
+    });
+}
+
+__device__ void embed_stage(Ctx& c, int cta) {
+    const StepArgs& a = *c.a;
+    const Plan& p = a.p;
+    const long long total = (long long)a.B * p.d;
+    const long long e0 = (long long)cta * total / p.C, e1 = (long long)(cta + 1) * total / p.C;
+    if (!c.sm->abort)
+        for (long long e = e0 + c.tid; e < e1; e += kConsumerThreads) {
+            const int b = (int)(e / p.d), k = (int)(e % p.d);
+            const int tok = __ldg(a.tokens + b);
+            p.x[(size_t)b * p.d + perm_col(k)] = __bfloat162float(p.embed[(size_t)tok * p.d + k]);
+        }
+    publish(c, cnt_embed(), -2);
+}
+
+__device__ void argmax_finish(Ctx& c, int cta) {
+    const StepArgs& a = *c.a;
+    const Plan& p = a.p;
+    if (c.tid < a.B)
+        p.amax_part[(size_t)cta * p.maxB + c.tid] =
+            make_float2(c.sm->amax_v[c.tid], __int_as_float(c.sm->amax_i[c.tid]));
+    consumer_sync();
+    if (c.tid == 0) {
+        int last = 0;
+        if (!c.sm->abort && a.skip_publish != p.L * 16) {
+            uint32_t* ctr = p.arrivals + ((size_t)p.L * p.maxB * p.Hkv) * kCounterStride;
+            __threadfence();
+            const uint32_t old = atom_acq_rel_add(ctr, 1u);
+            if (old == (uint32_t)(p.C - 1)) { last = 1; st_relaxed(ctr, 0u); }
+        }
+        c.sm->bcast = last;
+    }
+    consumer_sync();
+    if (c.sm->bcast && c.cw < a.B) {
+        const int b = c.cw;
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int k = c.lane; k < p.C; k += 32) {
+            const float2 v = __ldcg(&p.amax_part[(size_t)k * p.maxB + b]);
+            const int vi = __float_as_int(v.y);
+            if (v.x > bv || (v.x == bv && vi < bi)) { bv = v.x; bi = vi; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (c.lane == 0) a.next_tokens[b] = bi == 0x7fffffff ? 0 : bi;
+    }
+}
+
+template <int HD>
+__device__ void consumer_run(Ctx& c, int cta) {
+    const Plan& p = c.a->p;
+    if (c.sm->abort) return;  // step inputs rejected (uniform: set before the first barrier)
+    embed_stage(c, cta);
+    for (int l = 0; l < p.L; ++l) {
+        gemv_stage(c, make_gemv(*c.a, G_QKV, l), cta);
+        attention_stage<HD>(c, l, cta);
+        gemv_stage(c, make_gemv(*c.a, G_O, l), cta);
+        gemv_stage(c, make_gemv(*c.a, G_GU, l), cta);
+        gemv_stage(c, make_gemv(*c.a, G_DOWN, l), cta);
+    }
+    gemv_stage(c, make_gemv(*c.a, G_LM, 0), cta);
+    argmax_finish(c, cta);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ StepArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    uint8_t* ring = smem_raw + pad;
+    float* scratch = reinterpret_cast<float*>(ring + kStages * kSlotBytes);
+    Smem* sm = reinterpret_cast<Smem*>(ring + kStages * kSlotBytes + kScratchBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+
+    if (threadIdx.x == 0) {
+        sm->abort = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sm->full[s]), 1);
+            mbar_init(smem_u32(&sm->empty[s]), kConsumerWarps);
+        }
+        fence_barrier_init();
+        // step-input checks (every CTA reads the same values)
+        bool bad = a.B < 1 || a.B > a.p.maxB;
+        for (int b = 0; b < kMaxBatch; ++b) sm->pos[b] = 0;
+        for (int b = 0; b < a.B && !bad; ++b) {
+            const int tok = __ldg(a.tokens + b), pos = __ldg(a.positions + b);
+            const int sl = __ldg(a.seq_lens + b);
+            bad = tok < 0 || tok >= a.p.V || pos < 0 || pos >= a.p.max_pos || sl != pos + 1 ||
+                  pos / kPage >= a.max_pages;
+            sm->pos[b] = pos;
+        }
+        if (bad) set_error(a.p, sm, kErrInvalid, -1);
+        if (status_bad(a.p)) sm->abort = 1;
+    }
+    if (threadIdx.x < kMaxBatch) {
+        sm->amax_v[threadIdx.x] = -INFINITY;
+        sm->amax_i[threadIdx.x] = 0x7fffffff;
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            Producer pr;
+            pr.a = &a;
+            pr.sm = sm;
+            pr.ring_s = smem_u32(ring);
+            pr.run<HD>(cta);
+        }
+        return;
+    }
+    Ctx c;
+    c.a = &a;
+    c.sm = sm;
+    c.ring = ring;
+    c.scratch = scratch;
+    c.ring_s = smem_u32(ring);
+    c.seq = 0;
+    c.cw = warp - 1;
+    c.lane = lane;
+    c.tid = threadIdx.x - 32;
+    consumer_run<HD>(c, cta);
+}
+
+}  // namespace mk

@@ -1,0 +1,190 @@
+"""GPU parity: the CUDA decode step (called through the C ABI) against the CPU oracle
+on the same seeded weights, KV pools, page tables and tokens."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import persistent_megakernel_05_b300 as mk
+from harness import Pair, check_kv, check_logits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from persistent_megakernel_05_b300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+
+
+# ------------------------------------------------------------------ tiny model
+@pytest.mark.parametrize("gain_noise", [0.0, 0.02])
+def test_tiny_prompt_then_greedy(gain_noise):
+    """Tiny config: 32-token random prompt fed as teacher-forced decode steps, then 16
+    greedy steps (both sides fed the GPU's token); pool of 8 permuted pages."""
+    cfg = synth.TINY
+    pair = Pair(cfg, seed=0, num_pages=8, gain_noise=gain_noise)
+    rng = np.random.default_rng(0)
+    prompt = synth.random_tokens(rng, cfg.vocab, 32)
+    pt = synth.random_page_tables(rng, 8, [3], max_pages=4)
+    tok = int(prompt[0])
+    worst = 0.0
+    for t in range(48):
+        g_lg, g_nx, o_lg, o_nx = pair.step([tok], [t], pt)
+        worst = max(worst, check_logits(g_lg, g_nx, o_lg, o_nx, what=f"step {t}"))
+        tok = int(prompt[t + 1]) if t + 1 < 32 else int(g_nx[0])
+    assert check_kv(pair) == 48 * cfg.n_layers * 2 * cfg.n_kv_heads
+    pair.close()
+
+
+@pytest.mark.parametrize("window", [0, 24])
+def test_tiny_batch8_ragged(window):
+    """Batch 8, ragged lengths (incl. position 0 and page-boundary positions), disjoint
+    random page runs, seeded N(0,1) KV history, optional sliding window."""
+    cfg = synth.TINY.with_(sliding_window=window)
+    pair = Pair(cfg, seed=3, num_pages=96, kv_seed=7)
+    rng = np.random.default_rng(3)
+    pos = np.array([0, 15, 16, 17, 100, 31, 200, 63], np.int32)
+    pages = [(int(p) + 4) // 16 + 1 for p in pos]
+    pt = synth.random_page_tables(rng, 96, pages, max_pages=max(pages) + 1)
+    toks = synth.random_tokens(rng, cfg.vocab, 8)
+    for s in range(4):
+        g_lg, g_nx, o_lg, o_nx = pair.step(toks, pos + s, pt)
+        check_logits(g_lg, g_nx, o_lg, o_nx, what=f"step {s}")
+        toks = g_nx
+    check_kv(pair)
+    pair.close()
+
+
+def test_tiny_batch_sizes_and_shared_prefix():
+    """Batches 1..8 in turn on one handle (continuous-batching style), with rows that
+    share a read-only prefix run of pages."""
+    cfg = synth.TINY
+    pair = Pair(cfg, seed=4, num_pages=64, kv_seed=2)
+    rng = np.random.default_rng(4)
+    pt = synth.prefix_shared_page_tables(rng, 64, 8, prefix_pages=4, private_pages=3, max_pages=8)
+    for B in (1, 3, 8, 2):
+        pos = rng.integers(64, 64 + 40, size=B).astype(np.int32)  # beyond the 4-page prefix
+        toks = synth.random_tokens(rng, cfg.vocab, B)
+        g_lg, g_nx, o_lg, o_nx = pair.step(toks, pos, pt[:B])
+        check_logits(g_lg, g_nx, o_lg, o_nx, what=f"B={B}")
+    check_kv(pair)
+    pair.close()
+
+
+def test_logits_are_deterministic_and_optional():
+    cfg = synth.TINY
+    W = synth.make_weights(cfg, 5, device="cuda")
+    outs = []
+    for _ in range(2):
+        pair = Pair(cfg, seed=5, num_pages=16, kv_seed=3, weights=W)
+        pt = np.arange(16, dtype=np.int32).reshape(2, 8)
+        g_lg, g_nx, _, _ = pair.step([1, 2], [70, 90], pt)
+        _, g_nx2, _, _ = pair.step(g_nx, [71, 91], pt, with_logits=False)
+        outs.append((g_lg, g_nx, g_nx2))
+        pair.close()
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][2], outs[1][2])
+
+
+# ------------------------------------------------------------------ device-side errors
+def _small_model():
+    cfg = synth.TINY
+    return cfg, Pair(cfg, seed=6, num_pages=8, kv_seed=1)
+
+
+def test_bad_page_latches_error_then_reset_recovers():
+    cfg, pair = _small_model()
+    g = pair.gpu
+    dev = "cuda"
+    pt = torch.tensor([[0, 99]], dtype=torch.int32, device=dev)  # page 99 does not exist
+    t = torch.tensor([5], dtype=torch.int32, device=dev)
+    p = torch.tensor([20], dtype=torch.int32, device=dev)
+    nxt = torch.zeros(1, dtype=torch.int32, device=dev)
+    g.step(t, p, pt, p + 1, nxt)
+    code, task = g.status()
+    assert code == mk.MK_ERR_BAD_PAGE
+    g.reset()
+    assert g.status()[0] == mk.MK_OK
+    g_lg, g_nx, o_lg, o_nx = pair.step([5], [20], np.array([[0, 1]], np.int32))
+    check_logits(g_lg, g_nx, o_lg, o_nx)
+    pair.close()
+
+
+def test_bad_step_inputs_latch_invalid():
+    cfg, pair = _small_model()
+    g = pair.gpu
+    dev = "cuda"
+    pt = torch.tensor([[0, 1]], dtype=torch.int32, device=dev)
+    nxt = torch.zeros(1, dtype=torch.int32, device=dev)
+    for tok, pos, sl in ((cfg.vocab, 3, 4), (3, 3, 7), (3, 40, 41), (-1, 0, 1)):
+        g.step(torch.tensor([tok], dtype=torch.int32, device=dev),
+               torch.tensor([pos], dtype=torch.int32, device=dev), pt,
+               torch.tensor([sl], dtype=torch.int32, device=dev), nxt)
+        assert g.status()[0] == mk.MK_ERR_INVALID_ARG, (tok, pos, sl)
+        g.reset()
+    pair.close()
+
+
+def test_wait_timeout_is_reported_not_hung():
+    """A task that never publishes (test hook) makes its waiters time out after the
+    configured limit; the kernel returns, the status names the task, reset recovers."""
+    cfg, pair = _small_model()
+    g = pair.gpu
+    g.set_option(mk.MK_OPT_TIMEOUT_NS, 50_000_000)  # 50 ms
+    g.set_option(mk.MK_OPT_SKIP_PUBLISH, 1 * 16 + 2)  # layer 1, O-projection stage
+    dev = "cuda"
+    pt = torch.tensor([[0, 1]], dtype=torch.int32, device=dev)
+    nxt = torch.zeros(1, dtype=torch.int32, device=dev)
+    p = torch.tensor([3], dtype=torch.int32, device=dev)
+    g.step(torch.tensor([9], dtype=torch.int32, device=dev), p, pt, p + 1, nxt)
+    code, task = g.status()
+    assert code == mk.MK_ERR_TIMEOUT
+    assert task == 1 * 16 + 3  # the gate/up stage of layer 1 waits on it
+    g.set_option(mk.MK_OPT_SKIP_PUBLISH, -1)
+    g.reset()
+    g_lg, g_nx, o_lg, o_nx = pair.step([9], [3], np.array([[0, 1]], np.int32))
+    check_logits(g_lg, g_nx, o_lg, o_nx)
+    pair.close()
+
+
+# ------------------------------------------------------------------ full-size configs
+@pytest.fixture(scope="module")
+def dense2b_weights():
+    return synth.make_weights(synth.DENSE_2B, 1, device="cuda")
+
+
+def test_dense2b_batch1_8k_context(dense2b_weights):
+    """~2B dense decoder, batch 1, 8192 seeded KV tokens on 512 permuted pages; two
+    steps, full logits compared with the oracle."""
+    cfg = synth.DENSE_2B
+    npages = 530
+    pair = Pair(cfg, seed=1, num_pages=npages, kv_seed=11, weights=dense2b_weights)
+    rng = np.random.default_rng(1)
+    pt = synth.random_page_tables(rng, npages, [528], max_pages=528)
+    tok = [int(synth.random_tokens(rng, cfg.vocab, 1)[0])]
+    for s in range(2):
+        g_lg, g_nx, o_lg, o_nx = pair.step(tok, [8192 + s], pt)
+        check_logits(g_lg, g_nx, o_lg, o_nx, what=f"2B step {s}")
+        tok = [int(g_nx[0])]
+    check_kv(pair)
+    pair.close()
+
+
+def test_dense2b_batch8_ragged_sliding(dense2b_weights):
+    """~2B dense, batch 8, lengths uniform in [512, 8192], disjoint random page tables,
+    sliding window 4096 on odd layers; one step, full logits of all 8 rows."""
+    cfg = synth.DENSE_2B_SWA
+    rng = np.random.default_rng(2)
+    lens = rng.integers(512, 8193, size=8).astype(np.int32)
+    pages = [int(n) // 16 + 2 for n in lens]
+    npages = sum(pages) + 8
+    pair = Pair(cfg, seed=1, num_pages=npages, kv_seed=12, weights=dense2b_weights)
+    pt = synth.random_page_tables(rng, npages, pages, max_pages=max(pages))
+    toks = synth.random_tokens(rng, cfg.vocab, 8)
+    g_lg, g_nx, o_lg, o_nx = pair.step(toks, lens, pt)
+    check_logits(g_lg, g_nx, o_lg, o_nx, what="2B b8")
+    check_kv(pair)
+    pair.close()
