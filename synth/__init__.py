@@ -79,7 +79,7 @@ class ModelConfig:
 TINY = ModelConfig("tiny", n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
                    ffn_dim=768, vocab=4096, max_batch=8, max_positions=512)
 DENSE_2B = ModelConfig("dense-2b", n_layers=25, d_model=2048, n_q_heads=16, n_kv_heads=4,
-                       head_dim=128, ffn_dim=8192, vocab=128256, max_positions=8192 + 512)
+                       head_dim=128, ffn_dim=8192, vocab=128256, max_positions=8192 + 1024)
 DENSE_2B_SWA = DENSE_2B.with_(name="dense-2b-swa", sliding_window=4096)
 MOE = ModelConfig("moe-64x768", n_layers=24, d_model=2048, n_q_heads=32, n_kv_heads=4,
                   head_dim=64, ffn_dim=0, vocab=128256, n_experts=64, top_k=8,
