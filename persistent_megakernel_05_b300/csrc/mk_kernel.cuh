@@ -916,6 +916,7 @@ __device__ void embed_stage(Ctx& c, int cta) {
 __device__ void argmax_finish(Ctx& c, int cta) {
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
+    consumer_sync();  // every warp's LM-head epilogue has updated amax_v / amax_i
     if (c.tid < a.B)
         p.amax_part[(size_t)cta * p.maxB + c.tid] =
             make_float2(c.sm->amax_v[c.tid], __int_as_float(c.sm->amax_i[c.tid]));
