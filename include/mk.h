@@ -185,6 +185,43 @@ typedef struct mk_info {
 } mk_info;
 MK_API mk_status mk_get_info(const mk_handle *h, mk_info *out);
 
+/* The decode step for callers that cannot allocate device memory. It has no
+ * counterpart in the pages: it is the same kernel as mk_decode_step, but it needs no
+ * handle and allocates nothing. Callers that cannot call cudaMalloc -- code running
+ * under a memory plan that owns every byte of HBM, allocator-free or sandboxed
+ * runtimes, paths where an allocation would synchronise the device -- pass every
+ * input and output themselves, including the KV pool.
+ *
+ * All scratch (norm gains, RoPE table, layer table, activations, attention partials,
+ * dependency counters, status word, KV tensor map) lives in one file-scope static
+ * device array of MK_NOALLOC_SCRATCH_BYTES (8 MiB), which every GPU that loads this
+ * library holds until the process exits. Descriptors whose scratch does not fit
+ * (roughly: max_batch * n_kv_heads * 148 * (n_q_heads/n_kv_heads) * head_dim * 4 bytes
+ * of attention partials, plus max_positions * head_dim * 4 bytes of RoPE table, plus
+ * small terms) are rejected with MK_ERR_INVALID_ARG before anything is enqueued.
+ *   desc, weights        as for mk_create (host structs; weights on the current device)
+ *   kv_pool, num_pages   caller-owned device pool in the mk_kv_pool layout (BF16,
+ *                        [n_layers][num_pages][2][n_kv_heads][16][head_dim], dense)
+ *   tokens .. logits     as for mk_decode_step
+ *   status_out           device int32[2], out: {status, failing task} of the step,
+ *                        written on `stream` after the kernel (read it after a sync)
+ * Runs on the CURRENT device. The first call on a device does a one-time set-up
+ * (device checks, kernel attributes, and cudaGetSymbolAddress of the static array);
+ * make that first call before any stream capture. Every call re-initialises the parts
+ * of the array that must start from zero (counters, status) and rewrites the tables;
+ * the array keeps the last call's contents otherwise. All calls share the one array,
+ * so calls whose work overlaps on the GPU (different streams, or threads) race: run
+ * them one after another. Host-side errors return at once; device-side errors are
+ * reported through status_out. */
+#define MK_NOALLOC_SCRATCH_BYTES (8u << 20)
+MK_API mk_status mk_decode_step_noalloc(const mk_model_desc *desc, const mk_weights *weights,
+                                        void *kv_pool, int32_t num_pages,
+                                        const int32_t *tokens, const int32_t *positions,
+                                        const int32_t *page_table, int32_t max_pages_per_seq,
+                                        const int32_t *seq_lens, int32_t batch,
+                                        int32_t *next_tokens, float *logits,
+                                        int32_t *status_out, void *stream);
+
 /* Introspection for stage-by-stage verification. After a step has completed (sync
  * the stream first), these device buffers hold the activations of the LAST layer the
  * step ran; they are overwritten by the next step. Layouts (fp32, row b at b*width):

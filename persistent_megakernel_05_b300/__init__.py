@@ -32,7 +32,8 @@ MK_OPT_SKIP_PUBLISH = 2
 # exported symbols of include/mk.h
 ABI_SYMBOLS = ("mk_create", "mk_kv_alloc", "mk_kv_free", "mk_decode_step", "mk_status_sync",
                "mk_status_reset", "mk_set_option", "mk_get_info", "mk_debug_buffer",
-               "mk_status_string", "mk_destroy")
+               "mk_status_string", "mk_destroy", "mk_decode_step_noalloc")
+MK_NOALLOC_SCRATCH_BYTES = 8 << 20
 MK_BUF_X, MK_BUF_QKV, MK_BUF_ATTN, MK_BUF_H = 1, 2, 3, 4
 
 
@@ -115,6 +116,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mk_get_info.argtypes = [_vp, _P(mk_info)]
     L.mk_debug_buffer.restype = ctypes.c_int
     L.mk_debug_buffer.argtypes = [_vp, ctypes.c_int32, _P(_vp), _P(i64)]
+    L.mk_decode_step_noalloc.restype = ctypes.c_int
+    L.mk_decode_step_noalloc.argtypes = [_P(mk_model_desc), _P(mk_weights), _vp, i32, _vp, _vp,
+                                         _vp, i32, _vp, i32, _vp, _vp, _vp, _vp]
     L.mk_status_string.restype = ctypes.c_char_p
     L.mk_status_string.argtypes = [ctypes.c_int]
     L.mk_destroy.restype = None
@@ -192,6 +196,20 @@ def mk_debug_buffer(handle: int, which: int):
 def perm_col(k):
     """Storage column of logical column k in the permuted activation layouts."""
     return (k & ~63) | (((k & 7) >> 1) << 4) | (((k & 63) >> 3) << 1) | (k & 1)
+
+
+def mk_decode_step_noalloc(desc: mk_model_desc, weights: mk_weights, kv_pool: int,
+                           num_pages: int, tokens: int, positions: int, page_table: int,
+                           max_pages_per_seq: int, seq_lens: int, batch: int, next_tokens: int,
+                           logits: Optional[int], status_out: int,
+                           stream: Optional[int] = None) -> int:
+    """Decode step without a handle and without any device allocation (all scratch in
+    the library's static device array); raw device addresses. Returns the mk_status of
+    the host-side checks; the device status lands in status_out (int32[2])."""
+    return load().mk_decode_step_noalloc(ctypes.byref(desc), ctypes.byref(weights), kv_pool,
+                                         num_pages, tokens, positions, page_table,
+                                         max_pages_per_seq, seq_lens, batch, next_tokens,
+                                         logits, status_out, stream)
 
 
 def mk_destroy(handle: int):

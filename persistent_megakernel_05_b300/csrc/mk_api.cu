@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -495,3 +496,250 @@ void mk_destroy(mk_handle* h) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// mk_decode_step_noalloc: the same decode-step kernel, with every byte of its
+// scratch (plan tables, norm gains, RoPE table, activations, attention partials,
+// counters, status word, KV tensor map) carved out of one file-scope static device
+// array instead of memory from cudaMalloc. It exists for callers that must not
+// allocate device memory: code running where an allocation would synchronise the
+// device or is forbidden (allocator-free runtimes, memory-capped sandboxes, hosts
+// that pre-plan every byte of HBM).
+// ===========================================================================
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;  // 8 MiB, held on every GPU
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+struct NoAllocDevice {
+    bool ready;
+    int num_sms;
+    unsigned char* base;  // device address of g_noalloc_scratch on this device
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Parameters of the set-up kernel: the layer table and gain sources travel as kernel
+// parameters, so nothing is staged through allocated memory.
+struct NoAllocSetup {
+    mk::LayerPlan layers[mk::kMaxLayers];
+    const uint16_t* gain_src[2 * mk::kMaxLayers + 1];
+    mk::LayerPlan* layers_dst;
+    float* gains_dst;
+    float2* rope_dst;
+    uint32_t* zero_dst;
+    long long zero_words;
+    int L, d, hd, max_pos;
+    float theta;
+};
+
+__global__ void noalloc_setup_kernel(const __grid_constant__ NoAllocSetup s) {
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long n = (long long)gridDim.x * blockDim.x;
+    for (long long i = tid; i < s.L; i += n) s.layers_dst[i] = s.layers[i];
+    const long long ng = (long long)(2 * s.L + 1) * s.d;
+    for (long long i = tid; i < ng; i += n) {
+        const int v = (int)(i / s.d), k = (int)(i % s.d);
+        const uint32_t u = (uint32_t)s.gain_src[v][k] << 16;
+        s.gains_dst[(size_t)v * s.d + mk::perm_col(k)] = __uint_as_float(u);
+    }
+    const int half = s.hd / 2;
+    const long long nr = (long long)s.max_pos * half;
+    for (long long i = tid; i < nr; i += n) {
+        const int pos = (int)(i / half), j = (int)(i % half);
+        const double inv_freq = pow((double)s.theta, -2.0 * j / (double)s.hd);
+        const double ang = (double)pos * inv_freq;
+        s.rope_dst[i] = make_float2((float)cos(ang), (float)sin(ang));
+    }
+    for (long long i = tid; i < s.zero_words; i += n) s.zero_dst[i] = 0u;
+}
+
+// Once per device, with that device current: check it, set the kernel attributes and
+// look up the device address of the static array.
+mk_status noalloc_device_setup(int dev, NoAllocDevice** out) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return MK_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocDevice& D = g_noalloc_dev[dev];
+    if (!D.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return MK_ERR_INTERNAL;
+        }
+        if (prop.major != 10 || prop.minor != 3 || !prop.cooperativeLaunch)
+            return MK_ERR_UNSUPPORTED_DEVICE;
+        if (set_kernel_attrs<128>() != cudaSuccess || set_kernel_attrs<64>() != cudaSuccess) {
+            cudaGetLastError();
+            return MK_ERR_UNSUPPORTED_DEVICE;
+        }
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return MK_ERR_INTERNAL;
+        }
+        D.base = static_cast<unsigned char*>(ptr);
+        D.num_sms = prop.multiProcessorCount;
+        D.ready = true;
+    }
+    *out = &D;
+    return MK_OK;
+}
+
+}  // namespace
+
+extern "C" mk_status mk_decode_step_noalloc(
+    const mk_model_desc* desc, const mk_weights* weights, void* kv_pool, int32_t num_pages,
+    const int32_t* tokens, const int32_t* positions, const int32_t* page_table,
+    int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t* next_tokens,
+    float* logits, int32_t* status_out, void* stream) {
+    mk_status st = validate_desc(desc);
+    if (st != MK_OK) return st;
+    st = validate_weights(desc, weights);
+    if (st != MK_OK) return st;
+    if (!kv_pool || num_pages < 1 || !tokens || !positions || !page_table || !seq_lens ||
+        !next_tokens || !status_out || max_pages_per_seq < 1)
+        return MK_ERR_INVALID_ARG;
+    if (batch < 1 || batch > desc->max_batch) return MK_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_NO_DEVICE;
+    }
+    NoAllocDevice* D = nullptr;
+    st = noalloc_device_setup(dev, &D);
+    if (st != MK_OK) return st;
+
+    const int L = desc->n_layers, d = desc->d_model, Hq = desc->n_q_heads, Hkv = desc->n_kv_heads;
+    const int hd = desc->head_dim, G = Hq / Hkv, F = desc->ffn_dim, V = desc->vocab;
+    const int maxB = desc->max_batch, C = D->num_sms;
+    const int qkv_rows = (Hq + 2 * Hkv) * hd;
+    const int64_t rows = (int64_t)L * num_pages * 2 * Hkv * mk::kPage;
+    if (rows >= (1LL << 31)) return MK_ERR_INVALID_ARG;
+
+    // carve the static array
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t o_tmap = take(sizeof(CUtensorMap));
+    const size_t o_layers = take(sizeof(mk::LayerPlan) * L);
+    const size_t o_gains = take(sizeof(float) * (size_t)(2 * L + 1) * d);
+    const size_t o_rope = take(sizeof(float2) * (size_t)desc->max_positions * (hd / 2));
+    const size_t o_x = take(sizeof(float) * maxB * d);
+    const size_t o_qkv = take(sizeof(float) * maxB * qkv_rows);
+    const size_t o_attn = take(sizeof(float) * maxB * Hq * hd);
+    const size_t o_h = take(sizeof(float) * maxB * F);
+    const size_t o_po = take(sizeof(float) * (size_t)maxB * Hkv * C * G * hd);
+    const size_t o_pml = take(sizeof(float2) * (size_t)maxB * Hkv * C * G);
+    const size_t o_am = take(sizeof(float2) * (size_t)C * maxB);
+    const size_t counters_words = (size_t)(2 + L * mk::kStagesPerLayer) * mk::kCounterStride;
+    const size_t arrivals_words = (size_t)(L * maxB * Hkv + 1) * mk::kCounterStride;
+    const size_t o_zero = off;  // counters, arrivals, status: contiguous, cleared every call
+    const size_t o_cnt = take(sizeof(uint32_t) * counters_words);
+    const size_t o_arr = take(sizeof(uint32_t) * arrivals_words);
+    const size_t o_status = take(sizeof(int) * 4);
+    if (off > kNoAllocScratchBytes) return MK_ERR_INVALID_ARG;  // model/batch too large
+    unsigned char* base = D->base;
+
+    // KV tensor map, encoded on the host and copied into the array (no allocation)
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void**)&encode, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !encode) {
+        cudaGetLastError();
+        return MK_ERR_INTERNAL;
+    }
+    CUtensorMap map;
+    cuuint64_t gdim[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)hd * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)mk::kPage};
+    cuuint32_t estride[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pool, gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MK_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(base + o_tmap, &map, sizeof(map), cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_INTERNAL;
+    }
+
+    NoAllocSetup su;
+    std::memset(&su, 0, sizeof(su));
+    float* gains = reinterpret_cast<float*>(base + o_gains);
+    for (int l = 0; l < L; ++l) {
+        const mk_layer_weights& W = weights->layers[l];
+        mk::LayerPlan& lp = su.layers[l];
+        lp.wq = (const bf16*)W.wq; lp.wk = (const bf16*)W.wk; lp.wv = (const bf16*)W.wv;
+        lp.wo = (const bf16*)W.wo; lp.w_gate = (const bf16*)W.w_gate;
+        lp.w_up = (const bf16*)W.w_up; lp.w_down = (const bf16*)W.w_down;
+        lp.attn_gain = gains + (size_t)(2 * l) * d;
+        lp.mlp_gain = gains + (size_t)(2 * l + 1) * d;
+        lp.sliding = (desc->layer_is_sliding && desc->layer_is_sliding[l]) ? 1 : 0;
+        su.gain_src[2 * l] = (const uint16_t*)W.attn_norm;
+        su.gain_src[2 * l + 1] = (const uint16_t*)W.mlp_norm;
+    }
+    su.gain_src[2 * L] = (const uint16_t*)weights->final_norm;
+    su.layers_dst = reinterpret_cast<mk::LayerPlan*>(base + o_layers);
+    su.gains_dst = gains;
+    su.rope_dst = reinterpret_cast<float2*>(base + o_rope);
+    su.zero_dst = reinterpret_cast<uint32_t*>(base + o_zero);
+    su.zero_words = (long long)((o_status + sizeof(int) * 4 - o_zero) / sizeof(uint32_t));
+    su.L = L; su.d = d; su.hd = hd; su.max_pos = desc->max_positions; su.theta = desc->rope_theta;
+    noalloc_setup_kernel<<<C, 256, 0, s>>>(su);
+    if (cudaGetLastError() != cudaSuccess) return MK_ERR_LAUNCH;
+
+    mk::StepArgs a;
+    mk::Plan& p = a.p;
+    p.L = L; p.d = d; p.Hq = Hq; p.Hkv = Hkv; p.hd = hd; p.G = G; p.F = F; p.V = V;
+    p.window = desc->sliding_window; p.max_pos = desc->max_positions; p.maxB = maxB;
+    p.num_pages = num_pages;
+    p.eps = desc->rms_eps;
+    p.scale = (float)(1.0 / std::sqrt((double)hd));
+    p.C = C;
+    p.qkv_rows = qkv_rows;
+    p.layers = su.layers_dst;
+    p.embed = (const bf16*)weights->embed;
+    p.lm_head = (const bf16*)weights->lm_head;
+    p.final_gain = gains + (size_t)(2 * L) * d;
+    p.rope = su.rope_dst;
+    p.x = (float*)(base + o_x);
+    p.qkv = (float*)(base + o_qkv);
+    p.attn = (float*)(base + o_attn);
+    p.h = (float*)(base + o_h);
+    p.part_o = (float*)(base + o_po);
+    p.part_ml = (float2*)(base + o_pml);
+    p.amax_part = (float2*)(base + o_am);
+    p.counters = (uint32_t*)(base + o_cnt);
+    p.arrivals = (uint32_t*)(base + o_arr);
+    p.status = (int*)(base + o_status);
+    p.kv = (bf16*)kv_pool;
+    p.kv_map = base + o_tmap;
+    a.tokens = tokens;
+    a.positions = positions;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.next_tokens = next_tokens;
+    a.logits = logits;
+    a.max_pages = max_pages_per_seq;
+    a.B = batch;
+    a.stage_target = (uint32_t)C;  // counters start at zero every call: epoch 1
+    a.embed_target = (uint32_t)C;
+    a.attn_target = (uint32_t)batch * (uint32_t)Hkv;
+    a.skip_publish = -1;
+    a.timeout_ns = 1000000000LL;
+    void* args[] = {&a};
+    const void* fn = hd == 128 ? (const void*)mk::decode_step_kernel<128>
+                               : (const void*)mk::decode_step_kernel<64>;
+    if (cudaLaunchCooperativeKernel(fn, dim3(C), dim3(mk::kThreads), args, mk::kSmemBytes, s) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_LAUNCH;
+    }
+    if (cudaMemcpyAsync(status_out, base + o_status, 2 * sizeof(int), cudaMemcpyDeviceToDevice, s) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_INTERNAL;
+    }
+    return MK_OK;
+}
