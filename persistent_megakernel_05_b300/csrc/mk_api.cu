@@ -175,6 +175,9 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
         return MK_ERR_UNSUPPORTED_DEVICE;
     }
 
+    // each CTA keeps its ceil(d / CTAs) residual rows in shared memory
+    if ((desc->d_model + prop.multiProcessorCount - 1) / prop.multiProcessorCount > mk::kMaxOwnRows)
+        return MK_ERR_INVALID_ARG;
     mk_handle* h = new (std::nothrow) mk_handle();
     if (!h) return MK_ERR_OOM;
     h->device = device;
@@ -613,6 +616,7 @@ extern "C" mk_status mk_decode_step_noalloc(
     const int L = desc->n_layers, d = desc->d_model, Hq = desc->n_q_heads, Hkv = desc->n_kv_heads;
     const int hd = desc->head_dim, G = Hq / Hkv, F = desc->ffn_dim, V = desc->vocab;
     const int maxB = desc->max_batch, C = D->num_sms;
+    if ((d + C - 1) / C > mk::kMaxOwnRows) return MK_ERR_INVALID_ARG;
     const int qkv_rows = (Hq + 2 * Hkv) * hd;
     const int64_t rows = (int64_t)L * num_pages * 2 * Hkv * mk::kPage;
     if (rows >= (1LL << 31)) return MK_ERR_INVALID_ARG;
@@ -743,3 +747,17 @@ extern "C" mk_status mk_decode_step_noalloc(
     }
     return MK_OK;
 }
+
+#ifdef MK_TRACE
+// Trace builds only: copy the per-CTA timeline of the last step to host memory.
+extern "C" __attribute__((visibility("default"))) int mk_trace_read(void* dst, size_t bytes) {
+    if (bytes > sizeof(mk::g_mk_trace)) bytes = sizeof(mk::g_mk_trace);
+    return (int)cudaMemcpyFromSymbol(dst, mk::g_mk_trace, bytes);
+}
+extern "C" __attribute__((visibility("default"))) int mk_trace_clear() {
+    static ulonglong2 zero[mk::kTraceEvents];
+    for (int c = 0; c < mk::kTraceCtas; ++c)
+        if (cudaMemcpyToSymbol(mk::g_mk_trace, zero, sizeof(zero), sizeof(zero) * c) != cudaSuccess) return 1;
+    return 0;
+}
+#endif

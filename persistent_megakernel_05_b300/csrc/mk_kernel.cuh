@@ -34,16 +34,38 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kThreads = 32 + kConsumerThreads;   // warp 0 = producer
 constexpr int kStages = 6;                         // shared-memory ring depth
-constexpr int KC = 1024;                           // GEMV k-chunk (columns per ring slot)
-constexpr int kRowPitch = KC * 2 + 16;             // padded row pitch: conflict-free ldmatrix
-constexpr int kSlotBytes = 33 * 1024;              // >= 16 * kRowPitch, multiple of 1024
+constexpr int KCW = 2048;                          // GEMV k-chunk: columns of a weight slot
+constexpr int kGroupRows = 8;                      // weight rows per ring slot
+constexpr int kSlotBytes = 33 * 1024;              // >= 8 * (2 * KCW + 16), multiple of 1024
 constexpr int kScratchBytes = 20 * 1024;
 constexpr int kMaxBatch = 8;
 constexpr int kPage = 16;
-constexpr int kTaskRows = 128;                     // <= 8 row groups of 16 per GEMV task
+constexpr int kTaskRows = 128;                     // <= 16 row groups of 8 per GEMV task
 constexpr int kMaxLayers = 128;
 constexpr int kCounterStride = 32;                 // u32 words per counter (128 B apart)
 constexpr int kStagesPerLayer = 8;                 // counter slots per layer
+constexpr int kMaxOwnRows = 32;                    // residual rows a CTA owns: ceil(d / CTAs) <= 32
+constexpr int kMaxSplitsG = 1184;                  // splits (<= CTAs) x G (<= 8): merge staging
+
+// ---- optional timeline trace (compile with -DMK_TRACE; no code otherwise) ----
+#ifdef MK_TRACE
+constexpr int kTraceCtas = 160, kTraceEvents = 2048;  // [cta][consumer 0..1023 | producer 1024..]
+__device__ ulonglong2 g_mk_trace[kTraceCtas][kTraceEvents];
+__device__ __forceinline__ void trace_event(int cta, int& n, int base, uint32_t code, uint32_t arg) {
+    if (cta < kTraceCtas && n < kTraceEvents / 2)
+        g_mk_trace[cta][base + n++] = make_ulonglong2(globaltimer(), ((unsigned long long)code << 32) | arg);
+}
+#define MK_TRACE_C(c, code, arg) do { if ((c).tid == 0) trace_event(blockIdx.x, (c).tn, 0, code, arg); } while (0)
+#define MK_TRACE_P(pr, code, arg) do { if ((pr).lane == 0) trace_event(blockIdx.x, (pr).tn, kTraceEvents / 2, code, arg); } while (0)
+#else
+#define MK_TRACE_C(c, code, arg) do { } while (0)
+#define MK_TRACE_P(pr, code, arg) do { } while (0)
+#endif
+enum TraceCode { TR_WAIT = 1, TR_READY = 2, TR_DONE = 3, TR_PIECE = 4, TR_MERGE = 5, TR_END = 6,
+                 TR_P_STAGE = 11, TR_P_BLOCK = 12, TR_P_GO = 13,
+                 TR_S_WAIT = 20, TR_S_FULL = 21, TR_S_REL = 22, TR_S_ISSUE = 23,
+                 TR_A_Q = 30, TR_A_LOOP = 31, TR_A_PART = 32, TR_A_ARRIVED = 33, TR_A_MERGED = 34,
+                 TR_G_NORM = 40, TR_G_X = 41, TR_G_SUM = 42, TR_G_EPI = 43 };
 
 // error codes (same values as mk_status)
 constexpr int kErrInvalid = 1, kErrBadPage = 5, kErrTimeout = 6, kErrInternal = 7;
@@ -116,6 +138,8 @@ struct Smem {
     float amax_v[kMaxBatch];
     int amax_i[kMaxBatch];
     int pos[kMaxBatch];
+    float ssq[kConsumerWarps][kMaxBatch];  // per-warp sums of squares (fused RMSNorm)
+    float xown[kMaxBatch][kMaxOwnRows];    // this CTA's rows of the residual stream
     volatile int abort;
     int bcast;
     int pad_[6];
@@ -135,6 +159,7 @@ struct Ctx {
     uint32_t ring_s;     // shared address of the ring
     uint32_t seq;        // ring sequence number (slot = seq % kStages)
     int cw, lane, tid;   // consumer warp (0..7), lane, consumer thread id (0..255)
+    int tn;              // trace events recorded (MK_TRACE builds)
 };
 
 // ------------------------------------------------------------------ errors / waits
@@ -168,22 +193,21 @@ __device__ bool poll_counter(const StepArgs& a, Smem* sm, const uint32_t* c, uin
 }
 
 // all consumer threads: wait for a stage counter
-__device__ bool consumer_wait(Ctx& c, int slot, uint32_t target, int task) {
+__device__ __forceinline__ bool consumer_wait(Ctx& c, int slot, uint32_t target, int task) {
     if (c.tid == 0) poll_counter(*c.a, c.sm, c.a->p.counters + slot * kCounterStride, target, task);
     consumer_sync();
     return !c.sm->abort;
 }
 
-__device__ void publish(Ctx& c, int slot, int task) {
+__device__ __forceinline__ void publish(Ctx& c, int slot, int task) {
     consumer_sync();
-    if (c.tid == 0 && !c.sm->abort && c.a->skip_publish != task) {
-        __threadfence();
+    // bar.sync orders every consumer thread's stores before thread 0's release add
+    if (c.tid == 0 && !c.sm->abort && c.a->skip_publish != task)
         red_release_add(c.a->p.counters + slot * kCounterStride, 1u);
-    }
 }
 
 // a consumer warp waits for ring slot `seq` to be full; warp-uniform result
-__device__ bool wait_full(Ctx& c, int task) {
+__device__ __forceinline__ bool wait_full(Ctx& c, int task) {
     const uint32_t slot = c.seq % kStages, parity = (c.seq / kStages) & 1;
     const uint32_t bar = smem_u32(&c.sm->full[slot]);
     int ok = 1;
@@ -192,7 +216,7 @@ __device__ bool wait_full(Ctx& c, int task) {
         else if (!mbar_try_wait(bar, parity)) {
             uint64_t t0 = globaltimer();
             for (int it = 0;; ++it) {
-                if (mbar_try_wait(bar, parity)) break;
+                if (mbar_wait_sleep(bar, parity, 20000u)) break;
                 if (c.sm->abort) { ok = 0; break; }
                 if ((it & 7) == 7) {
                     if (status_bad(c.a->p)) { c.sm->abort = 1; ok = 0; break; }
@@ -274,18 +298,31 @@ __device__ GemvStage make_gemv(const StepArgs& a, int kind, int l) {
     return s;
 }
 
-// rows per task: GU tasks count gate/up row PAIRS (<= 64 pairs = 8 row groups)
+// stages whose individual ring slots are traced in MK_TRACE builds
+__device__ __forceinline__ bool trace_slots(const GemvStage& s) {
+    return s.kind == G_LM || (s.layer == 1 && s.kind == G_GU);
+}
+
+// rows per task: GU tasks count gate/up row PAIRS (<= 64 pairs = 8 + 8 row groups)
 __device__ __forceinline__ int task_rows(int kind) { return kind == G_GU ? kTaskRows / 2 : kTaskRows; }
 
-// weight row `r` of row group `rg` (GU: groups [0, ng/2) are gate, the rest up)
-__device__ __forceinline__ const bf16* gemv_row(const GemvStage& s, int r0, int rg, int ng, int i) {
+// Row groups of 8 weight rows; GU tasks list their gate groups first, then up groups.
+__device__ __forceinline__ int num_groups(const GemvStage& s, int n) {
+    const int g = (n + kGroupRows - 1) / kGroupRows;
+    return s.kind == G_GU ? 2 * g : g;
+}
+__device__ __forceinline__ int group_rows(const GemvStage& s, int n, int gi, int ngate) {
+    const int base = kGroupRows * (s.kind == G_GU ? (gi % ngate) : gi);
+    return min(kGroupRows, n - base);
+}
+// weight row i of row group gi, as a pointer to its first column
+__device__ __forceinline__ const bf16* gemv_row(const GemvStage& s, int r0, int gi, int ngate, int i) {
     if (s.kind == G_GU) {
-        const int half = ng >> 1;
-        const bool up = rg >= half;
-        const int r = r0 + 16 * (up ? rg - half : rg) + i;
+        const bool up = gi >= ngate;
+        const int r = r0 + kGroupRows * (up ? gi - ngate : gi) + i;
         return (up ? s.w1 : s.w0) + (size_t)r * s.K;
     }
-    const int r = r0 + 16 * rg + i;
+    const int r = r0 + kGroupRows * gi + i;
     if (s.kind == G_QKV) {
         if (r < s.split1) return s.w0 + (size_t)r * s.K;
         if (r < s.split2) return s.w1 + (size_t)(r - s.split1) * s.K;
@@ -293,14 +330,31 @@ __device__ __forceinline__ const bf16* gemv_row(const GemvStage& s, int r0, int 
     }
     return s.w0 + (size_t)r * s.K;
 }
-__device__ __forceinline__ int group_rows(const GemvStage& s, int r0, int r1, int rg, int ng) {
-    const int n = r1 - r0;
-    const int base = 16 * (s.kind == G_GU ? (rg % (ng >> 1)) : rg);
-    return min(16, n - base);
-}
-__device__ __forceinline__ int num_groups(const GemvStage& s, int n) {
-    const int g = (n + 15) >> 4;
-    return s.kind == G_GU ? 2 * g : g;
+
+// Shared-memory geometry of one weight slot (8 rows x kc columns of k-chunk k0).
+// When a whole row fits in a chunk (K <= KCW), rpc consecutive rows travel in one
+// contiguous copy of up to 8 KB; otherwise each row segment is its own copy. Copies are
+// 16 B apart so that 8 rows read by ldmatrix fall into distinct (or at most 2-way
+// shared) bank groups.
+struct SlotGeom {
+    int kc, rpc, rpc_log2, cpitch, rowb;  // rowb = kc * 2 (bytes of one row segment)
+    __device__ __forceinline__ int row_off(int r) const {
+        return (r >> rpc_log2) * cpitch + (r & (rpc - 1)) * rowb;
+    }
+};
+__device__ __forceinline__ SlotGeom slot_geom(int K, int k0) {
+    SlotGeom g;
+    g.kc = min(KCW, K - k0);
+    int lg = 0;
+    if (K <= KCW) {
+        const int r = 4096 / K;
+        lg = r >= 8 ? 3 : r >= 4 ? 2 : r >= 2 ? 1 : 0;
+    }
+    g.rpc_log2 = lg;
+    g.rpc = 1 << lg;
+    g.rowb = g.kc * 2;
+    g.cpitch = g.rpc * g.rowb + 16;
+    return g;
 }
 
 // ---- attention work partition (identical in producer and consumers) ----
@@ -349,56 +403,84 @@ __device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta
     }
 }
 
-// ------------------------------------------------------------------ producer (1 thread)
+// ------------------------------------------------------------------ producer (warp 0)
+// All 32 lanes walk the same schedule (warp-uniform control flow); lane 0 owns the
+// ring barriers and up to 16 lanes issue the row / page copies of a slot in parallel.
 struct Producer {
     const StepArgs* a;
     Smem* sm;
     uint32_t ring_s;
     uint32_t seq = 0;
     uint64_t policy;
+    int lane;
+    int tn = 0;  // trace events recorded (MK_TRACE builds)
 
     __device__ bool acquire_slot(int task) {
-        if (sm->abort) return false;
-        if (seq >= (uint32_t)kStages) {
-            const uint32_t bar = smem_u32(&sm->empty[seq % kStages]);
-            const uint32_t parity = ((seq / kStages) - 1) & 1;
-            if (!mbar_try_wait(bar, parity)) {
-                uint64_t t0 = globaltimer();
-                for (int it = 0;; ++it) {
-                    if (mbar_try_wait(bar, parity)) break;
-                    if (sm->abort) return false;
-                    if ((it & 7) == 7) {
-                        if (status_bad(a->p)) { sm->abort = 1; return false; }
-                        if ((long long)(globaltimer() - t0) > a->timeout_ns) {
-                            set_error(a->p, sm, kErrTimeout, task);
-                            return false;
+        int ok = 1;
+        if (lane == 0) {
+            if (sm->abort) ok = 0;
+            else if (seq >= (uint32_t)kStages) {
+                const uint32_t bar = smem_u32(&sm->empty[seq % kStages]);
+                const uint32_t parity = ((seq / kStages) - 1) & 1;
+                if (!mbar_try_wait(bar, parity)) {
+                    MK_TRACE_P(*this, TR_P_BLOCK, task);
+                    uint64_t t0 = globaltimer();
+                    for (int it = 0;; ++it) {
+                        if (mbar_wait_sleep(bar, parity, 20000u)) break;
+                        if (sm->abort) { ok = 0; break; }
+                        if ((it & 7) == 7) {
+                            if (status_bad(a->p)) { sm->abort = 1; ok = 0; break; }
+                            // a full ring only stalls when a consumer stalls; let the
+                            // consumer's own (shorter) wait report the cause first
+                            if ((long long)(globaltimer() - t0) > 4 * a->timeout_ns) {
+                                set_error(a->p, sm, kErrTimeout, task);
+                                ok = 0;
+                                break;
+                            }
                         }
                     }
+                    MK_TRACE_P(*this, TR_P_GO, task);
                 }
             }
         }
-        return true;
+        return __shfl_sync(0xffffffffu, ok, 0) != 0;
     }
     __device__ uint32_t slot_addr() const { return ring_s + (seq % kStages) * kSlotBytes; }
     __device__ uint32_t full_bar() const { return smem_u32(&sm->full[seq % kStages]); }
 
     __device__ bool gemv(const GemvStage& s, int cta) {
+        MK_TRACE_P(*this, TR_P_STAGE, s.task_id);
         int a0, a1;
         cta_rows(s.R, cta, a->p.C, a0, a1);
         const int tr = task_rows(s.kind);
         for (int r0 = a0; r0 < a1; r0 += tr) {
             const int r1 = min(a1, r0 + tr);
-            const int ng = num_groups(s, r1 - r0);
-            for (int k0 = 0; k0 < s.K; k0 += KC) {
-                const int kc = min(KC, s.K - k0);
-                for (int rg = 0; rg < ng; ++rg) {
+            const int n = r1 - r0;
+            const int ng = num_groups(s, n), ngate = s.kind == G_GU ? ng / 2 : ng;
+            for (int k0 = 0; k0 < s.K; k0 += KCW) {
+                const SlotGeom geo = slot_geom(s.K, k0);
+                for (int gi = 0; gi < ng; ++gi) {
                     if (!acquire_slot(s.task_id)) return false;
-                    const int nr = group_rows(s, r0, r1, rg, ng);
+                    const int nr = group_rows(s, n, gi, ngate);
+                    const int ncop = (nr + geo.rpc - 1) / geo.rpc;
                     const uint32_t dst = slot_addr(), bar = full_bar();
-                    mbar_arrive_expect_tx(bar, (uint32_t)(nr * kc * 2));
-                    for (int i = 0; i < nr; ++i)
-                        tma_load_1d(dst + i * kRowPitch, gemv_row(s, r0, rg, ng, i) + k0,
-                                    (uint32_t)(kc * 2), bar, policy);
+                    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nr * geo.kc * 2));
+                    __syncwarp();
+                    if (lane < ncop) {
+                        const int i0 = lane * geo.rpc;
+                        const int cnt = min(geo.rpc, nr - i0);
+                        const bf16* p0 = gemv_row(s, r0, gi, ngate, i0) + k0;
+                        const bf16* p1 = gemv_row(s, r0, gi, ngate, i0 + cnt - 1) + k0;
+                        const uint32_t d0 = dst + lane * geo.cpitch;
+                        if (p1 == p0 + (size_t)(cnt - 1) * s.K) {
+                            tma_load_1d(d0, p0, (uint32_t)(cnt * geo.kc * 2), bar, policy);
+                        } else {  // the rows straddle two weight tensors (q|k|v)
+                            for (int i = 0; i < cnt; ++i)
+                                tma_load_1d(d0 + i * geo.kc * 2, gemv_row(s, r0, gi, ngate, i0 + i) + k0,
+                                            (uint32_t)(geo.kc * 2), bar, policy);
+                        }
+                    }
+                    if (trace_slots(s)) MK_TRACE_P(*this, TR_S_ISSUE, seq);
                     ++seq;
                 }
             }
@@ -409,7 +491,9 @@ struct Producer {
     template <int HD>
     __device__ bool attention(int l, int cta) {
         const Plan& p = a->p;
-        constexpr int PPS = 512 / HD;  // pages per ring slot (K + V of one kv head)
+        constexpr int PPS = 512 / HD;   // pages per ring slot (K + V of one kv head)
+        constexpr int NB = HD / 64;     // 64-wide boxes per page row
+        MK_TRACE_P(*this, TR_P_STAGE, l * 16 + ST_ATTN);
         bool ok = true;
         for_each_piece(*a, sm, l, cta, [&](int b, int g, const SeqSpan& sp, int u, int n,
                                            int split, int nsplit) {
@@ -418,24 +502,28 @@ struct Producer {
             for (int st = 0; st < n; st += PPS) {
                 const int np = min(PPS, n - st);
                 if (!acquire_slot(l * 16 + ST_ATTN)) { ok = false; return; }
-                int pages[PPS];
-                for (int i = 0; i < np; ++i) {
-                    pages[i] = __ldg(pt + sp.p0 + u + st + i);
-                    if (pages[i] < 0 || pages[i] >= p.num_pages) {
-                        set_error(p, sm, kErrBadPage, l * 16 + ST_ATTN);
-                        ok = false;
-                        return;
-                    }
+                const int nbox = np * 2 * NB;  // <= 16
+                const int i = lane / (2 * NB), kv = (lane / NB) & 1, bx = lane % NB;
+                int page = 0;
+                bool bad = false;
+                if (lane < nbox) {
+                    page = __ldg(pt + sp.p0 + u + st + i);
+                    bad = page < 0 || page >= p.num_pages;
+                }
+                if (__any_sync(0xffffffffu, bad)) {
+                    if (lane == 0) set_error(p, sm, kErrBadPage, l * 16 + ST_ATTN);
+                    ok = false;
+                    return;
                 }
                 const uint32_t dst = slot_addr(), bar = full_bar();
-                mbar_arrive_expect_tx(bar, (uint32_t)(np * 2 * 2 * kPage * HD));
-                for (int i = 0; i < np; ++i)
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const int row = (((l * p.num_pages + pages[i]) * 2 + kv) * p.Hkv + g) * kPage;
-                        for (int bx = 0; bx < HD / 64; ++bx)
-                            tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, p.kv_map,
-                                        bx * 64, row, bar, policy);
-                    }
+                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(np * 2 * 2 * kPage * HD));
+                __syncwarp();
+                if (lane < nbox) {
+                    const int row = (((l * p.num_pages + page) * 2 + kv) * p.Hkv + g) * kPage;
+                    tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, p.kv_map, bx * 64, row,
+                                bar, policy);
+                }
+                if (l == 1) MK_TRACE_P(*this, TR_S_ISSUE, seq);
                 ++seq;
             }
         });
@@ -443,9 +531,9 @@ struct Producer {
     }
 
     template <int HD>
-    __device__ void run(int cta) {
+    __device__ __noinline__ void run(int cta) {
         policy = policy_evict_first();
-        prefetch_tmap(a->p.kv_map);
+        if (lane == 0) prefetch_tmap(a->p.kv_map);
         const Plan& p = a->p;
         bool ok = !sm->abort;
         for (int l = 0; l < p.L && ok; ++l) {
@@ -457,22 +545,25 @@ struct Producer {
         }
         if (ok) gemv(make_gemv(*a, G_LM, 0), cta);
         // drain: never leave a copy in flight into shared memory
-        const uint32_t first = seq > (uint32_t)kStages ? seq - kStages : 0;
-        for (uint32_t k = first; k < seq; ++k) {
-            const uint32_t bar = smem_u32(&sm->full[k % kStages]);
-            const uint32_t parity = (k / kStages) & 1;
-            uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(bar, parity))
-                if ((long long)(globaltimer() - t0) > a->timeout_ns) {
-                    set_error(p, sm, kErrInternal, -3);
-                    break;
-                }
+        if (lane == 0) {
+            const uint32_t first = seq > (uint32_t)kStages ? seq - kStages : 0;
+            for (uint32_t k = first; k < seq; ++k) {
+                const uint32_t bar = smem_u32(&sm->full[k % kStages]);
+                const uint32_t parity = (k / kStages) & 1;
+                uint64_t t0 = globaltimer();
+                while (!mbar_wait_sleep(bar, parity, 20000u))
+                    if ((long long)(globaltimer() - t0) > a->timeout_ns) {
+                        set_error(p, sm, kErrInternal, -3);
+                        break;
+                    }
+            }
         }
+        __syncwarp();
     }
 };
 
 // ------------------------------------------------------------------ consumer pieces
-__device__ void rms_scale(Ctx& c, const float* src, int K) {
+__device__ __forceinline__ void rms_scale(Ctx& c, const float* src, int K) {
     // rstd[b] = 1 / sqrt(mean(src[b]^2) + eps); fixed summation order
     const StepArgs& a = *c.a;
     float* red = c.scratch;
@@ -496,26 +587,275 @@ __device__ void rms_scale(Ctx& c, const float* src, int K) {
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+__device__ __forceinline__ int cta_of(const Ctx&) { return blockIdx.x; }
 
-__device__ __noinline__ void gemv_task(Ctx& c, const GemvStage& s, int r0, int r1) {
+// the small-batch path computes the RMSNorm statistics from its own activation loads
+// when the whole input row is one k-chunk
+__device__ __forceinline__ bool fused_norm_stage(const StepArgs& a, const GemvStage& s) {
+    return a.B <= 4 && s.K <= KCW;
+}
+
+// a consumer warp waits for ring slot `q` to be full; warp-uniform result. Fast path:
+// every lane tests the barrier once (an acquire for each lane) and the warp votes.
+__device__ __forceinline__ bool wait_full_at(Ctx& c, uint32_t q, int task) {
+    const uint32_t slot = q % kStages, parity = (q / kStages) & 1;
+    const uint32_t bar = smem_u32(&c.sm->full[slot]);
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    int ok = 1;
+    if (c.lane == 0) {
+        uint64_t t0 = globaltimer();
+        for (int it = 0;; ++it) {
+            if (mbar_wait_sleep(bar, parity, 20000u)) break;
+            if (c.sm->abort) { ok = 0; break; }
+            if ((it & 7) == 7) {
+                if (status_bad(c.a->p)) { c.sm->abort = 1; ok = 0; break; }
+                if ((long long)(globaltimer() - t0) > c.a->timeout_ns) {
+                    set_error(c.a->p, c.sm, kErrTimeout, task);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_try_wait(bar, parity);  // every lane acquires the completed phase
+    return ok != 0;
+}
+__device__ __forceinline__ void release_at(Ctx& c, uint32_t q) {
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(smem_u32(&c.sm->empty[q % kStages]));
+}
+
+// Sum of V = 8 * BP per-lane values over the 32 lanes of a warp, transposed: after the
+// halving steps lane L holds the total of value index idx(L) (returned through `idx`).
+template <int BP>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[8 * BP], int lane, int& idx) {
+    constexpr int V = 8 * BP;
+    idx = 0;
+    int o = 16;
+#pragma unroll
+    for (int h = V / 2; h >= 1; h >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = up ? v[i] : v[i + h];
+            const float keep = up ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+        if (up) idx += h;
+    }
+    for (; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    return v[0];
+}
+
+// Small batches (B <= 4): exact fp32 CUDA-core dot products. Each lane owns one 8-column
+// piece of the k-chunk (a 16 B read of every row), with the piece's activations in
+// registers. The 8 x BP partial sums of 32 / (8 BP) consecutive slots are reduced across
+// the warp together (32 values, one per lane at the end), then summed over warps in a
+// fixed order. When the whole input row is one chunk the RMSNorm statistics come from
+// the same loads. Writes yout[vrow][8].
+template <int BP>
+__device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int r1, float* yout,
+                                         bool fused_norm) {
+    constexpr int SB = 4 / BP;  // slots per reduction batch (8 * BP * SB = 32 values)
+    const StepArgs& a = *c.a;
+    const int B = a.B;
+    const int n = r1 - r0, ng = num_groups(s, n), ngate = s.kind == G_GU ? ng / 2 : ng;
+    float* red = c.scratch;  // [8 warps][128 vrows][BP]
+    for (int i = c.lane; i < kTaskRows * BP; i += 32) red[c.cw * kTaskRows * BP + i] = 0.f;
+    __syncwarp();
+    for (int k0 = 0; k0 < s.K; k0 += KCW) {
+        const SlotGeom geo = slot_geom(s.K, k0);
+        const int piece = 32 * c.cw + c.lane;
+        const bool has_p = piece < (geo.kc >> 3);
+        float xv[BP][8];
+#pragma unroll
+        for (int b = 0; b < BP; ++b)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xv[b][i] = 0.f;
+        const int col = k0 + 8 * piece;
+        const int base = (col & ~63) + 2 * ((col >> 3) & 7);  // permuted pair (t = 0)
+        if (has_p && !c.sm->abort) {
+#pragma unroll
+            for (int b = 0; b < BP; ++b)
+                if (b < B)
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float2 v = __ldcg(reinterpret_cast<const float2*>(s.src + (size_t)b * s.K + base + 16 * t));
+                        xv[b][2 * t] = v.x;
+                        xv[b][2 * t + 1] = v.y;
+                    }
+        }
+        if (s.gain) {
+            if (fused_norm) {  // this chunk is the whole row: sum of squares from registers
+#pragma unroll
+                for (int b = 0; b < BP; ++b) {
+                    float ss = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ss += xv[b][i] * xv[b][i];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                    if (c.lane == 0) c.sm->ssq[c.cw][b] = ss;
+                }
+                consumer_sync();
+            }
+            float rs[BP];
+#pragma unroll
+            for (int b = 0; b < BP; ++b) {
+                if (fused_norm) {  // every thread folds the 8 warp sums itself: no second barrier
+                    float ss = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) ss += c.sm->ssq[w][b];
+                    rs[b] = b < B ? rsqrtf(ss / (float)s.K + a.p.eps) : 0.f;
+                } else {
+                    rs[b] = b < B ? c.sm->rstd[b] : 0.f;
+                }
+            }
+            if (has_p) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 gg = __ldg(reinterpret_cast<const float2*>(s.gain + base + 16 * t));
+#pragma unroll
+                    for (int b = 0; b < BP; ++b) {
+                        xv[b][2 * t] *= rs[b] * gg.x;
+                        xv[b][2 * t + 1] *= rs[b] * gg.y;
+                    }
+                }
+            }
+        }
+        if (trace_slots(s)) MK_TRACE_C(c, TR_G_X, 0);
+        uint32_t roff[8];  // byte offset of row r (this lane's piece) inside a slot
+#pragma unroll
+        for (int r = 0; r < 8; ++r) roff[r] = (uint32_t)(geo.row_off(r) + 16 * piece);
+        for (int gb = 0; gb < ng; gb += SB) {
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+#pragma unroll
+            for (int j = 0; j < SB; ++j) {
+                const int gi = gb + j;
+                if (gi < ng) {
+                    const int nr = group_rows(s, n, gi, ngate);
+                    if (trace_slots(s)) MK_TRACE_C(c, TR_S_WAIT, c.seq);
+                    const bool ok = wait_full_at(c, c.seq, s.task_id);
+                    if (trace_slots(s)) MK_TRACE_C(c, TR_S_FULL, c.seq);
+                    uint4 wr[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) wr[r] = make_uint4(0u, 0u, 0u, 0u);
+                    if (ok && has_p) {
+                        const uint32_t slot = c.ring_s + (c.seq % kStages) * kSlotBytes;
+#pragma unroll
+                        for (int r = 0; r < 8; ++r)
+                            if (r < nr)
+                                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                             : "=r"(wr[r].x), "=r"(wr[r].y), "=r"(wr[r].z), "=r"(wr[r].w)
+                                             : "r"(slot + roff[r]));
+                    }
+                    release_at(c, c.seq);  // the rows are in registers: hand the slot back
+                    if (trace_slots(s)) MK_TRACE_C(c, TR_S_REL, c.seq);
+                    c.seq++;
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const uint32_t w[4] = {wr[r].x, wr[r].y, wr[r].z, wr[r].w};
+#pragma unroll
+                        for (int b = 0; b < BP; ++b) {
+                            float sacc = 0.f;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                sacc = fmaf(__uint_as_float(w[q] << 16), xv[b][2 * q], sacc);
+                                sacc = fmaf(__uint_as_float(w[q] & 0xffff0000u), xv[b][2 * q + 1], sacc);
+                            }
+                            acc[(j * 8 + r) * BP + b] = sacc;
+                        }
+                    }
+                }
+            }
+            int idx;  // = lane: (slot j, row r, batch b) = idx / (8 BP), (idx / BP) % 8, idx % BP
+            const float v = warp_transpose_reduce<4>(acc, c.lane, idx);
+            const int j = idx / (8 * BP), r = (idx / BP) & 7, b = idx % BP;
+            if (gb + j < ng) red[(c.cw * kTaskRows + (gb + j) * kGroupRows + r) * BP + b] += v;
+        }
+    }
+    consumer_sync();
+    if (trace_slots(s)) MK_TRACE_C(c, TR_G_SUM, 0);
+    if (yout)
+        for (int e = c.tid; e < ng * kGroupRows * 8; e += kConsumerThreads) {
+            const int vr = e >> 3, b = e & 7;
+            float y = 0.f;
+            if (b < BP) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) y += red[(w * kTaskRows + vr) * BP + b];
+            }
+            yout[e] = y;
+        }
+}
+
+// Epilogues of the small-batch path straight from the per-warp partials (no staging,
+// no extra barrier): store q|k|v, residual add into the owned rows, or SiLU(gate) * up.
+template <int BP>
+__device__ __forceinline__ void fma_epilogue(Ctx& c, const GemvStage& s, int r0, int r1, int cta) {
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
-    const int ng = num_groups(s, r1 - r0);
+    const int B = a.B, n = r1 - r0;
+    const float* red = c.scratch;
+    auto ysum = [&](int vr, int b) {
+        float y = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) y += red[(w * kTaskRows + vr) * BP + b];
+        return y;
+    };
+    switch (s.kind) {
+        case G_QKV:
+            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+                const int r = e / B, b = e % B;
+                p.qkv[(size_t)b * p.qkv_rows + r0 + r] = ysum(r, b);
+            }
+            break;
+        case G_O:
+        case G_DOWN: {
+            int a0, a1;
+            cta_rows(p.d, cta, p.C, a0, a1);
+            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+                const int r = e / B, b = e % B;
+                const float xn = c.sm->xown[b][r0 + r - a0] + ysum(r, b);
+                c.sm->xown[b][r0 + r - a0] = xn;
+                p.x[(size_t)b * p.d + perm_col(r0 + r)] = xn;
+            }
+            break;
+        }
+        default: {  // G_GU
+            const int up0 = kGroupRows * (num_groups(s, n) >> 1);
+            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+                const int r = e / B, b = e % B;
+                p.h[(size_t)b * p.F + perm_col(r0 + r)] = silu(ysum(r, b)) * ysum(up0 + r, b);
+            }
+            break;
+        }
+    }
+}
+
+// Larger batches: BF16 mma.sync tiles of 16 weight rows (two consecutive slots) as the
+// A operand and the batch rows as the 8 B columns, activations split hi + lo.
+__device__ __forceinline__ void gemv_mma(Ctx& c, const GemvStage& s, int r0, int r1, float* yout) {
+    const StepArgs& a = *c.a;
+    const int n = r1 - r0, ng = num_groups(s, n);
+    const int nt = (ng + 1) >> 1;  // 16-row tiles
     const int g = c.lane >> 2, t = c.lane & 3;
     const bool has_b = g < a.B;
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     const float rs = has_b ? c.sm->rstd[g] : 0.f;
+    // ldmatrix lane -> (tile row, chunk): lanes 0-7 rows 0-7 chunk X, 8-15 rows 8-15
+    // chunk X (second slot), 16-23 rows 0-7 chunk X+1, 24-31 rows 8-15 chunk X+1
+    const int lrow = c.lane & 7, lhalf = (c.lane >> 3) & 1, lch = c.lane >> 4;
 
-    for (int k0 = 0; k0 < s.K; k0 += KC) {
-        const int kc = min(KC, s.K - k0);
-        const int nblk = kc >> 6;
-        // B fragments (activations) for this warp's 64-column blocks cw and cw + 8
-        // [jj][mma i][0,1 = hi b0b1, b2b3; 2,3 = lo b0b1, b2b3]
-        uint32_t bfr[2][4][4];
+    for (int k0 = 0; k0 < s.K; k0 += KCW) {
+        const SlotGeom geo = slot_geom(s.K, k0);
+        const int nblk = geo.kc >> 6;
+        uint32_t bfr[4][4][4];  // [block][k-step][hi b0b1, hi b2b3, lo b0b1, lo b2b3]
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
+        for (int jj = 0; jj < 4; ++jj) {
             const int j = c.cw + 8 * jj;
 #pragma unroll
             for (int i = 0; i < 4; ++i) bfr[jj][i][0] = bfr[jj][i][1] = bfr[jj][i][2] = bfr[jj][i][3] = 0u;
@@ -535,68 +875,109 @@ __device__ __noinline__ void gemv_task(Ctx& c, const GemvStage& s, int r0, int r
             }
         }
 #pragma unroll
-        for (int rg = 0; rg < 8; ++rg) {
-            if (rg < ng) {
-                const bool ok = wait_full(c, s.task_id);
+        for (int ti = 0; ti < 8; ++ti) {
+            if (ti < nt) {
+                const bool two = 2 * ti + 1 < ng;
+                const uint32_t qa = c.seq, qb = c.seq + 1;
+                bool ok = wait_full_at(c, qa, s.task_id);
+                if (two) ok = wait_full_at(c, qb, s.task_id) && ok;
                 if (ok) {
-                    const uint32_t slot = c.ring_s + (c.seq % kStages) * kSlotBytes;
-                    // ldmatrix lane -> (row, chunk): lanes 0-7 rows 0-7 chunk X, 8-15 rows
-                    // 8-15 chunk X, 16-23 rows 0-7 chunk X+1, 24-31 rows 8-15 chunk X+1
-                    const int lrow = (c.lane & 7) + ((c.lane >> 3) & 1) * 8;
-                    const int lch = c.lane >> 4;
+                    const uint32_t sa = c.ring_s + (qa % kStages) * kSlotBytes;
+                    const uint32_t sb = two ? c.ring_s + (qb % kStages) * kSlotBytes : sa;
+                    const uint32_t rowaddr = (lhalf ? sb : sa) + geo.row_off(lrow);
+                    // four independent accumulator chains (hi/lo x even/odd k-step) keep
+                    // the tensor pipe busy instead of waiting on one serial chain
+                    float ct[4][4];
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
+                    for (int q = 0; q < 4; ++q) ct[q][0] = ct[q][1] = ct[q][2] = ct[q][3] = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
                         const int j = c.cw + 8 * jj;
                         if (j < nblk) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const int chunk = 8 * j + 2 * i + lch;
                                 uint32_t a0, a1, a2, a3;
-                                ldmatrix_x4(slot + lrow * kRowPitch + chunk * 16, a0, a1, a2, a3);
-                                mma_16816(acc[rg], a0, a1, a2, a3, bfr[jj][i][0], bfr[jj][i][1]);
-                                mma_16816(acc[rg], a0, a1, a2, a3, bfr[jj][i][2], bfr[jj][i][3]);
+                                ldmatrix_x4(rowaddr + chunk * 16, a0, a1, a2, a3);
+                                mma_16816(ct[(i & 1) * 2], a0, a1, a2, a3, bfr[jj][i][0], bfr[jj][i][1]);
+                                mma_16816(ct[(i & 1) * 2 + 1], a0, a1, a2, a3, bfr[jj][i][2], bfr[jj][i][3]);
                             }
                         }
                     }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[ti][e] += (ct[0][e] + ct[1][e]) + (ct[2][e] + ct[3][e]);
                 }
-                release_slot(c);
+                release_at(c, qa);
+                if (two) release_at(c, qb);
+                c.seq += two ? 2 : 1;
             }
         }
     }
-
-    // cross-warp reduction: red[w][rr][row][col] in rounds of 4 row groups
-    float* red = c.scratch;                       // 8*4*16*8 floats = 16 KB
-    float* yout = c.scratch + 8 * 4 * 16 * 8;     // [8 rg][16][8]
+    // cross-warp reduction: red[w][tile][16 rows][8 cols] in rounds of 4 tiles
+    float* red = c.scratch;
 #pragma unroll
     for (int round = 0; round < 2; ++round) {
-        if (round * 4 < ng) {
+        if (round * 4 < nt) {
             consumer_sync();
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
-                const int rg = round * 4 + rr;
-                if (rg < ng) {
+                const int ti = round * 4 + rr;
+                if (ti < nt) {
                     float* base = red + ((c.cw * 4 + rr) * 16) * 8;
-                    *reinterpret_cast<float2*>(base + g * 8 + 2 * t) = make_float2(acc[rg][0], acc[rg][1]);
-                    *reinterpret_cast<float2*>(base + (g + 8) * 8 + 2 * t) = make_float2(acc[rg][2], acc[rg][3]);
+                    *reinterpret_cast<float2*>(base + g * 8 + 2 * t) = make_float2(acc[ti][0], acc[ti][1]);
+                    *reinterpret_cast<float2*>(base + (g + 8) * 8 + 2 * t) = make_float2(acc[ti][2], acc[ti][3]);
                 }
             }
             consumer_sync();
             for (int e = c.tid; e < 4 * 16 * 8; e += kConsumerThreads) {
                 const int rr = e >> 7, rem = e & 127;
-                const int rg = round * 4 + rr;
-                if (rg < ng) {
+                const int ti = round * 4 + rr;
+                if (ti < nt) {
                     float y = 0.f;
 #pragma unroll
                     for (int w = 0; w < kConsumerWarps; ++w) y += red[(w * 4 + rr) * 128 + rem];
-                    yout[rg * 128 + rem] = y;
+                    yout[ti * 128 + rem] = y;  // vrow = 16 ti + row = 8 * group + row
                 }
             }
         }
     }
-    consumer_sync();
-    if (c.sm->abort) return;
+}
 
-    // epilogues
+// Non-inlined (own register budget). Works on register copies of the context and of
+// the stage description; only the ring sequence number goes back to the caller.
+__device__ __noinline__ void gemv_task(Ctx& c_in, int kind, int layer, int r0, int r1) {
+    Ctx c = c_in;
+    const StepArgs& a = *c.a;
+    const Plan& p = a.p;
+    const GemvStage s = make_gemv(a, kind, layer);
+    float* yout = c.scratch + kConsumerWarps * kTaskRows * 4;  // [128 vrows][8]
+    const bool fused = fused_norm_stage(a, s);
+    if (a.B <= 4 && s.kind != G_LM) {
+        if (a.B == 1) gemv_fma<1>(c, s, r0, r1, nullptr, fused);
+        else if (a.B == 2) gemv_fma<2>(c, s, r0, r1, nullptr, fused);
+        else gemv_fma<4>(c, s, r0, r1, nullptr, fused);
+        if (!c.sm->abort) {
+            if (a.B == 1) fma_epilogue<1>(c, s, r0, r1, cta_of(c));
+            else if (a.B == 2) fma_epilogue<2>(c, s, r0, r1, cta_of(c));
+            else fma_epilogue<4>(c, s, r0, r1, cta_of(c));
+        }
+        if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
+        c_in.seq = c.seq;
+        c_in.tn = c.tn;
+        return;
+    }
+    if (a.B == 1) gemv_fma<1>(c, s, r0, r1, yout, fused);
+    else if (a.B == 2) gemv_fma<2>(c, s, r0, r1, yout, fused);
+    else if (a.B <= 4) gemv_fma<4>(c, s, r0, r1, yout, fused);
+    else gemv_mma(c, s, r0, r1, yout);
+    consumer_sync();
+    if (c.sm->abort) {
+        c_in.seq = c.seq;
+        c_in.tn = c.tn;
+        return;
+    }
+
+    // epilogues (vrow = 8 * group + row; GU: up rows start at vrow 8 * ngate)
     const int n = r1 - r0;
     const int B = a.B;
     switch (s.kind) {
@@ -607,19 +988,23 @@ __device__ __noinline__ void gemv_task(Ctx& c, const GemvStage& s, int r0, int r
             }
             break;
         case G_O:
-        case G_DOWN:
+        case G_DOWN: {
+            int a0, a1;
+            cta_rows(p.d, cta_of(c), p.C, a0, a1);
             for (int e = c.tid; e < n * B; e += kConsumerThreads) {
                 const int r = e / B, b = e % B;
-                float* xp = p.x + (size_t)b * p.d + perm_col(r0 + r);
-                *xp = __ldcg(xp) + yout[r * 8 + b];
+                const float xn = c.sm->xown[b][r0 + r - a0] + yout[r * 8 + b];
+                c.sm->xown[b][r0 + r - a0] = xn;
+                p.x[(size_t)b * p.d + perm_col(r0 + r)] = xn;
             }
             break;
+        }
         case G_GU: {
-            const int half = ng >> 1;
+            const int up0 = kGroupRows * (num_groups(s, n) >> 1);
             for (int e = c.tid; e < n * B; e += kConsumerThreads) {
                 const int r = e / B, b = e % B;
                 const float yg = yout[r * 8 + b];
-                const float yu = yout[(half * 16 + r) * 8 + b];
+                const float yu = yout[(up0 + r) * 8 + b];
                 p.h[(size_t)b * p.F + perm_col(r0 + r)] = silu(yg) * yu;
             }
             break;
@@ -653,6 +1038,9 @@ __device__ __noinline__ void gemv_task(Ctx& c, const GemvStage& s, int r0, int r
             break;
         }
     }
+    if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
+    c_in.seq = c.seq;
+    c_in.tn = c.tn;
 }
 
 __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
@@ -660,18 +1048,146 @@ __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
     int a0, a1;
     cta_rows(s.R, cta, p.C, a0, a1);
     if (a0 < a1) {
+        MK_TRACE_C(c, TR_WAIT, s.task_id);
         consumer_wait(c, s.cnt_wait, s.wait_target, s.task_id);
-        if (s.gain) rms_scale(c, s.src, s.K);
+        MK_TRACE_C(c, TR_READY, s.task_id);
+        if (s.gain && !fused_norm_stage(*c.a, s)) rms_scale(c, s.src, s.K);
+        if (trace_slots(s)) MK_TRACE_C(c, TR_G_NORM, 0);
         const int tr = task_rows(s.kind);
-        for (int r0 = a0; r0 < a1; r0 += tr) gemv_task(c, s, r0, min(a1, r0 + tr));
+        for (int r0 = a0; r0 < a1; r0 += tr) gemv_task(c, s.kind, s.layer, r0, min(a1, r0 + tr));
     }
     if (s.kind != G_LM) publish(c, s.cnt_pub, s.task_id);
+    MK_TRACE_C(c, TR_DONE, s.task_id);
 }
 
+__device__ __forceinline__ int bg_id(const Plan& p, int b, int g) { return b * p.Hkv + g; }
+
 // ---- attention: one piece (a CTA's share of one (b, kv head)) ----
+// After the key loop of a piece: merge the 8 warps' partial softmax states (left in
+// shared memory by the loop), write this split's partial, count the arrival, and if it
+// is the last split of its (sequence, kv head), merge all splits into the attention
+// output and publish. Non-inlined so the key loop keeps its registers to itself.
 template <int HD>
-__device__ __noinline__ void attention_piece(Ctx& c, int l, int b, int g, const SeqSpan& sp, int u, int n,
-                                int split, int nsplit) {
+__device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, int split, int nsplit) {
+    Ctx c = c_in;
+    const StepArgs& a = *c.a;
+    const Plan& p = a.p;
+    const int G = p.G;
+    const int task = l * 16 + ST_ATTN;
+    float* ws_o = c.scratch;                                  // [8][G][HD]
+    float* ws_m = c.scratch + kConsumerWarps * 512;           // [8][8]
+    float* ws_l = ws_m + 64;                                  // [8][8]
+    consumer_sync();
+    const int bg = b * p.Hkv + g;
+    const size_t pbase = ((size_t)bg * p.C + split) * G;
+    if (!c.sm->abort) {
+        for (int e = c.tid; e < G * HD; e += kConsumerThreads) {
+            const int hl = e / HD, d = e % HD;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ws_m[w * 8 + hl]);
+            float o = 0.f, L = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = ws_m[w * 8 + hl];
+                const float f = mw == -INFINITY ? 0.f : expf(mw - M);
+                o += f * ws_o[(w * G + hl) * HD + d];
+                L += f * ws_l[w * 8 + hl];
+            }
+            p.part_o[(pbase + hl) * HD + d] = o;
+            if (d == 0) p.part_ml[pbase + hl] = make_float2(M, L);
+        }
+    }
+    // arrival: the last of the nsplit pieces merges them all
+    consumer_sync();
+    if (l == 0) MK_TRACE_C(c, TR_A_PART, (uint32_t)nsplit);
+    if (c.tid == 0) {
+        int last = 0;
+        if (!c.sm->abort) {
+            uint32_t* ctr = p.arrivals + ((size_t)l * p.maxB * p.Hkv + bg) * kCounterStride;
+            const uint32_t old = atom_acq_rel_add(ctr, 1u);
+            if (old == (uint32_t)(nsplit - 1)) { last = 1; st_relaxed(ctr, 0u); }
+        }
+        c.sm->bcast = last;
+    }
+    consumer_sync();
+    if (l == 0) MK_TRACE_C(c, TR_A_ARRIVED, (uint32_t)c.sm->bcast);
+    if (c.sm->bcast) {
+        // 1) all (m, l) of the nsplit partials into shared memory in one parallel pass
+        const size_t base0 = (size_t)bg * p.C * G;
+        float2* mls = reinterpret_cast<float2*>(c.scratch);     // [nsplit][G]
+        float* fw = c.scratch + 2 * kMaxSplitsG;                // [nsplit][G] weights
+        float* Ls = fw + kMaxSplitsG;                           // [G]
+        for (int i = c.tid; i < nsplit * G; i += kConsumerThreads) mls[i] = __ldcg(&p.part_ml[base0 + i]);
+        consumer_sync();
+        // 2) per head (one warp each): M = max m_s, w_s = exp(m_s - M), L = sum w_s l_s
+        if (c.cw < G) {
+            const int hl = c.cw;
+            float M = -INFINITY;
+            for (int i = c.lane; i < nsplit; i += 32) M = fmaxf(M, mls[i * G + hl].x);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            float L = 0.f;
+            for (int i = c.lane; i < nsplit; i += 32) {
+                const float2 ml = mls[i * G + hl];
+                const float f = expf(ml.x - M);
+                fw[i * G + hl] = f;
+                L += f * ml.y;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+            if (c.lane == 0) Ls[hl] = L;
+        }
+        consumer_sync();
+        // 3) O = sum_s w_s o_s / L: threads own 4 consecutive dims of one head; the splits
+        //    are dealt to kRep threads per quad and combined with shuffles
+        constexpr int kQuads = 8 * HD / 4;  // upper bound of G * HD / 4
+        const int nquad = G * HD / 4;
+        const int rep = kConsumerThreads / nquad >= 4 ? 4 : kConsumerThreads / nquad >= 2 ? 2 : 1;
+        (void)kQuads;
+        const int quad = c.tid / rep, sub = c.tid % rep;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        int hl = 0, d = 0;
+        if (quad < nquad) {
+            hl = (quad * 4) / HD;
+            d = (quad * 4) % HD;
+            const float4* po = reinterpret_cast<const float4*>(p.part_o + (base0 + hl) * HD + d);
+            const size_t stride4 = (size_t)G * HD / 4;
+#pragma unroll 4
+            for (int sidx = sub; sidx < nsplit; sidx += rep) {
+                const float f = fw[sidx * G + hl];
+                const float4 v = __ldcg(po + (size_t)sidx * stride4);
+                o.x += f * v.x; o.y += f * v.y; o.z += f * v.z; o.w += f * v.w;
+            }
+        }
+        for (int off = 1; off < rep; off <<= 1) {
+            o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
+            o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
+            o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
+            o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
+        }
+        if (quad < nquad && sub == 0) {
+            const float inv = 1.0f / Ls[hl];
+            float* dst = p.attn + (size_t)b * p.Hq * HD;
+            const int k = (g * G + hl) * HD + d;
+            dst[perm_col(k)] = o.x * inv;
+            dst[perm_col(k + 1)] = o.y * inv;
+            dst[perm_col(k + 2)] = o.z * inv;
+            dst[perm_col(k + 3)] = o.w * inv;
+        }
+        consumer_sync();
+        if (c.tid == 0 && !c.sm->abort && a.skip_publish != task)
+            red_release_add(p.counters + cnt_stage(l, ST_ATTN) * kCounterStride, 1u);
+        if (l == 0) MK_TRACE_C(c, TR_A_MERGED, 0);
+    }
+    c_in.tn = c.tn;
+}
+
+template <int HD>
+__device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, const SeqSpan& sp_in, int u,
+                                             int n, int split, int nsplit) {
+    Ctx c = c_in;  // register copy (see gemv_task)
+    const SeqSpan sp = sp_in;
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
     constexpr int NKS = HD / 16;   // k16 steps over the head dim
@@ -685,42 +1201,58 @@ __device__ __noinline__ void attention_piece(Ctx& c, int l, int b, int g, const 
     const bool has_last = (sp.p0 + u + n - 1) == pos / kPage;
     const float2* rope = p.rope + (size_t)pos * (HD / 2);
 
+    // Stage q of the G heads (and the new token's k, v when this piece appends), plus
+    // the RoPE row, through shared memory with coalesced loads: one L2 round trip.
+    float* qs = c.scratch;                         // [G][HD]
+    float* ks = qs + 8 * HD;                       // [HD]
+    float* vs = ks + HD;                           // [HD]
+    float2* rs = reinterpret_cast<float2*>(vs + HD);  // [HD / 2]
+    if (!c.sm->abort) {
+        const float* qrow = p.qkv + (size_t)b * p.qkv_rows + (size_t)g * G * HD;
+        for (int i = c.tid; i < G * HD / 4; i += kConsumerThreads)
+            reinterpret_cast<float4*>(qs)[i] = __ldcg(reinterpret_cast<const float4*>(qrow) + i);
+        for (int i = c.tid; i < HD / 2; i += kConsumerThreads) rs[i] = __ldg(rope + i);
+        if (has_last) {
+            const float* kp = p.qkv + (size_t)b * p.qkv_rows + (size_t)(p.Hq + g) * HD;
+            const float* vp = p.qkv + (size_t)b * p.qkv_rows + (size_t)(p.Hq + p.Hkv + g) * HD;
+            for (int i = c.tid; i < HD / 4; i += kConsumerThreads) {
+                reinterpret_cast<float4*>(ks)[i] = __ldcg(reinterpret_cast<const float4*>(kp) + i);
+                reinterpret_cast<float4*>(vs)[i] = __ldcg(reinterpret_cast<const float4*>(vp) + i);
+            }
+        }
+    }
+    consumer_sync();
     // q (after RoPE) as A fragments: row gq = query head, k = head dims; hi/lo split
     uint32_t qa[NKS][2], ql[NKS][2];
-    {
-        const float* q = p.qkv + (size_t)b * p.qkv_rows + (size_t)hq * HD;
 #pragma unroll
-        for (int s = 0; s < NKS; ++s)
+    for (int s = 0; s < NKS; ++s)
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float v[2] = {0.f, 0.f};
-                if (gq < G && !c.sm->abort) {
+        for (int hh = 0; hh < 2; ++hh) {
+            float v[2] = {0.f, 0.f};
+            if (gq < G) {
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int d = 16 * s + 8 * hh + 2 * t + e;
-                        const int i = d % (HD / 2);
-                        const float2 cs = __ldg(rope + i);
-                        const float x0 = __ldcg(q + d);
-                        const float xp = __ldcg(q + (d < HD / 2 ? d + HD / 2 : d - HD / 2));
-                        v[e] = d < HD / 2 ? x0 * cs.x - xp * cs.y : x0 * cs.x + xp * cs.y;
-                    }
+                for (int e = 0; e < 2; ++e) {
+                    const int d = 16 * s + 8 * hh + 2 * t + e;
+                    const float2 cs = rs[d % (HD / 2)];
+                    const float x0 = qs[gq * HD + d];
+                    const float xp = qs[gq * HD + (d < HD / 2 ? d + HD / 2 : d - HD / 2)];
+                    v[e] = d < HD / 2 ? x0 * cs.x - xp * cs.y : x0 * cs.x + xp * cs.y;
                 }
-                split_bf16x2(v[0], v[1], qa[s][hh], ql[s][hh]);
             }
-    }
-    // the new token's K (after RoPE) and V, rounded to BF16, staged in shared memory
-    if (has_last && c.cw == 0 && !c.sm->abort) {
-        const float* kp = p.qkv + (size_t)b * p.qkv_rows + (size_t)(p.Hq + g) * HD;
-        const float* vp = p.qkv + (size_t)b * p.qkv_rows + (size_t)(p.Hq + p.Hkv + g) * HD;
+            split_bf16x2(v[0], v[1], qa[s][hh], ql[s][hh]);
+        }
+    // the new token's K (after RoPE) and V, rounded to BF16 (warp 0 also splices them)
+    if (has_last && c.cw == 0) {
         for (int i = c.lane; i < HD / 2; i += 32) {
-            const float2 cs = __ldg(rope + i);
-            const float k0 = __ldcg(kp + i), k1 = __ldcg(kp + i + HD / 2);
+            const float2 cs = rs[i];
+            const float k0 = ks[i], k1 = ks[i + HD / 2];
             c.sm->knew[i] = __float2bfloat16_rn(k0 * cs.x - k1 * cs.y);
             c.sm->knew[i + HD / 2] = __float2bfloat16_rn(k1 * cs.x + k0 * cs.y);
         }
-        for (int i = c.lane; i < HD; i += 32) c.sm->vnew[i] = __float2bfloat16_rn(__ldcg(vp + i));
+        for (int i = c.lane; i < HD; i += 32) c.sm->vnew[i] = __float2bfloat16_rn(vs[i]);
+        __syncwarp();
     }
-    if (has_last) consumer_sync();
+    if (l == 0) MK_TRACE_C(c, TR_A_Q, (uint32_t)bg_id(p, b, g));
 
     float m_run = -INFINITY, l_run = 0.f;
     float oacc[NCH][2];  // O[head gq][8 i + 2 t + {0, 1}]
@@ -729,7 +1261,9 @@ __device__ __noinline__ void attention_piece(Ctx& c, int l, int b, int g, const 
 
     for (int st = 0; st < n; st += PPS) {
         const int np = min(PPS, n - st);
+        if (l == 1) MK_TRACE_C(c, TR_S_WAIT, c.seq);
         const bool ok = wait_full(c, task);
+        if (l == 1) MK_TRACE_C(c, TR_S_FULL, c.seq);
         const uint32_t slot = c.ring_s + (c.seq % kStages) * kSlotBytes;
         if (has_last && st + np == n) {
             // splice the new row into the last page and append it to the pool
@@ -764,7 +1298,7 @@ __device__ __noinline__ void attention_piece(Ctx& c, int l, int b, int g, const 
                 const bool v0 = key0 >= lo && key0 <= pos;
                 const bool v1 = key0 + 1 >= lo && key0 + 1 <= pos;
                 // S = q K^T for 8 keys (n) x 16 head rows (m)
-                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacl[4] = {0.f, 0.f, 0.f, 0.f};
                 const int lrow = half * 8 + (c.lane & 7);
                 const int lmi = c.lane >> 3;
 #pragma unroll
@@ -774,12 +1308,12 @@ __device__ __noinline__ void attention_piece(Ctx& c, int l, int b, int g, const 
                     ldmatrix_x4(kbase + (ch >> 3) * 2048 + lrow * 128 + (((ch & 7) ^ (lrow & 7)) << 4),
                                 k0r, k1r, k2r, k3r);
                     mma_16816(sacc, qa[2 * s2][0], 0u, qa[2 * s2][1], 0u, k0r, k1r);
-                    mma_16816(sacc, ql[2 * s2][0], 0u, ql[2 * s2][1], 0u, k0r, k1r);
+                    mma_16816(sacl, ql[2 * s2][0], 0u, ql[2 * s2][1], 0u, k0r, k1r);
                     mma_16816(sacc, qa[2 * s2 + 1][0], 0u, qa[2 * s2 + 1][1], 0u, k2r, k3r);
-                    mma_16816(sacc, ql[2 * s2 + 1][0], 0u, ql[2 * s2 + 1][1], 0u, k2r, k3r);
+                    mma_16816(sacl, ql[2 * s2 + 1][0], 0u, ql[2 * s2 + 1][1], 0u, k2r, k3r);
                 }
-                const float s0 = v0 ? sacc[0] * p.scale : -INFINITY;
-                const float s1 = v1 ? sacc[1] * p.scale : -INFINITY;
+                const float s0 = v0 ? (sacc[0] + sacl[0]) * p.scale : -INFINITY;
+                const float s1 = v1 ? (sacc[1] + sacl[1]) * p.scale : -INFINITY;
                 float mb = fmaxf(s0, s1);
                 mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
                 mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
@@ -812,8 +1346,10 @@ __device__ __noinline__ void attention_piece(Ctx& c, int l, int b, int g, const 
             }
         }
         release_slot(c);
+        if (l == 1) MK_TRACE_C(c, TR_S_REL, c.seq - 1);
     }
 
+    if (l == 0) MK_TRACE_C(c, TR_A_LOOP, (uint32_t)n);
     // merge the 8 warps' partial softmax states (rows gq < G hold real heads)
     float* ws_o = c.scratch;                                  // [8][G][HD]
     float* ws_m = c.scratch + kConsumerWarps * 512;           // [8][8]
@@ -828,62 +1364,9 @@ __device__ __noinline__ void attention_piece(Ctx& c, int l, int b, int g, const 
             *reinterpret_cast<float2*>(ws_o + (c.cw * G + gq) * HD + 8 * i + 2 * t) =
                 make_float2(oacc[i][0], oacc[i][1]);
     }
-    consumer_sync();
-    const int bg = b * p.Hkv + g;
-    const size_t pbase = ((size_t)bg * p.C + split) * G;
-    if (!c.sm->abort) {
-        for (int e = c.tid; e < G * HD; e += kConsumerThreads) {
-            const int hl = e / HD, d = e % HD;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ws_m[w * 8 + hl]);
-            float o = 0.f, L = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = ws_m[w * 8 + hl];
-                const float f = mw == -INFINITY ? 0.f : expf(mw - M);
-                o += f * ws_o[(w * G + hl) * HD + d];
-                L += f * ws_l[w * 8 + hl];
-            }
-            p.part_o[(pbase + hl) * HD + d] = o;
-            if (d == 0) p.part_ml[pbase + hl] = make_float2(M, L);
-        }
-    }
-    // arrival: the last of the nsplit pieces merges them all
-    consumer_sync();
-    if (c.tid == 0) {
-        int last = 0;
-        if (!c.sm->abort) {
-            uint32_t* ctr = p.arrivals + ((size_t)l * p.maxB * p.Hkv + bg) * kCounterStride;
-            __threadfence();
-            const uint32_t old = atom_acq_rel_add(ctr, 1u);
-            if (old == (uint32_t)(nsplit - 1)) { last = 1; st_relaxed(ctr, 0u); }
-        }
-        c.sm->bcast = last;
-    }
-    consumer_sync();
-    if (c.sm->bcast) {
-        const size_t base0 = (size_t)bg * p.C * G;
-        for (int e = c.tid; e < G * HD; e += kConsumerThreads) {
-            const int hl = e / HD, d = e % HD;
-            float M = -INFINITY;
-            for (int sidx = 0; sidx < nsplit; ++sidx)
-                M = fmaxf(M, __ldcg(&p.part_ml[base0 + (size_t)sidx * G + hl].x));
-            float o = 0.f, L = 0.f;
-            for (int sidx = 0; sidx < nsplit; ++sidx) {
-                const float2 ml = __ldcg(&p.part_ml[base0 + (size_t)sidx * G + hl]);
-                const float f = expf(ml.x - M);
-                o += f * __ldcg(&p.part_o[(base0 + (size_t)sidx * G + hl) * HD + d]);
-                L += f * ml.y;
-            }
-            p.attn[(size_t)b * p.Hq * HD + perm_col((g * G + hl) * HD + d)] = o / L;
-        }
-        consumer_sync();
-        if (c.tid == 0 && !c.sm->abort && a.skip_publish != task) {
-            __threadfence();
-            red_release_add(p.counters + cnt_stage(l, ST_ATTN) * kCounterStride, 1u);
-        }
-    }
+    c_in.seq = c.seq;
+    c_in.tn = c.tn;
+    attention_finish<HD>(c_in, l, b, g, split, nsplit);
 }
 
 template <int HD>
@@ -892,23 +1375,32 @@ __device__ void attention_stage(Ctx& c, int l, int cta) {
     for_each_piece(*c.a, c.sm, l, cta, [&](int b, int g, const SeqSpan& sp, int u, int n,
                                           int split, int nsplit) {
         if (!waited) {
+            MK_TRACE_C(c, TR_WAIT, l * 16 + ST_ATTN);
             consumer_wait(c, cnt_stage(l, ST_QKV), c.a->stage_target, l * 16 + ST_ATTN);
+            MK_TRACE_C(c, TR_READY, l * 16 + ST_ATTN);
             waited = true;
         }
+        MK_TRACE_C(c, TR_PIECE, (uint32_t)(b * 256 + g));
         attention_piece<HD>(c, l, b, g, sp, u, n, split, nsplit);
+        MK_TRACE_C(c, TR_MERGE, (uint32_t)(b * 256 + g));
     });
 }
 
+// x[b] = E[token b]. Each CTA writes the residual rows it owns (the same rows its O and
+// down tiles update) and keeps them in shared memory for those residual adds.
 __device__ void embed_stage(Ctx& c, int cta) {
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
-    const long long total = (long long)a.B * p.d;
-    const long long e0 = (long long)cta * total / p.C, e1 = (long long)(cta + 1) * total / p.C;
+    int a0, a1;
+    cta_rows(p.d, cta, p.C, a0, a1);
+    const int nr = a1 - a0;
     if (!c.sm->abort)
-        for (long long e = e0 + c.tid; e < e1; e += kConsumerThreads) {
-            const int b = (int)(e / p.d), k = (int)(e % p.d);
+        for (int e = c.tid; e < a.B * nr; e += kConsumerThreads) {
+            const int b = e / nr, k = a0 + e % nr;
             const int tok = __ldg(a.tokens + b);
-            p.x[(size_t)b * p.d + perm_col(k)] = __bfloat162float(p.embed[(size_t)tok * p.d + k]);
+            const float v = __bfloat162float(p.embed[(size_t)tok * p.d + k]);
+            p.x[(size_t)b * p.d + perm_col(k)] = v;
+            c.sm->xown[b][k - a0] = v;
         }
     publish(c, cnt_embed(), -2);
 }
@@ -925,7 +1417,6 @@ __device__ void argmax_finish(Ctx& c, int cta) {
         int last = 0;
         if (!c.sm->abort && a.skip_publish != p.L * 16) {
             uint32_t* ctr = p.arrivals + ((size_t)p.L * p.maxB * p.Hkv) * kCounterStride;
-            __threadfence();
             const uint32_t old = atom_acq_rel_add(ctr, 1u);
             if (old == (uint32_t)(p.C - 1)) { last = 1; st_relaxed(ctr, 0u); }
         }
@@ -965,6 +1456,7 @@ __device__ void consumer_run(Ctx& c, int cta) {
     }
     gemv_stage(c, make_gemv(*c.a, G_LM, 0), cta);
     argmax_finish(c, cta);
+    MK_TRACE_C(c, TR_END, 0);
 }
 
 template <int HD>
@@ -1005,13 +1497,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     __syncthreads();
 
     if (warp == 0) {
-        if (lane == 0) {
-            Producer pr;
-            pr.a = &a;
-            pr.sm = sm;
-            pr.ring_s = smem_u32(ring);
-            pr.run<HD>(cta);
-        }
+        Producer pr;
+        pr.a = &a;
+        pr.sm = sm;
+        pr.ring_s = smem_u32(ring);
+        pr.lane = lane;
+        pr.run<HD>(cta);
         return;
     }
     Ctx c;
@@ -1024,6 +1515,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     c.cw = warp - 1;
     c.lane = lane;
     c.tid = threadIdx.x - 32;
+    c.tn = 0;
     consumer_run<HD>(c, cta);
 }
 
