@@ -65,7 +65,8 @@ enum TraceCode { TR_WAIT = 1, TR_READY = 2, TR_DONE = 3, TR_PIECE = 4, TR_MERGE 
                  TR_P_STAGE = 11, TR_P_BLOCK = 12, TR_P_GO = 13,
                  TR_S_WAIT = 20, TR_S_FULL = 21, TR_S_REL = 22, TR_S_ISSUE = 23,
                  TR_A_Q = 30, TR_A_LOOP = 31, TR_A_PART = 32, TR_A_ARRIVED = 33, TR_A_MERGED = 34,
-                 TR_G_NORM = 40, TR_G_X = 41, TR_G_SUM = 42, TR_G_EPI = 43 };
+                 TR_G_NORM = 40, TR_G_X = 41, TR_G_SUM = 42, TR_G_EPI = 43,
+                 TR_Q_LOADED = 50, TR_Q_SYNCED = 51, TR_Q_FRAG = 52, TR_M_ML = 53, TR_M_W = 54, TR_M_O = 55 };
 
 // error codes (same values as mk_status)
 constexpr int kErrInvalid = 1, kErrBadPage = 5, kErrTimeout = 6, kErrInternal = 7;
@@ -1074,8 +1075,9 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
     const Plan& p = a.p;
     const int G = p.G;
     const int task = l * 16 + ST_ATTN;
-    float* ws_o = c.scratch;                                  // [8][G][HD]
-    float* ws_m = c.scratch + kConsumerWarps * 512;           // [8][8]
+    constexpr int OS = HD + 8;
+    float* ws_o = c.scratch;                                  // [8][G][OS]
+    float* ws_m = c.scratch + kConsumerWarps * G * OS;        // [8][8]
     float* ws_l = ws_m + 64;                                  // [8][8]
     consumer_sync();
     const int bg = b * p.Hkv + g;
@@ -1091,7 +1093,7 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
             for (int w = 0; w < kConsumerWarps; ++w) {
                 const float mw = ws_m[w * 8 + hl];
                 const float f = mw == -INFINITY ? 0.f : expf(mw - M);
-                o += f * ws_o[(w * G + hl) * HD + d];
+                o += f * ws_o[(w * G + hl) * OS + d];
                 L += f * ws_l[w * 8 + hl];
             }
             p.part_o[(pbase + hl) * HD + d] = o;
@@ -1100,7 +1102,7 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
     }
     // arrival: the last of the nsplit pieces merges them all
     consumer_sync();
-    if (l == 0) MK_TRACE_C(c, TR_A_PART, (uint32_t)nsplit);
+    if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_PART, (uint32_t)nsplit);
     if (c.tid == 0) {
         int last = 0;
         if (!c.sm->abort) {
@@ -1111,7 +1113,7 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
         c.sm->bcast = last;
     }
     consumer_sync();
-    if (l == 0) MK_TRACE_C(c, TR_A_ARRIVED, (uint32_t)c.sm->bcast);
+    if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_ARRIVED, (uint32_t)c.sm->bcast);
     if (c.sm->bcast) {
         // 1) all (m, l) of the nsplit partials into shared memory in one parallel pass
         const size_t base0 = (size_t)bg * p.C * G;
@@ -1120,6 +1122,7 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
         float* Ls = fw + kMaxSplitsG;                           // [G]
         for (int i = c.tid; i < nsplit * G; i += kConsumerThreads) mls[i] = __ldcg(&p.part_ml[base0 + i]);
         consumer_sync();
+        if (l == 1) MK_TRACE_C(c, TR_M_ML, 0);
         // 2) per head (one warp each): M = max m_s, w_s = exp(m_s - M), L = sum w_s l_s
         if (c.cw < G) {
             const int hl = c.cw;
@@ -1139,6 +1142,7 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
             if (c.lane == 0) Ls[hl] = L;
         }
         consumer_sync();
+        if (l == 1) MK_TRACE_C(c, TR_M_W, 0);
         // 3) O = sum_s w_s o_s / L: threads own 4 consecutive dims of one head; the splits
         //    are dealt to kRep threads per quad and combined with shuffles
         constexpr int kQuads = 8 * HD / 4;  // upper bound of G * HD / 4
@@ -1153,11 +1157,20 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
             d = (quad * 4) % HD;
             const float4* po = reinterpret_cast<const float4*>(p.part_o + (base0 + hl) * HD + d);
             const size_t stride4 = (size_t)G * HD / 4;
-#pragma unroll 4
-            for (int sidx = sub; sidx < nsplit; sidx += rep) {
-                const float f = fw[sidx * G + hl];
-                const float4 v = __ldcg(po + (size_t)sidx * stride4);
-                o.x += f * v.x; o.y += f * v.y; o.z += f * v.z; o.w += f * v.w;
+            // 8 independent loads in flight per round
+            for (int s0 = sub; s0 < nsplit; s0 += 8 * rep) {
+                float4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int si = s0 + j * rep;
+                    v[j] = si < nsplit ? __ldcg(po + (size_t)si * stride4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int si = s0 + j * rep;
+                    const float f = si < nsplit ? fw[si * G + hl] : 0.f;
+                    o.x += f * v[j].x; o.y += f * v[j].y; o.z += f * v[j].z; o.w += f * v[j].w;
+                }
             }
         }
         for (int off = 1; off < rep; off <<= 1) {
@@ -1178,7 +1191,7 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
         consumer_sync();
         if (c.tid == 0 && !c.sm->abort && a.skip_publish != task)
             red_release_add(p.counters + cnt_stage(l, ST_ATTN) * kCounterStride, 1u);
-        if (l == 0) MK_TRACE_C(c, TR_A_MERGED, 0);
+        if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_MERGED, 0);
     }
     c_in.tn = c.tn;
 }
@@ -1202,15 +1215,19 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
     const float2* rope = p.rope + (size_t)pos * (HD / 2);
 
     // Stage q of the G heads (and the new token's k, v when this piece appends), plus
-    // the RoPE row, through shared memory with coalesced loads: one L2 round trip.
-    float* qs = c.scratch;                         // [G][HD]
-    float* ks = qs + 8 * HD;                       // [HD]
+    // the RoPE row, through shared memory with coalesced loads: one L2 round trip. Rows
+    // of q are padded to HD + 8 floats so the fragment reads below are conflict-free.
+    constexpr int QS = HD + 8;
+    float* qs = c.scratch;                         // [G][QS]
+    float* ks = qs + 8 * QS;                       // [HD]
     float* vs = ks + HD;                           // [HD]
     float2* rs = reinterpret_cast<float2*>(vs + HD);  // [HD / 2]
     if (!c.sm->abort) {
         const float* qrow = p.qkv + (size_t)b * p.qkv_rows + (size_t)g * G * HD;
-        for (int i = c.tid; i < G * HD / 4; i += kConsumerThreads)
-            reinterpret_cast<float4*>(qs)[i] = __ldcg(reinterpret_cast<const float4*>(qrow) + i);
+        for (int i = c.tid; i < G * HD / 4; i += kConsumerThreads) {
+            const int h = (4 * i) / HD, d = (4 * i) % HD;
+            *reinterpret_cast<float4*>(qs + h * QS + d) = __ldcg(reinterpret_cast<const float4*>(qrow) + i);
+        }
         for (int i = c.tid; i < HD / 2; i += kConsumerThreads) rs[i] = __ldg(rope + i);
         if (has_last) {
             const float* kp = p.qkv + (size_t)b * p.qkv_rows + (size_t)(p.Hq + g) * HD;
@@ -1221,25 +1238,32 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
             }
         }
     }
+    if (l == 1) MK_TRACE_C(c, TR_Q_LOADED, 0);
     consumer_sync();
-    // q (after RoPE) as A fragments: row gq = query head, k = head dims; hi/lo split
+    if (l == 1) MK_TRACE_C(c, TR_Q_SYNCED, 0);
+    // q^T (after RoPE) as the B operand: column gq = query head, k = head dims; hi/lo split.
+    // b0b1 of k-step s holds dims 16s + 2t, +1; b2b3 holds 16s + 8 + 2t, +1.
     uint32_t qa[NKS][2], ql[NKS][2];
 #pragma unroll
     for (int s = 0; s < NKS; ++s)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            float v[2] = {0.f, 0.f};
+            float v0 = 0.f, v1 = 0.f;
             if (gq < G) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int d = 16 * s + 8 * hh + 2 * t + e;
-                    const float2 cs = rs[d % (HD / 2)];
-                    const float x0 = qs[gq * HD + d];
-                    const float xp = qs[gq * HD + (d < HD / 2 ? d + HD / 2 : d - HD / 2)];
-                    v[e] = d < HD / 2 ? x0 * cs.x - xp * cs.y : x0 * cs.x + xp * cs.y;
+                const int d = 16 * s + 8 * hh + 2 * t;
+                const int dp = d < HD / 2 ? d + HD / 2 : d - HD / 2;
+                const float4 cs = *reinterpret_cast<const float4*>(rs + (d % (HD / 2)));
+                const float2 x0 = *reinterpret_cast<const float2*>(qs + gq * QS + d);
+                const float2 xp = *reinterpret_cast<const float2*>(qs + gq * QS + dp);
+                if (d < HD / 2) {
+                    v0 = x0.x * cs.x - xp.x * cs.y;
+                    v1 = x0.y * cs.z - xp.y * cs.w;
+                } else {
+                    v0 = x0.x * cs.x + xp.x * cs.y;
+                    v1 = x0.y * cs.z + xp.y * cs.w;
                 }
             }
-            split_bf16x2(v[0], v[1], qa[s][hh], ql[s][hh]);
+            split_bf16x2(v0, v1, qa[s][hh], ql[s][hh]);
         }
     // the new token's K (after RoPE) and V, rounded to BF16 (warp 0 also splices them)
     if (has_last && c.cw == 0) {
@@ -1252,14 +1276,27 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
         for (int i = c.lane; i < HD; i += 32) c.sm->vnew[i] = __float2bfloat16_rn(vs[i]);
         __syncwarp();
     }
-    if (l == 0) MK_TRACE_C(c, TR_A_Q, (uint32_t)bg_id(p, b, g));
+    if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_Q, (uint32_t)bg_id(p, b, g));
+    consumer_sync();  // the staging area becomes the per-warp P buffers below
 
-    float m_run = -INFINITY, l_run = 0.f;
-    float oacc[NCH][2];  // O[head gq][8 i + 2 t + {0, 1}]
+    // Keys in the MMA M dimension: S^T = K q^T (16 keys x 8 head columns) and
+    // O^T += V^T P^T (16 dims x 8 head columns), two MMAs (hi/lo) per 16x16 step.
+    // This thread owns heads 2t, 2t+1 (real when < G) and, in O^T, dims 16 mt + g (+8).
+    constexpr int NMT = HD / 16;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float oacc[NMT][4];
 #pragma unroll
-    for (int i = 0; i < NCH; ++i) oacc[i][0] = oacc[i][1] = 0.f;
+    for (int i = 0; i < NMT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+    float* pbuf = c.scratch + c.cw * 16 * 9;  // P[16 keys][9] for this warp (fp32)
+    // warp groups: a 32 KB slot holds PPS pages; WPS warps take one page each, and the
+    // 8 / WPS groups take consecutive slots in turn
+    constexpr int WPS = PPS < kConsumerWarps ? PPS : kConsumerWarps;
+    constexpr int NGRP = kConsumerWarps / WPS;
+    const int grp = c.cw / WPS, wpage = c.cw % WPS;
+    const int lrow8 = c.lane & 7, lmi = c.lane >> 3;
 
-    for (int st = 0; st < n; st += PPS) {
+    int sidx = 0;
+    for (int st = 0; st < n; st += PPS, ++sidx) {
         const int np = min(PPS, n - st);
         if (l == 1) MK_TRACE_C(c, TR_S_WAIT, c.seq);
         const bool ok = wait_full(c, task);
@@ -1289,59 +1326,82 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
             }
             consumer_sync();
         }
-        if (ok && !c.sm->abort) {
-            for (int kb = c.cw; kb < 2 * np; kb += kConsumerWarps) {
-                const int pi = kb >> 1, half = kb & 1;
+        if (ok && !c.sm->abort && (sidx % NGRP) == grp) {
+            for (int pi = wpage; pi < np; pi += WPS) {
                 const uint32_t kbase = slot + pi * 64 * HD;
                 const uint32_t vbase = kbase + 32 * HD;
-                const int key0 = (sp.p0 + u + st + pi) * kPage + half * 8 + 2 * t;
-                const bool v0 = key0 >= lo && key0 <= pos;
-                const bool v1 = key0 + 1 >= lo && key0 + 1 <= pos;
-                // S = q K^T for 8 keys (n) x 16 head rows (m)
-                float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacl[4] = {0.f, 0.f, 0.f, 0.f};
-                const int lrow = half * 8 + (c.lane & 7);
-                const int lmi = c.lane >> 3;
+                const int kbase_key = (sp.p0 + u + st + pi) * kPage;
+                const bool vA = kbase_key + gq >= lo && kbase_key + gq <= pos;        // key g
+                const bool vB = kbase_key + gq + 8 >= lo && kbase_key + gq + 8 <= pos;  // key g + 8
+                // S^T = K q^T: A = K rows (keys) via ldmatrix, B = q^T
+                float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    const int krow = lrow8 + (lmi & 1) * 8;
 #pragma unroll
-                for (int s2 = 0; s2 < NKS / 2; ++s2) {
-                    const int ch = 4 * s2 + lmi;
-                    uint32_t k0r, k1r, k2r, k3r;
-                    ldmatrix_x4(kbase + (ch >> 3) * 2048 + lrow * 128 + (((ch & 7) ^ (lrow & 7)) << 4),
-                                k0r, k1r, k2r, k3r);
-                    mma_16816(sacc, qa[2 * s2][0], 0u, qa[2 * s2][1], 0u, k0r, k1r);
-                    mma_16816(sacl, ql[2 * s2][0], 0u, ql[2 * s2][1], 0u, k0r, k1r);
-                    mma_16816(sacc, qa[2 * s2 + 1][0], 0u, qa[2 * s2 + 1][1], 0u, k2r, k3r);
-                    mma_16816(sacl, ql[2 * s2 + 1][0], 0u, ql[2 * s2 + 1][1], 0u, k2r, k3r);
-                }
-                const float s0 = v0 ? (sacc[0] + sacl[0]) * p.scale : -INFINITY;
-                const float s1 = v1 ? (sacc[1] + sacl[1]) * p.scale : -INFINITY;
-                float mb = fmaxf(s0, s1);
-                mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-                mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-                const float m_new = fmaxf(m_run, mb);
-                float corr = 1.f, p0 = 0.f, p1 = 0.f;
-                if (m_new != -INFINITY) {
-                    corr = expf(m_run - m_new);
-                    p0 = expf(s0 - m_new);
-                    p1 = expf(s1 - m_new);
-                }
-                m_run = m_new;
-                l_run = l_run * corr + p0 + p1;
-#pragma unroll
-                for (int i = 0; i < NCH; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; }
-                uint32_t pa, pl;
-                split_bf16x2(p0, p1, pa, pl);
-                const uint32_t mask = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
-#pragma unroll
-                for (int q4 = 0; q4 < NCH / 4; ++q4) {
-                    const int ch = 4 * q4 + lmi;
-                    uint32_t r[4];
-                    ldmatrix_x4_trans(vbase + (ch >> 3) * 2048 + lrow * 128 + (((ch & 7) ^ (lrow & 7)) << 4),
-                                      r[0], r[1], r[2], r[3]);
-#pragma unroll
-                    for (int mi = 0; mi < 4; ++mi) {
-                        mma_1688_top(oacc[4 * q4 + mi][0], oacc[4 * q4 + mi][1], pa, r[mi] & mask);
-                        mma_1688_top(oacc[4 * q4 + mi][0], oacc[4 * q4 + mi][1], pl, r[mi] & mask);
+                    for (int s = 0; s < NKS; ++s) {
+                        const int ch = 2 * s + (lmi >> 1);
+                        uint32_t a0, a1, a2, a3;
+                        ldmatrix_x4(kbase + (ch >> 3) * 2048 + krow * 128 + (((ch & 7) ^ (krow & 7)) << 4),
+                                    a0, a1, a2, a3);
+                        mma_16816(sh, a0, a1, a2, a3, qa[s][0], qa[s][1]);
+                        mma_16816(sl, a0, a1, a2, a3, ql[s][0], ql[s][1]);
                     }
+                }
+                // scores: [key g][head 2t], [g][2t+1], [g+8][2t], [g+8][2t+1]
+                float sc[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool v = e < 2 ? vA : vB;
+                    sc[e] = v ? (sh[e] + sl[e]) * p.scale : -INFINITY;
+                }
+                float pv[4];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float mb = fmaxf(sc[hh], sc[2 + hh]);
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+                    const float m_new = fmaxf(m_run[hh], mb);
+                    float corr = 1.f, p0 = 0.f, p1 = 0.f;
+                    if (m_new != -INFINITY) {
+                        corr = expf(m_run[hh] - m_new);
+                        p0 = expf(sc[hh] - m_new);
+                        p1 = expf(sc[2 + hh] - m_new);
+                    }
+                    m_run[hh] = m_new;
+                    l_run[hh] = l_run[hh] * corr + p0 + p1;
+                    pv[hh] = p0;
+                    pv[2 + hh] = p1;
+#pragma unroll
+                    for (int mt = 0; mt < NMT; ++mt) { oacc[mt][hh] *= corr; oacc[mt][2 + hh] *= corr; }
+                }
+                // P^T as the B operand (keys x heads): transpose through this warp's buffer
+                pbuf[gq * 9 + 2 * t] = pv[0];
+                pbuf[gq * 9 + 2 * t + 1] = pv[1];
+                pbuf[(gq + 8) * 9 + 2 * t] = pv[2];
+                pbuf[(gq + 8) * 9 + 2 * t + 1] = pv[3];
+                __syncwarp();
+                uint32_t pbh0, pbl0, pbh1, pbl1;
+                split_bf16x2(pbuf[(2 * t) * 9 + gq], pbuf[(2 * t + 1) * 9 + gq], pbh0, pbl0);
+                split_bf16x2(pbuf[(2 * t + 8) * 9 + gq], pbuf[(2 * t + 9) * 9 + gq], pbh1, pbl1);
+                __syncwarp();
+                // keys 2t, 2t+1 / 2t+8, 2t+9 of V^T: zero the invalid ones (garbage-safe)
+                const int k2 = kbase_key + 2 * t;
+                const uint32_t mlo = ((k2 >= lo && k2 <= pos) ? 0x0000ffffu : 0u) |
+                                     ((k2 + 1 >= lo && k2 + 1 <= pos) ? 0xffff0000u : 0u);
+                const uint32_t mhi = ((k2 + 8 >= lo && k2 + 8 <= pos) ? 0x0000ffffu : 0u) |
+                                     ((k2 + 9 >= lo && k2 + 9 <= pos) ? 0xffff0000u : 0u);
+                // O^T += V^T P^T: A = V^T (dims x keys) via ldmatrix.trans of the V rows
+                const int vrow = lrow8 + (lmi >> 1) * 8;
+#pragma unroll
+                for (int mt = 0; mt < NMT; ++mt) {
+                    const int ch = 2 * mt + (lmi & 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4_trans(vbase + (ch >> 3) * 2048 + vrow * 128 + (((ch & 7) ^ (vrow & 7)) << 4),
+                                      a0, a1, a2, a3);
+                    a0 &= mlo; a1 &= mlo; a2 &= mhi; a3 &= mhi;
+                    mma_16816(oacc[mt], a0, a1, a2, a3, pbh0, pbh1);
+                    mma_16816(oacc[mt], a0, a1, a2, a3, pbl0, pbl1);
                 }
             }
         }
@@ -1350,19 +1410,29 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
     }
 
     if (l == 0) MK_TRACE_C(c, TR_A_LOOP, (uint32_t)n);
-    // merge the 8 warps' partial softmax states (rows gq < G hold real heads)
-    float* ws_o = c.scratch;                                  // [8][G][HD]
-    float* ws_m = c.scratch + kConsumerWarps * 512;           // [8][8]
+    // this warp's softmax state for heads 2t, 2t+1 -> shared memory (rows padded to HD + 8)
+    constexpr int OS = HD + 8;
+    float* ws_o = c.scratch;                                  // [8][G][OS]
+    float* ws_m = c.scratch + kConsumerWarps * G * OS;        // [8][8]
     float* ws_l = ws_m + 64;                                  // [8][8]
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-    consumer_sync();
-    if (gq < G) {
-        if (t == 0) { ws_m[c.cw * 8 + gq] = m_run; ws_l[c.cw * 8 + gq] = l_run; }
 #pragma unroll
-        for (int i = 0; i < NCH; ++i)
-            *reinterpret_cast<float2*>(ws_o + (c.cw * G + gq) * HD + 8 * i + 2 * t) =
-                make_float2(oacc[i][0], oacc[i][1]);
+    for (int hh = 0; hh < 2; ++hh) {
+        l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 4);
+        l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 8);
+        l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 16);
+    }
+    consumer_sync();
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int h = 2 * t + hh;
+        if (h < G) {
+            if (gq == 0) { ws_m[c.cw * 8 + h] = m_run[hh]; ws_l[c.cw * 8 + h] = l_run[hh]; }
+#pragma unroll
+            for (int mt = 0; mt < NMT; ++mt) {
+                ws_o[(c.cw * G + h) * OS + 16 * mt + gq] = oacc[mt][hh];
+                ws_o[(c.cw * G + h) * OS + 16 * mt + gq + 8] = oacc[mt][2 + hh];
+            }
+        }
     }
     c_in.seq = c.seq;
     c_in.tn = c.tn;
