@@ -164,14 +164,22 @@ MK_API mk_status mk_decode_step(mk_handle *h, const int32_t *tokens, const int32
  * that latched it (layer*16 + stage, or -1). */
 MK_API mk_status mk_status_sync(mk_handle *h, void *stream, int32_t *failing_task);
 
-/* Clears a latched device error and re-zeroes the dependency counters (synchronous). */
+/* Clears a latched device error and re-zeroes the argmax arrival counter (synchronous). */
 MK_API mk_status mk_status_reset(mk_handle *h);
 
 /* Options (host-side; take effect from the next step):
  *   MK_OPT_TIMEOUT_NS   limit for every device-side wait, in ns (default 1e9)
  *   MK_OPT_SKIP_PUBLISH test hook: the task with this id never publishes its
- *                       completion, so its waiters time out (-1 = off) */
-typedef enum mk_option { MK_OPT_TIMEOUT_NS = 1, MK_OPT_SKIP_PUBLISH = 2 } mk_option;
+ *                       completion, so its waiters time out (-1 = off)
+ *   MK_OPT_PREFETCH_SLOTS how many ring slots (32 KB each) a second producer warp
+ *                       runs ahead of the loading warp, prefetching weights and KV
+ *                       pages into L2 so that HBM streams across dependency waits;
+ *                       0..64, 0 = off (the default). Results do not depend on it. */
+typedef enum mk_option {
+    MK_OPT_TIMEOUT_NS = 1,
+    MK_OPT_SKIP_PUBLISH = 2,
+    MK_OPT_PREFETCH_SLOTS = 3
+} mk_option;
 MK_API mk_status mk_set_option(mk_handle *h, mk_option opt, int64_t value);
 
 /* Read-only facts about a handle (for schedulers and benchmarks). */
@@ -224,7 +232,11 @@ MK_API mk_status mk_decode_step_noalloc(const mk_model_desc *desc, const mk_weig
 
 /* Introspection for stage-by-stage verification. After a step has completed (sync
  * the stream first), these device buffers hold the activations of the LAST layer the
- * step ran; they are overwritten by the next step. Layouts (fp32, row b at b*width):
+ * step ran; they are overwritten by the next step. The element size is
+ * *bytes / (max_batch * width): 8 bytes when the element is a tagged word (low 32 bits
+ * the fp32 value, high 32 bits the tag of the write that produced it; QKV always, the
+ * others after a step with batch <= 4), else 4 bytes of plain fp32.
+ * Layouts (row b at b*width elements):
  *   MK_BUF_X     residual stream after the last layer (input of the final norm),
  *                [max_batch][d_model], permuted columns (below)
  *   MK_BUF_QKV   q|k|v projections of the last layer, BEFORE RoPE, natural order,

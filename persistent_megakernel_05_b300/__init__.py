@@ -28,6 +28,7 @@ MK_ERR_INTERNAL = 7
 MK_ERR_NO_DEVICE = 8
 MK_OPT_TIMEOUT_NS = 1
 MK_OPT_SKIP_PUBLISH = 2
+MK_OPT_PREFETCH_SLOTS = 3
 
 # exported symbols of include/mk.h
 ABI_SYMBOLS = ("mk_create", "mk_kv_alloc", "mk_kv_free", "mk_decode_step", "mk_status_sync",
@@ -285,9 +286,12 @@ class DecodeModel:
         import numpy as np
         import torch
         ptr, nbytes = mk_debug_buffer(self.handle, which)
-        n = nbytes // 4
-        t = torch.as_tensor(_CudaArray(ptr, (n,), "<f4"), device=f"cuda:{self.device}")
-        a = t.cpu().numpy().reshape(self.cfg.max_batch, -1).copy()
+        cfg = self.cfg
+        width = {MK_BUF_X: cfg.d_model, MK_BUF_QKV: (cfg.n_q_heads + 2 * cfg.n_kv_heads) * cfg.head_dim,
+                 MK_BUF_ATTN: cfg.n_q_heads * cfg.head_dim, MK_BUF_H: cfg.ffn_dim}[which]
+        step = nbytes // (cfg.max_batch * width * 4)  # 2: tagged words (value in the low half)
+        t = torch.as_tensor(_CudaArray(ptr, (nbytes // 4,), "<f4"), device=f"cuda:{self.device}")
+        a = t.cpu().numpy()[0::step].reshape(cfg.max_batch, -1).copy()
         if which != MK_BUF_QKV:
             idx = np.array([perm_col(k) for k in range(a.shape[1])])
             a = a[:, idx]

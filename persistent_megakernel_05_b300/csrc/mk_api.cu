@@ -30,10 +30,12 @@ struct mk_handle {
     void* d_kvmap = nullptr;        // CUtensorMap (128 B, 64-B aligned)
     void* kv = nullptr;
     mk_kv_pool pool{};
-    uint32_t epoch = 0;
-    uint32_t attn_total = 0;
+    uint32_t epoch = 0;             // tag epoch of the last step (1 .. 2^20 - 1, cycling)
+    uint32_t cnt_epoch = 0;         // steps since the counters were last zeroed
+    int last_batch = 0;             // batch of the last step (selects the activation format)
     long long timeout_ns = 1000000000LL;
     int skip_publish = -1;
+    int prefetch_slots = mk::kDefaultPrefetchSlots;
     int num_ctas = 0;
     int hd = 0;
     int64_t weight_bytes = 0;
@@ -197,15 +199,18 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     // ---- scratch arena
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-    const size_t o_x = take(sizeof(float) * maxB * d);
-    const size_t o_qkv = take(sizeof(float) * maxB * qkv_rows);
-    const size_t o_attn = take(sizeof(float) * maxB * Hq * hd);
-    const size_t o_h = take(sizeof(float) * maxB * F);
-    const size_t o_po = take(sizeof(float) * (size_t)maxB * Hkv * C * G * hd);
-    const size_t o_pml = take(sizeof(float2) * (size_t)maxB * Hkv * C * G);
+    // activations and attention partials are tagged 64-bit words
+    const size_t o_x = take(8 * (size_t)maxB * d);
+    const size_t o_qkv = take(8 * (size_t)maxB * qkv_rows);
+    const size_t o_attn = take(8 * (size_t)maxB * Hq * hd);
+    const size_t o_h = take(8 * (size_t)maxB * F);
+    const size_t o_part = take(8 * (size_t)maxB * Hkv * C * (G * hd + 2 * G));
+    const size_t o_xf = take(sizeof(float) * (size_t)maxB * d);
+    const size_t o_attnf = take(sizeof(float) * (size_t)maxB * Hq * hd);
+    const size_t o_hf = take(sizeof(float) * (size_t)maxB * F);
     const size_t o_am = take(sizeof(float2) * (size_t)C * maxB);
-    h->counters_words = (size_t)(2 + L * mk::kStagesPerLayer) * mk::kCounterStride;
-    h->arrivals_words = (size_t)(L * maxB * Hkv + 1) * mk::kCounterStride;
+    h->counters_words = (size_t)(1 + L * mk::kStagesPerLayer) * mk::kCounterStride;
+    h->arrivals_words = (size_t)mk::kCounterStride;
     const size_t o_cnt = take(sizeof(uint32_t) * h->counters_words);
     const size_t o_arr = take(sizeof(uint32_t) * h->arrivals_words);
     const size_t o_status = take(sizeof(int) * 4);
@@ -283,14 +288,16 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     p.lm_head = (const bf16*)weights->lm_head;
     p.final_gain = h->d_gains + (size_t)(2 * L) * d;
     p.rope = h->d_rope;
-    p.x = (float*)(base + o_x);
-    p.qkv = (float*)(base + o_qkv);
-    p.attn = (float*)(base + o_attn);
-    p.h = (float*)(base + o_h);
-    p.part_o = (float*)(base + o_po);
-    p.part_ml = (float2*)(base + o_pml);
-    p.amax_part = (float2*)(base + o_am);
+    p.x = (uint64_t*)(base + o_x);
+    p.qkv = (uint64_t*)(base + o_qkv);
+    p.attn = (uint64_t*)(base + o_attn);
+    p.h = (uint64_t*)(base + o_h);
+    p.part = (uint64_t*)(base + o_part);
+    p.xf = (float*)(base + o_xf);
+    p.attnf = (float*)(base + o_attnf);
+    p.hf = (float*)(base + o_hf);
     p.counters = (uint32_t*)(base + o_cnt);
+    p.amax_part = (float2*)(base + o_am);
     p.arrivals = (uint32_t*)(base + o_arr);
     p.status = (int*)(base + o_status);
     p.kv = nullptr;
@@ -398,12 +405,14 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
     a.logits = logits;
     a.max_pages = max_pages_per_seq;
     a.B = batch;
-    const uint32_t epoch = h->epoch + 1;
-    const uint32_t attn_total = h->attn_total + (uint32_t)batch * (uint32_t)h->desc.n_kv_heads;
-    a.stage_target = epoch * (uint32_t)h->num_ctas;
-    a.embed_target = a.stage_target;
-    a.attn_target = attn_total;
+    // 20-bit epochs, never 0 (zeroed memory never carries a valid tag)
+    const uint32_t epoch = h->epoch % 0xFFFFFu + 1u;
+    a.epoch = epoch;
+    // the stage counters only advance in steps whose batch exceeds the tagged-word limit
+    const uint32_t cnt_epoch = h->cnt_epoch + (batch > mk::kMaxTaggedBatch ? 1u : 0u);
+    a.stage_target = cnt_epoch * (uint32_t)h->num_ctas;
     a.skip_publish = h->skip_publish;
+    a.prefetch_slots = h->prefetch_slots;
     a.timeout_ns = h->timeout_ns;
     void* args[] = {&a};
     const void* fn = h->hd == 128 ? (const void*)mk::decode_step_kernel<128>
@@ -415,7 +424,8 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
         return MK_ERR_LAUNCH;
     }
     h->epoch = epoch;
-    h->attn_total = attn_total;
+    h->cnt_epoch = cnt_epoch;
+    h->last_batch = batch;
     return MK_OK;
 }
 
@@ -448,8 +458,8 @@ mk_status mk_status_reset(mk_handle* h) {
         cudaGetLastError();
         return MK_ERR_INTERNAL;
     }
-    h->epoch = 0;
-    h->attn_total = 0;
+    h->cnt_epoch = 0;
+    // the tag epoch keeps advancing: words written before the reset never match a later tag
     return MK_OK;
 }
 
@@ -462,6 +472,10 @@ mk_status mk_set_option(mk_handle* h, mk_option opt, int64_t value) {
             return MK_OK;
         case MK_OPT_SKIP_PUBLISH:
             h->skip_publish = (int)value;
+            return MK_OK;
+        case MK_OPT_PREFETCH_SLOTS:
+            if (value < 0 || value > 64) return MK_ERR_INVALID_ARG;
+            h->prefetch_slots = (int)value;
             return MK_OK;
     }
     return MK_ERR_INVALID_ARG;
@@ -482,11 +496,21 @@ mk_status mk_debug_buffer(const mk_handle* h, int32_t which, void** dev_ptr, int
     if (!h || !dev_ptr || !bytes) return MK_ERR_INVALID_ARG;
     const mk::Plan& p = h->plan;
     const int64_t B = p.maxB;
+    const bool tg = h->last_batch <= mk::kMaxTaggedBatch;
     switch (which) {
-        case MK_BUF_X: *dev_ptr = p.x; *bytes = 4 * B * p.d; return MK_OK;
-        case MK_BUF_QKV: *dev_ptr = p.qkv; *bytes = 4 * B * p.qkv_rows; return MK_OK;
-        case MK_BUF_ATTN: *dev_ptr = p.attn; *bytes = 4 * B * p.Hq * p.hd; return MK_OK;
-        case MK_BUF_H: *dev_ptr = p.h; *bytes = 4 * B * p.F; return MK_OK;
+        case MK_BUF_X:
+            *dev_ptr = tg ? (void*)p.x : (void*)p.xf;
+            *bytes = (tg ? 8 : 4) * B * p.d;
+            return MK_OK;
+        case MK_BUF_QKV: *dev_ptr = p.qkv; *bytes = 8 * B * p.qkv_rows; return MK_OK;
+        case MK_BUF_ATTN:
+            *dev_ptr = tg ? (void*)p.attn : (void*)p.attnf;
+            *bytes = (tg ? 8 : 4) * B * p.Hq * p.hd;
+            return MK_OK;
+        case MK_BUF_H:
+            *dev_ptr = tg ? (void*)p.h : (void*)p.hf;
+            *bytes = (tg ? 8 : 4) * B * p.F;
+            return MK_OK;
     }
     return MK_ERR_INVALID_ARG;
 }
@@ -628,18 +652,20 @@ extern "C" mk_status mk_decode_step_noalloc(
     const size_t o_layers = take(sizeof(mk::LayerPlan) * L);
     const size_t o_gains = take(sizeof(float) * (size_t)(2 * L + 1) * d);
     const size_t o_rope = take(sizeof(float2) * (size_t)desc->max_positions * (hd / 2));
-    const size_t o_x = take(sizeof(float) * maxB * d);
-    const size_t o_qkv = take(sizeof(float) * maxB * qkv_rows);
-    const size_t o_attn = take(sizeof(float) * maxB * Hq * hd);
-    const size_t o_h = take(sizeof(float) * maxB * F);
-    const size_t o_po = take(sizeof(float) * (size_t)maxB * Hkv * C * G * hd);
-    const size_t o_pml = take(sizeof(float2) * (size_t)maxB * Hkv * C * G);
     const size_t o_am = take(sizeof(float2) * (size_t)C * maxB);
-    const size_t counters_words = (size_t)(2 + L * mk::kStagesPerLayer) * mk::kCounterStride;
-    const size_t arrivals_words = (size_t)(L * maxB * Hkv + 1) * mk::kCounterStride;
-    const size_t o_zero = off;  // counters, arrivals, status: contiguous, cleared every call
-    const size_t o_cnt = take(sizeof(uint32_t) * counters_words);
-    const size_t o_arr = take(sizeof(uint32_t) * arrivals_words);
+    const size_t o_xf = take(sizeof(float) * (size_t)maxB * d);
+    const size_t o_attnf = take(sizeof(float) * (size_t)maxB * Hq * hd);
+    const size_t o_hf = take(sizeof(float) * (size_t)maxB * F);
+    // cleared every call (every call runs with tag epoch 1 and counter epoch 1): the
+    // tagged activations and attention partials, the counters and the status word
+    const size_t o_zero = off;
+    const size_t o_x = take(8 * (size_t)maxB * d);
+    const size_t o_qkv = take(8 * (size_t)maxB * qkv_rows);
+    const size_t o_attn = take(8 * (size_t)maxB * Hq * hd);
+    const size_t o_h = take(8 * (size_t)maxB * F);
+    const size_t o_part = take(8 * (size_t)maxB * Hkv * C * (G * hd + 2 * G));
+    const size_t o_cnt = take(sizeof(uint32_t) * (size_t)(1 + L * mk::kStagesPerLayer) * mk::kCounterStride);
+    const size_t o_arr = take(sizeof(uint32_t) * mk::kCounterStride);
     const size_t o_status = take(sizeof(int) * 4);
     if (off > kNoAllocScratchBytes) return MK_ERR_INVALID_ARG;  // model/batch too large
     unsigned char* base = D->base;
@@ -707,14 +733,16 @@ extern "C" mk_status mk_decode_step_noalloc(
     p.lm_head = (const bf16*)weights->lm_head;
     p.final_gain = gains + (size_t)(2 * L) * d;
     p.rope = su.rope_dst;
-    p.x = (float*)(base + o_x);
-    p.qkv = (float*)(base + o_qkv);
-    p.attn = (float*)(base + o_attn);
-    p.h = (float*)(base + o_h);
-    p.part_o = (float*)(base + o_po);
-    p.part_ml = (float2*)(base + o_pml);
-    p.amax_part = (float2*)(base + o_am);
+    p.x = (uint64_t*)(base + o_x);
+    p.qkv = (uint64_t*)(base + o_qkv);
+    p.attn = (uint64_t*)(base + o_attn);
+    p.h = (uint64_t*)(base + o_h);
+    p.part = (uint64_t*)(base + o_part);
+    p.xf = (float*)(base + o_xf);
+    p.attnf = (float*)(base + o_attnf);
+    p.hf = (float*)(base + o_hf);
     p.counters = (uint32_t*)(base + o_cnt);
+    p.amax_part = (float2*)(base + o_am);
     p.arrivals = (uint32_t*)(base + o_arr);
     p.status = (int*)(base + o_status);
     p.kv = (bf16*)kv_pool;
@@ -727,10 +755,10 @@ extern "C" mk_status mk_decode_step_noalloc(
     a.logits = logits;
     a.max_pages = max_pages_per_seq;
     a.B = batch;
-    a.stage_target = (uint32_t)C;  // counters start at zero every call: epoch 1
-    a.embed_target = (uint32_t)C;
-    a.attn_target = (uint32_t)batch * (uint32_t)Hkv;
+    a.epoch = 1;  // every tagged word and counter was cleared above
+    a.stage_target = (uint32_t)C;
     a.skip_publish = -1;
+    a.prefetch_slots = mk::kDefaultPrefetchSlots;
     a.timeout_ns = 1000000000LL;
     void* args[] = {&a};
     const void* fn = hd == 128 ? (const void*)mk::decode_step_kernel<128>

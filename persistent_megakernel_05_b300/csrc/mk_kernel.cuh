@@ -32,7 +32,8 @@ typedef __nv_bfloat16 bf16;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
-constexpr int kThreads = 32 + kConsumerThreads;   // warp 0 = producer
+constexpr int kThreads = 64 + kConsumerThreads;   // warp 0 = loader, warp 9 = L2 prefetcher
+constexpr int kDefaultPrefetchSlots = 0;          // L2 prefetch lead (slots); 0 = off
 constexpr int kStages = 6;                         // shared-memory ring depth
 constexpr int KCW = 2048;                          // GEMV k-chunk: columns of a weight slot
 constexpr int kGroupRows = 8;                      // weight rows per ring slot
@@ -56,7 +57,7 @@ __device__ __forceinline__ void trace_event(int cta, int& n, int base, uint32_t 
         g_mk_trace[cta][base + n++] = make_ulonglong2(globaltimer(), ((unsigned long long)code << 32) | arg);
 }
 #define MK_TRACE_C(c, code, arg) do { if ((c).tid == 0) trace_event(blockIdx.x, (c).tn, 0, code, arg); } while (0)
-#define MK_TRACE_P(pr, code, arg) do { if ((pr).lane == 0) trace_event(blockIdx.x, (pr).tn, kTraceEvents / 2, code, arg); } while (0)
+#define MK_TRACE_P(pr, code, arg) do { if ((pr).lane == 0 && !(pr).pf) trace_event(blockIdx.x, (pr).tn, kTraceEvents / 2, code, arg); } while (0)
 #else
 #define MK_TRACE_C(c, code, arg) do { } while (0)
 #define MK_TRACE_P(pr, code, arg) do { } while (0)
@@ -92,15 +93,20 @@ struct Plan {
     const bf16* lm_head;
     const float* final_gain;            // fp32, permuted
     const float2* rope;                 // [max_pos][hd/2] (cos, sin)
-    float* x;                           // [maxB][d]  residual stream, permuted
-    float* qkv;                         // [maxB][qkv_rows] natural order, pre-RoPE
-    float* attn;                        // [maxB][Hq*hd] permuted
-    float* h;                           // [maxB][F] permuted
-    float* part_o;                      // [maxB*Hkv][C][G][hd]
-    float2* part_ml;                    // [maxB*Hkv][C][G] (m, l)
-    float2* amax_part;                  // [C][maxB] (value, index as float bits)
+    // activations between stages, as tagged words (fp32 value | write tag)
+    uint64_t* x;                        // [maxB][d]  residual stream, permuted
+    uint64_t* qkv;                      // [maxB][qkv_rows] natural order, pre-RoPE
+    uint64_t* attn;                     // [maxB][Hq*hd] permuted
+    uint64_t* h;                        // [maxB][F] permuted
+    uint64_t* part;                     // [maxB*Hkv][C] records: o [G][hd], then (m, l) [G]
+    // batches above kMaxTaggedBatch: x, attn, h as plain fp32 (same layouts), published
+    // by per-stage counters with release / acquire ordering instead of tags
+    float* xf;
+    float* attnf;
+    float* hf;
     uint32_t* counters;                 // stage counters, kCounterStride apart
-    uint32_t* arrivals;                 // [L][maxB*Hkv] + 1 (argmax), kCounterStride apart
+    float2* amax_part;                  // [C][maxB] (value, index as float bits)
+    uint32_t* arrivals;                 // argmax arrival counter
     int* status;                        // [0] code, [1] task
     bf16* kv;                           // paged pool base
     const void* kv_map;                 // CUtensorMap of the pool as [rows][hd], 128B swizzle
@@ -116,17 +122,30 @@ struct StepArgs {
     float* logits;                      // may be null
     int max_pages;
     int B;
-    uint32_t stage_target;              // epoch * C
-    uint32_t attn_target;               // cumulative (sum of batch sizes) * Hkv
-    uint32_t embed_target;              // epoch * C
-    int skip_publish;                   // task id whose publish is suppressed, or -1
+    uint32_t epoch;                     // step number mod 2^20, never 0: high bits of every tag
+    uint32_t stage_target;              // counter target of every stage: steps since reset * C
+    int skip_publish;                   // task id whose outputs are never written, or -1
+    int prefetch_slots;                 // L2 prefetch lead over the loader, in slots (0 = off)
     long long timeout_ns;
 };
 
-// counter slots
+// Up to this batch size the activations between stages travel as tagged words (one
+// read latency per hand-off, no fence); above it, as fp32 behind counters, because a
+// tagged word doubles the bytes every CTA reads and the registers a poll holds.
+constexpr int kMaxTaggedBatch = 4;
+__device__ __forceinline__ bool tagged(const StepArgs& a) { return a.B <= kMaxTaggedBatch; }
+
+// counter slots (batches above kMaxTaggedBatch)
 __device__ __forceinline__ int cnt_embed() { return 0; }
 __device__ __forceinline__ int cnt_stage(int l, int s) { return 1 + l * kStagesPerLayer + s; }
-__device__ __forceinline__ int cnt_lm(int L) { return 1 + L * kStagesPerLayer; }
+
+// Tags of the tagged-word writes: (epoch, layer, producer). Two consecutive writes of a
+// word never carry the same tag, so a stale word is never taken for the awaited one.
+enum TagCode { TAG_EMBED = 0, TAG_QKV = 1, TAG_PART = 2, TAG_ATTN = 3, TAG_O = 4, TAG_GU = 5,
+               TAG_DOWN = 6 };
+__device__ __forceinline__ uint32_t tag_of(const StepArgs& a, int l, int code) {
+    return (a.epoch << 12) | ((uint32_t)l << 3) | (uint32_t)code;
+}
 
 // column permutation of fp32 activation rows: within each 64-column block, thread t of
 // an mma quad finds its 16 B-operand values (8 column pairs) in 4 consecutive float4s
@@ -143,7 +162,9 @@ struct Smem {
     float xown[kMaxBatch][kMaxOwnRows];    // this CTA's rows of the residual stream
     volatile int abort;
     int bcast;
-    int pad_[6];
+    volatile uint32_t lseq;  // ring slots the loader has started filling
+    int pad_[5];
+    LayerPlan lp[2];         // consumers' copies of the plans of layers l (l & 1) and l + 1
     uint64_t full[kStages];
     uint64_t empty[kStages];
     __align__(16) bf16 knew[128];
@@ -194,17 +215,60 @@ __device__ bool poll_counter(const StepArgs& a, Smem* sm, const uint32_t* c, uin
 }
 
 // all consumer threads: wait for a stage counter
-__device__ __forceinline__ bool consumer_wait(Ctx& c, int slot, uint32_t target, int task) {
-    if (c.tid == 0) poll_counter(*c.a, c.sm, c.a->p.counters + slot * kCounterStride, target, task);
+__device__ __forceinline__ bool consumer_wait(Ctx& c, int slot, int task) {
+    if (c.tid == 0) poll_counter(*c.a, c.sm, c.a->p.counters + slot * kCounterStride, c.a->stage_target, task);
     consumer_sync();
     return !c.sm->abort;
 }
 
+// all consumer threads: count this CTA's completion of a stage
 __device__ __forceinline__ void publish(Ctx& c, int slot, int task) {
     consumer_sync();
     // bar.sync orders every consumer thread's stores before thread 0's release add
     if (c.tid == 0 && !c.sm->abort && c.a->skip_publish != task)
         red_release_add(c.a->p.counters + slot * kCounterStride, 1u);
+}
+
+// Back-off step of a thread polling tagged words: false once the wait must end (the CTA
+// aborts, another CTA latched an error, or the time limit passes: kErrTimeout for `task`).
+__device__ __noinline__ bool spin_check(const StepArgs& a, Smem* sm, int task, uint64_t* t0) {
+    if (status_bad(a.p)) { sm->abort = 1; return false; }
+    const uint64_t now = globaltimer();
+    if (*t0 == 0) { *t0 = now; return true; }
+    if ((long long)(now - *t0) > a.timeout_ns) {
+        set_error(a.p, sm, kErrTimeout, task);
+        return false;
+    }
+    return true;
+}
+struct Spin {
+    uint64_t t0 = 0;
+    int it = 0;
+    __device__ __forceinline__ bool again(const StepArgs& a, Smem* sm, int task) {
+        if (sm->abort) return false;
+        if ((++it & 15) == 0 && !spin_check(a, sm, task, &t0)) return false;
+        __nanosleep(32);
+        return true;
+    }
+};
+
+// Slow path of every ring wait (one lane): sleep on the barrier phase until it completes
+// (true), the CTA aborts, another CTA latches an error, or `limit_ns` passes, which
+// latches kErrTimeout for `task` (false). Out of line: it is cold code.
+__device__ __noinline__ bool ring_wait_slow(const StepArgs* a, Smem* sm, uint32_t bar, uint32_t parity,
+                                            long long limit_ns, int task) {
+    const uint64_t t0 = globaltimer();
+    for (int it = 0;; ++it) {
+        if (mbar_wait_sleep(bar, parity, 20000u)) return true;
+        if (sm->abort) return false;
+        if ((it & 7) == 7) {
+            if (status_bad(a->p)) { sm->abort = 1; return false; }
+            if ((long long)(globaltimer() - t0) > limit_ns) {
+                set_error(a->p, sm, kErrTimeout, task);
+                return false;
+            }
+        }
+    }
 }
 
 // a consumer warp waits for ring slot `seq` to be full; warp-uniform result
@@ -214,21 +278,8 @@ __device__ __forceinline__ bool wait_full(Ctx& c, int task) {
     int ok = 1;
     if (c.lane == 0) {
         if (c.sm->abort) ok = 0;
-        else if (!mbar_try_wait(bar, parity)) {
-            uint64_t t0 = globaltimer();
-            for (int it = 0;; ++it) {
-                if (mbar_wait_sleep(bar, parity, 20000u)) break;
-                if (c.sm->abort) { ok = 0; break; }
-                if ((it & 7) == 7) {
-                    if (status_bad(c.a->p)) { c.sm->abort = 1; ok = 0; break; }
-                    if ((long long)(globaltimer() - t0) > c.a->timeout_ns) {
-                        set_error(c.a->p, c.sm, kErrTimeout, task);
-                        ok = 0;
-                        break;
-                    }
-                }
-            }
-        }
+        else if (!mbar_try_wait(bar, parity))
+            ok = ring_wait_slow(c.a, c.sm, bar, parity, c.a->timeout_ns, task);
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) mbar_try_wait(bar, parity);  // every lane acquires the completed phase
@@ -248,15 +299,18 @@ __device__ __forceinline__ void cta_rows(int R, int cta, int C, int& r0, int& r1
 }
 
 struct GemvStage {
-    int kind, layer, R, K, task_id, cnt_wait, cnt_pub;
-    uint32_t wait_target;
+    int kind, layer, R, K, task_id;
+    uint32_t src_tag, out_tag;   // tag awaited on every source word / written on the outputs
     const bf16 *w0, *w1, *w2;
     int split1, split2;          // QKV: row boundaries between wq / wk / wv
-    const float* src;            // B operand source rows [b][K], permuted
+    const uint64_t* src;         // B operand source rows [b][K] (tagged words), permuted
+    const float* srcf;           // the same rows as fp32 (batches above kMaxTaggedBatch)
+    int cnt_wait, cnt_pub;       // counter slots (batches above kMaxTaggedBatch)
     const float* gain;           // permuted fp32 gain or null (no norm)
 };
 
-__device__ GemvStage make_gemv(const StepArgs& a, int kind, int l) {
+// `lp` is layer l's plan (the consumers keep a copy in shared memory)
+__device__ GemvStage make_gemv(const StepArgs& a, int kind, int l, const LayerPlan& lp) {
     const Plan& p = a.p;
     GemvStage s;
     s.kind = kind;
@@ -264,39 +318,49 @@ __device__ GemvStage make_gemv(const StepArgs& a, int kind, int l) {
     s.w1 = s.w2 = nullptr;
     s.split1 = s.split2 = 0;
     s.gain = nullptr;
-    s.wait_target = a.stage_target;
+    s.out_tag = 0;
     if (kind == G_LM) {
-        s.R = p.V; s.K = p.d; s.w0 = p.lm_head; s.src = p.x; s.gain = p.final_gain;
-        s.task_id = p.L * 16; s.cnt_wait = cnt_stage(p.L - 1, ST_DOWN); s.cnt_pub = cnt_lm(p.L);
+        s.R = p.V; s.K = p.d; s.w0 = p.lm_head; s.src = p.x; s.srcf = p.xf; s.gain = p.final_gain;
+        s.task_id = p.L * 16; s.src_tag = tag_of(a, p.L - 1, TAG_DOWN);
+        s.cnt_wait = cnt_stage(p.L - 1, ST_DOWN); s.cnt_pub = -1;
         return s;
     }
-    const LayerPlan& lp = p.layers[l];
     switch (kind) {
         case G_QKV:
             s.R = p.qkv_rows; s.K = p.d; s.w0 = lp.wq; s.w1 = lp.wk; s.w2 = lp.wv;
             s.split1 = p.Hq * p.hd; s.split2 = (p.Hq + p.Hkv) * p.hd;
-            s.src = p.x; s.gain = lp.attn_gain; s.task_id = l * 16 + ST_QKV;
+            s.src = p.x; s.srcf = p.xf; s.gain = lp.attn_gain; s.task_id = l * 16 + ST_QKV;
+            s.src_tag = l == 0 ? tag_of(a, 0, TAG_EMBED) : tag_of(a, l - 1, TAG_DOWN);
+            s.out_tag = tag_of(a, l, TAG_QKV);
             s.cnt_wait = l == 0 ? cnt_embed() : cnt_stage(l - 1, ST_DOWN);
-            if (l == 0) s.wait_target = a.embed_target;
-            s.cnt_pub = cnt_stage(l, ST_QKV);
+            s.cnt_pub = -1;  // q|k|v always travel as tagged words
             break;
         case G_O:
-            s.R = p.d; s.K = p.Hq * p.hd; s.w0 = lp.wo; s.src = p.attn;
-            s.task_id = l * 16 + ST_O; s.cnt_wait = cnt_stage(l, ST_ATTN);
-            s.wait_target = a.attn_target; s.cnt_pub = cnt_stage(l, ST_O);
+            s.R = p.d; s.K = p.Hq * p.hd; s.w0 = lp.wo; s.src = p.attn; s.srcf = p.attnf;
+            s.task_id = l * 16 + ST_O;
+            s.src_tag = tag_of(a, l, TAG_ATTN);
+            s.out_tag = tag_of(a, l, TAG_O);
+            s.cnt_wait = cnt_stage(l, ST_ATTN); s.cnt_pub = cnt_stage(l, ST_O);
             break;
         case G_GU:
-            s.R = p.F; s.K = p.d; s.w0 = lp.w_gate; s.w1 = lp.w_up; s.src = p.x;
-            s.gain = lp.mlp_gain; s.task_id = l * 16 + ST_GU; s.cnt_wait = cnt_stage(l, ST_O);
-            s.cnt_pub = cnt_stage(l, ST_GU);
+            s.R = p.F; s.K = p.d; s.w0 = lp.w_gate; s.w1 = lp.w_up; s.src = p.x; s.srcf = p.xf;
+            s.gain = lp.mlp_gain; s.task_id = l * 16 + ST_GU;
+            s.src_tag = tag_of(a, l, TAG_O);
+            s.out_tag = tag_of(a, l, TAG_GU);
+            s.cnt_wait = cnt_stage(l, ST_O); s.cnt_pub = cnt_stage(l, ST_GU);
             break;
         default:  // G_DOWN
-            s.R = p.d; s.K = p.F; s.w0 = lp.w_down; s.src = p.h;
-            s.task_id = l * 16 + ST_DOWN; s.cnt_wait = cnt_stage(l, ST_GU);
-            s.cnt_pub = cnt_stage(l, ST_DOWN);
+            s.R = p.d; s.K = p.F; s.w0 = lp.w_down; s.src = p.h; s.srcf = p.hf;
+            s.task_id = l * 16 + ST_DOWN;
+            s.src_tag = tag_of(a, l, TAG_GU);
+            s.out_tag = tag_of(a, l, TAG_DOWN);
+            s.cnt_wait = cnt_stage(l, ST_GU); s.cnt_pub = cnt_stage(l, ST_DOWN);
             break;
     }
     return s;
+}
+__device__ __forceinline__ GemvStage make_gemv(const StepArgs& a, int kind, int l) {
+    return make_gemv(a, kind, l, a.p.layers[kind == G_LM ? 0 : l]);
 }
 
 // stages whose individual ring slots are traced in MK_TRACE builds
@@ -415,8 +479,31 @@ struct Producer {
     uint64_t policy;
     int lane;
     int tn = 0;  // trace events recorded (MK_TRACE builds)
+    // Prefetch mode: the same schedule walked ahead of the loader, each copy replaced by
+    // an L2 prefetch of its source, so that HBM keeps streaming while the consumers wait
+    // on a dependency and the loader on a full ring. It never blocks anyone and never
+    // reports errors: when anything goes wrong it simply stops.
+    bool pf = false;
 
     __device__ bool acquire_slot(int task) {
+        if (pf) {
+            int ok = 1;
+            if (lane == 0) {
+                const uint32_t lead = (uint32_t)a->prefetch_slots;
+                uint64_t t0 = 0;
+                for (int it = 0; seq >= sm->lseq + lead; ++it) {
+                    if (sm->abort) { ok = 0; break; }
+                    __nanosleep(128);
+                    if ((it & 63) == 63) {
+                        const uint64_t now = globaltimer();
+                        if (t0 == 0) t0 = now;
+                        else if ((long long)(now - t0) > a->timeout_ns) { ok = 0; break; }
+                    }
+                }
+            }
+            return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        }
+        if (lane == 0) sm->lseq = seq;
         int ok = 1;
         if (lane == 0) {
             if (sm->abort) ok = 0;
@@ -425,26 +512,18 @@ struct Producer {
                 const uint32_t parity = ((seq / kStages) - 1) & 1;
                 if (!mbar_try_wait(bar, parity)) {
                     MK_TRACE_P(*this, TR_P_BLOCK, task);
-                    uint64_t t0 = globaltimer();
-                    for (int it = 0;; ++it) {
-                        if (mbar_wait_sleep(bar, parity, 20000u)) break;
-                        if (sm->abort) { ok = 0; break; }
-                        if ((it & 7) == 7) {
-                            if (status_bad(a->p)) { sm->abort = 1; ok = 0; break; }
-                            // a full ring only stalls when a consumer stalls; let the
-                            // consumer's own (shorter) wait report the cause first
-                            if ((long long)(globaltimer() - t0) > 4 * a->timeout_ns) {
-                                set_error(a->p, sm, kErrTimeout, task);
-                                ok = 0;
-                                break;
-                            }
-                        }
-                    }
+                    // a full ring only stalls when a consumer stalls; let the consumer's
+                    // own (shorter) wait report the cause first
+                    ok = ring_wait_slow(a, sm, bar, parity, 4 * a->timeout_ns, task);
                     MK_TRACE_P(*this, TR_P_GO, task);
                 }
             }
         }
         return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    }
+    __device__ __forceinline__ void copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+        if (pf) l2_prefetch_1d(src, bytes);
+        else tma_load_1d(dst, src, bytes, bar, policy);
     }
     __device__ uint32_t slot_addr() const { return ring_s + (seq % kStages) * kSlotBytes; }
     __device__ uint32_t full_bar() const { return smem_u32(&sm->full[seq % kStages]); }
@@ -465,7 +544,7 @@ struct Producer {
                     const int nr = group_rows(s, n, gi, ngate);
                     const int ncop = (nr + geo.rpc - 1) / geo.rpc;
                     const uint32_t dst = slot_addr(), bar = full_bar();
-                    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nr * geo.kc * 2));
+                    if (lane == 0 && !pf) mbar_arrive_expect_tx(bar, (uint32_t)(nr * geo.kc * 2));
                     __syncwarp();
                     if (lane < ncop) {
                         const int i0 = lane * geo.rpc;
@@ -474,14 +553,14 @@ struct Producer {
                         const bf16* p1 = gemv_row(s, r0, gi, ngate, i0 + cnt - 1) + k0;
                         const uint32_t d0 = dst + lane * geo.cpitch;
                         if (p1 == p0 + (size_t)(cnt - 1) * s.K) {
-                            tma_load_1d(d0, p0, (uint32_t)(cnt * geo.kc * 2), bar, policy);
+                            copy(d0, p0, (uint32_t)(cnt * geo.kc * 2), bar);
                         } else {  // the rows straddle two weight tensors (q|k|v)
                             for (int i = 0; i < cnt; ++i)
-                                tma_load_1d(d0 + i * geo.kc * 2, gemv_row(s, r0, gi, ngate, i0 + i) + k0,
-                                            (uint32_t)(geo.kc * 2), bar, policy);
+                                copy(d0 + i * geo.kc * 2, gemv_row(s, r0, gi, ngate, i0 + i) + k0,
+                                     (uint32_t)(geo.kc * 2), bar);
                         }
                     }
-                    if (trace_slots(s)) MK_TRACE_P(*this, TR_S_ISSUE, seq);
+                    if (trace_slots(s) && !pf) MK_TRACE_P(*this, TR_S_ISSUE, seq);
                     ++seq;
                 }
             }
@@ -512,19 +591,20 @@ struct Producer {
                     bad = page < 0 || page >= p.num_pages;
                 }
                 if (__any_sync(0xffffffffu, bad)) {
-                    if (lane == 0) set_error(p, sm, kErrBadPage, l * 16 + ST_ATTN);
+                    if (lane == 0 && !pf) set_error(p, sm, kErrBadPage, l * 16 + ST_ATTN);
                     ok = false;
                     return;
                 }
                 const uint32_t dst = slot_addr(), bar = full_bar();
-                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(np * 2 * 2 * kPage * HD));
+                if (lane == 0 && !pf) mbar_arrive_expect_tx(bar, (uint32_t)(np * 2 * 2 * kPage * HD));
                 __syncwarp();
                 if (lane < nbox) {
                     const int row = (((l * p.num_pages + page) * 2 + kv) * p.Hkv + g) * kPage;
-                    tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, p.kv_map, bx * 64, row,
-                                bar, policy);
+                    if (pf) l2_prefetch_2d(p.kv_map, bx * 64, row);
+                    else tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, p.kv_map, bx * 64, row,
+                                     bar, policy);
                 }
-                if (l == 1) MK_TRACE_P(*this, TR_S_ISSUE, seq);
+                if (l == 1 && !pf) MK_TRACE_P(*this, TR_S_ISSUE, seq);
                 ++seq;
             }
         });
@@ -546,7 +626,7 @@ struct Producer {
         }
         if (ok) gemv(make_gemv(*a, G_LM, 0), cta);
         // drain: never leave a copy in flight into shared memory
-        if (lane == 0) {
+        if (lane == 0 && !pf) {
             const uint32_t first = seq > (uint32_t)kStages ? seq - kStages : 0;
             for (uint32_t k = first; k < seq; ++k) {
                 const uint32_t bar = smem_u32(&sm->full[k % kStages]);
@@ -564,15 +644,43 @@ struct Producer {
 };
 
 // ------------------------------------------------------------------ consumer pieces
-__device__ __forceinline__ void rms_scale(Ctx& c, const float* src, int K) {
-    // rstd[b] = 1 / sqrt(mean(src[b]^2) + eps); fixed summation order
+// rstd[b] = 1 / sqrt(mean(src[b]^2) + eps); fixed summation order. Small batches read
+// the tagged rows (4 pairs in flight per thread and round), larger ones the fp32 rows.
+__device__ __forceinline__ void rms_scale(Ctx& c, const GemvStage& s) {
     const StepArgs& a = *c.a;
+    const int K = s.K;
     float* red = c.scratch;
     for (int b = 0; b < a.B; ++b) {
         float ss = 0.f;
-        for (int k = c.tid * 4; k < K; k += kConsumerThreads * 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)b * K + k));
-            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        if (tagged(a)) {
+            const uint64_t* row = s.src + (size_t)b * K;
+            for (int k0 = c.tid * 2; k0 < K; k0 += kConsumerThreads * 8) {
+                uint64_t w[4][2];
+                Spin sp;
+                for (;;) {
+                    bool ok = true;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int k = k0 + j * kConsumerThreads * 2;
+                        w[j][0] = w[j][1] = (uint64_t)s.src_tag << 32;
+                        if (k < K) ll_ld2(row + k, w[j][0], w[j][1]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) ok = ok && ll_tag(w[j][0]) == s.src_tag && ll_tag(w[j][1]) == s.src_tag;
+                    if (ok || !sp.again(a, c.sm, s.task_id)) break;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (k0 + j * kConsumerThreads * 2 < K) {
+                        const float v0 = ll_val(w[j][0]), v1 = ll_val(w[j][1]);
+                        ss += v0 * v0 + v1 * v1;
+                    }
+            }
+        } else {
+            for (int k = c.tid * 4; k < K; k += kConsumerThreads * 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(s.srcf + (size_t)b * K + k));
+                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -603,21 +711,7 @@ __device__ __forceinline__ bool wait_full_at(Ctx& c, uint32_t q, int task) {
     const uint32_t bar = smem_u32(&c.sm->full[slot]);
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     int ok = 1;
-    if (c.lane == 0) {
-        uint64_t t0 = globaltimer();
-        for (int it = 0;; ++it) {
-            if (mbar_wait_sleep(bar, parity, 20000u)) break;
-            if (c.sm->abort) { ok = 0; break; }
-            if ((it & 7) == 7) {
-                if (status_bad(c.a->p)) { c.sm->abort = 1; ok = 0; break; }
-                if ((long long)(globaltimer() - t0) > c.a->timeout_ns) {
-                    set_error(c.a->p, c.sm, kErrTimeout, task);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-    }
+    if (c.lane == 0) ok = ring_wait_slow(c.a, c.sm, bar, parity, c.a->timeout_ns, task);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) mbar_try_wait(bar, parity);  // every lane acquires the completed phase
     return ok != 0;
@@ -665,28 +759,52 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
     float* red = c.scratch;  // [8 warps][128 vrows][BP]
     for (int i = c.lane; i < kTaskRows * BP; i += 32) red[c.cw * kTaskRows * BP + i] = 0.f;
     __syncwarp();
-    for (int k0 = 0; k0 < s.K; k0 += KCW) {
-        const SlotGeom geo = slot_geom(s.K, k0);
-        const int piece = 32 * c.cw + c.lane;
-        const bool has_p = piece < (geo.kc >> 3);
-        float xv[BP][8];
+    const int piece = 32 * c.cw + c.lane;
+    // This lane's tagged activation words of chunk k0: BP rows x 8 columns (4 pairs).
+    auto issue = [&](int k0, uint64_t (&w)[BP][8]) {
+        const int col = k0 + 8 * piece;
+        const int base = (col & ~63) + 2 * ((col >> 3) & 7);  // permuted pair (t = 0)
+        const bool has = piece < (min(KCW, s.K - k0) >> 3);
 #pragma unroll
         for (int b = 0; b < BP; ++b)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xv[b][i] = 0.f;
+            for (int t = 0; t < 4; ++t) {
+                w[b][2 * t] = w[b][2 * t + 1] = (uint64_t)s.src_tag << 32;
+                if (b < B && has) ll_ld2(s.src + (size_t)b * s.K + base + 16 * t, w[b][2 * t], w[b][2 * t + 1]);
+            }
+    };
+    auto tags_ok = [&](const uint64_t (&w)[BP][8]) {
+        bool ok = true;
+#pragma unroll
+        for (int b = 0; b < BP; ++b)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ok = ok && ll_tag(w[b][i]) == s.src_tag;
+        return ok;
+    };
+    // With BP == 1 the next chunk's words are requested before this chunk's slots are
+    // processed, so a multi-chunk row (K > KCW) pays one read latency, not one per chunk.
+    constexpr bool kAhead = BP == 1;
+    uint64_t wn[BP][8];
+    issue(0, wn);
+    for (int k0 = 0; k0 < s.K; k0 += KCW) {
+        const SlotGeom geo = slot_geom(s.K, k0);
+        const bool has_p = piece < (geo.kc >> 3);
+        float xv[BP][8];
+        if (!kAhead && k0 > 0) issue(k0, wn);
+        if (!c.sm->abort) {  // poll until every word carries the awaited tag
+            Spin sp;
+            while (!tags_ok(wn)) {
+                if (!sp.again(a, c.sm, s.task_id)) break;
+                issue(k0, wn);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < BP; ++b)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xv[b][i] = (b < B && has_p) ? ll_val(wn[b][i]) : 0.f;
+        if (kAhead && k0 + KCW < s.K) issue(k0 + KCW, wn);
         const int col = k0 + 8 * piece;
         const int base = (col & ~63) + 2 * ((col >> 3) & 7);  // permuted pair (t = 0)
-        if (has_p && !c.sm->abort) {
-#pragma unroll
-            for (int b = 0; b < BP; ++b)
-                if (b < B)
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const float2 v = __ldcg(reinterpret_cast<const float2*>(s.src + (size_t)b * s.K + base + 16 * t));
-                        xv[b][2 * t] = v.x;
-                        xv[b][2 * t + 1] = v.y;
-                    }
-        }
         if (s.gain) {
             if (fused_norm) {  // this chunk is the whole row: sum of squares from registers
 #pragma unroll
@@ -805,11 +923,13 @@ __device__ __forceinline__ void fma_epilogue(Ctx& c, const GemvStage& s, int r0,
         for (int w = 0; w < kConsumerWarps; ++w) y += red[(w * kTaskRows + vr) * BP + b];
         return y;
     };
+    const bool pub = a.skip_publish != s.task_id;
     switch (s.kind) {
         case G_QKV:
             for (int e = c.tid; e < n * B; e += kConsumerThreads) {
                 const int r = e / B, b = e % B;
-                p.qkv[(size_t)b * p.qkv_rows + r0 + r] = ysum(r, b);
+                const float y = ysum(r, b);
+                if (pub) ll_st(p.qkv + (size_t)b * p.qkv_rows + r0 + r, y, s.out_tag);
             }
             break;
         case G_O:
@@ -820,7 +940,7 @@ __device__ __forceinline__ void fma_epilogue(Ctx& c, const GemvStage& s, int r0,
                 const int r = e / B, b = e % B;
                 const float xn = c.sm->xown[b][r0 + r - a0] + ysum(r, b);
                 c.sm->xown[b][r0 + r - a0] = xn;
-                p.x[(size_t)b * p.d + perm_col(r0 + r)] = xn;
+                if (pub) ll_st(p.x + (size_t)b * p.d + perm_col(r0 + r), xn, s.out_tag);
             }
             break;
         }
@@ -828,7 +948,8 @@ __device__ __forceinline__ void fma_epilogue(Ctx& c, const GemvStage& s, int r0,
             const int up0 = kGroupRows * (num_groups(s, n) >> 1);
             for (int e = c.tid; e < n * B; e += kConsumerThreads) {
                 const int r = e / B, b = e % B;
-                p.h[(size_t)b * p.F + perm_col(r0 + r)] = silu(ysum(r, b)) * ysum(up0 + r, b);
+                const float y = silu(ysum(r, b)) * ysum(up0 + r, b);
+                if (pub) ll_st(p.h + (size_t)b * p.F + perm_col(r0 + r), y, s.out_tag);
             }
             break;
         }
@@ -862,7 +983,7 @@ __device__ __forceinline__ void gemv_mma(Ctx& c, const GemvStage& s, int r0, int
             for (int i = 0; i < 4; ++i) bfr[jj][i][0] = bfr[jj][i][1] = bfr[jj][i][2] = bfr[jj][i][3] = 0u;
             if (j < nblk && has_b && !c.sm->abort) {
                 const int col = k0 + 64 * j + 16 * t;
-                const float4* src = reinterpret_cast<const float4*>(s.src + (size_t)g * s.K + col);
+                const float4* src = reinterpret_cast<const float4*>(s.srcf + (size_t)g * s.K + col);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     float4 v = __ldcg(src + i);
@@ -944,48 +1065,20 @@ __device__ __forceinline__ void gemv_mma(Ctx& c, const GemvStage& s, int r0, int
     }
 }
 
-// Non-inlined (own register budget). Works on register copies of the context and of
-// the stage description; only the ring sequence number goes back to the caller.
-__device__ __noinline__ void gemv_task(Ctx& c_in, int kind, int layer, int r0, int r1) {
-    Ctx c = c_in;
+// Epilogues from the staged outputs yout[vrow][8] (vrow = 8 * group + row; GU: up rows
+// start at vrow 8 * ngate): the LM head at every batch, every stage above 4 rows.
+__device__ __forceinline__ void yout_epilogue(Ctx& c, const GemvStage& s, int r0, int r1,
+                                              const float* yout) {
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
-    const GemvStage s = make_gemv(a, kind, layer);
-    float* yout = c.scratch + kConsumerWarps * kTaskRows * 4;  // [128 vrows][8]
-    const bool fused = fused_norm_stage(a, s);
-    if (a.B <= 4 && s.kind != G_LM) {
-        if (a.B == 1) gemv_fma<1>(c, s, r0, r1, nullptr, fused);
-        else if (a.B == 2) gemv_fma<2>(c, s, r0, r1, nullptr, fused);
-        else gemv_fma<4>(c, s, r0, r1, nullptr, fused);
-        if (!c.sm->abort) {
-            if (a.B == 1) fma_epilogue<1>(c, s, r0, r1, cta_of(c));
-            else if (a.B == 2) fma_epilogue<2>(c, s, r0, r1, cta_of(c));
-            else fma_epilogue<4>(c, s, r0, r1, cta_of(c));
-        }
-        if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
-        c_in.seq = c.seq;
-        c_in.tn = c.tn;
-        return;
-    }
-    if (a.B == 1) gemv_fma<1>(c, s, r0, r1, yout, fused);
-    else if (a.B == 2) gemv_fma<2>(c, s, r0, r1, yout, fused);
-    else if (a.B <= 4) gemv_fma<4>(c, s, r0, r1, yout, fused);
-    else gemv_mma(c, s, r0, r1, yout);
-    consumer_sync();
-    if (c.sm->abort) {
-        c_in.seq = c.seq;
-        c_in.tn = c.tn;
-        return;
-    }
-
-    // epilogues (vrow = 8 * group + row; GU: up rows start at vrow 8 * ngate)
     const int n = r1 - r0;
     const int B = a.B;
+    const bool pub = a.skip_publish != s.task_id;
     switch (s.kind) {
         case G_QKV:
             for (int e = c.tid; e < n * B; e += kConsumerThreads) {
                 const int r = e / B, b = e % B;
-                p.qkv[(size_t)b * p.qkv_rows + r0 + r] = yout[r * 8 + b];
+                if (pub) ll_st(p.qkv + (size_t)b * p.qkv_rows + r0 + r, yout[r * 8 + b], s.out_tag);
             }
             break;
         case G_O:
@@ -996,7 +1089,9 @@ __device__ __noinline__ void gemv_task(Ctx& c_in, int kind, int layer, int r0, i
                 const int r = e / B, b = e % B;
                 const float xn = c.sm->xown[b][r0 + r - a0] + yout[r * 8 + b];
                 c.sm->xown[b][r0 + r - a0] = xn;
-                p.x[(size_t)b * p.d + perm_col(r0 + r)] = xn;
+                const size_t o = (size_t)b * p.d + perm_col(r0 + r);
+                if (!tagged(a)) p.xf[o] = xn;
+                else if (pub) ll_st(p.x + o, xn, s.out_tag);
             }
             break;
         }
@@ -1006,7 +1101,9 @@ __device__ __noinline__ void gemv_task(Ctx& c_in, int kind, int layer, int r0, i
                 const int r = e / B, b = e % B;
                 const float yg = yout[r * 8 + b];
                 const float yu = yout[(up0 + r) * 8 + b];
-                p.h[(size_t)b * p.F + perm_col(r0 + r)] = silu(yg) * yu;
+                const size_t o = (size_t)b * p.F + perm_col(r0 + r);
+                if (!tagged(a)) p.hf[o] = silu(yg) * yu;
+                else if (pub) ll_st(p.h + o, silu(yg) * yu, s.out_tag);
             }
             break;
         }
@@ -1039,25 +1136,65 @@ __device__ __noinline__ void gemv_task(Ctx& c_in, int kind, int layer, int r0, i
             break;
         }
     }
+}
+
+// Non-inlined, one function per arithmetic path, so that each gets its own register
+// budget. They work on register copies of the context and of the stage description;
+// only the ring sequence number (and the trace count) go back to the caller.
+template <int BP>
+__device__ __noinline__ void gemv_task_fma(Ctx& c_in, int kind, int layer, int r0, int r1) {
+    Ctx c = c_in;
+    const StepArgs& a = *c.a;
+    const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[layer & 1]);
+    const bool fused = fused_norm_stage(a, s);
+    if (s.kind != G_LM) {
+        gemv_fma<BP>(c, s, r0, r1, nullptr, fused);
+        if (!c.sm->abort) fma_epilogue<BP>(c, s, r0, r1, cta_of(c));
+    } else {
+        float* yout = c.scratch + kConsumerWarps * kTaskRows * 4;  // [128 vrows][8]
+        gemv_fma<BP>(c, s, r0, r1, yout, fused);
+        consumer_sync();
+        if (!c.sm->abort) yout_epilogue(c, s, r0, r1, yout);
+    }
     if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
     c_in.seq = c.seq;
     c_in.tn = c.tn;
+}
+__device__ __noinline__ void gemv_task_mma(Ctx& c_in, int kind, int layer, int r0, int r1) {
+    Ctx c = c_in;
+    const StepArgs& a = *c.a;
+    const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[layer & 1]);
+    float* yout = c.scratch + kConsumerWarps * kTaskRows * 4;  // [128 vrows][8]
+    gemv_mma(c, s, r0, r1, yout);
+    consumer_sync();
+    if (!c.sm->abort) yout_epilogue(c, s, r0, r1, yout);
+    if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
+    c_in.seq = c.seq;
+    c_in.tn = c.tn;
+}
+__device__ __forceinline__ void gemv_task(Ctx& c, int kind, int layer, int r0, int r1) {
+    const int B = c.a->B;
+    if (B == 1) gemv_task_fma<1>(c, kind, layer, r0, r1);
+    else if (B == 2) gemv_task_fma<2>(c, kind, layer, r0, r1);
+    else if (B <= 4) gemv_task_fma<4>(c, kind, layer, r0, r1);
+    else gemv_task_mma(c, kind, layer, r0, r1);
 }
 
 __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
     const Plan& p = c.a->p;
     int a0, a1;
     cta_rows(s.R, cta, p.C, a0, a1);
+    const bool tg = tagged(*c.a);
     if (a0 < a1) {
         MK_TRACE_C(c, TR_WAIT, s.task_id);
-        consumer_wait(c, s.cnt_wait, s.wait_target, s.task_id);
-        MK_TRACE_C(c, TR_READY, s.task_id);
-        if (s.gain && !fused_norm_stage(*c.a, s)) rms_scale(c, s.src, s.K);
+        if (!tg) consumer_wait(c, s.cnt_wait, s.task_id);
+        if (s.gain && !fused_norm_stage(*c.a, s)) rms_scale(c, s);
         if (trace_slots(s)) MK_TRACE_C(c, TR_G_NORM, 0);
         const int tr = task_rows(s.kind);
         for (int r0 = a0; r0 < a1; r0 += tr) gemv_task(c, s.kind, s.layer, r0, min(a1, r0 + tr));
     }
-    if (s.kind != G_LM) publish(c, s.cnt_pub, s.task_id);
+    if (!tg && s.cnt_pub >= 0) publish(c, s.cnt_pub, s.task_id);
+    else consumer_sync();  // every warp is done with the shared scratch of this stage
     MK_TRACE_C(c, TR_DONE, s.task_id);
 }
 
@@ -1065,11 +1202,10 @@ __device__ __forceinline__ int bg_id(const Plan& p, int b, int g) { return b * p
 
 // ---- attention: one piece (a CTA's share of one (b, kv head)) ----
 // After the key loop of a piece: merge the 8 warps' partial softmax states (left in
-// shared memory by the loop), write this split's partial, count the arrival, and if it
-// is the last split of its (sequence, kv head), merge all splits into the attention
-// output and publish. Non-inlined so the key loop keeps its registers to itself.
+// shared memory by the loop) and write this split's partial record as tagged words.
+// Non-inlined so the key loop keeps its registers to itself.
 template <int HD>
-__device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, int split, int nsplit) {
+__device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, int split) {
     Ctx c = c_in;
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
@@ -1081,118 +1217,132 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
     float* ws_l = ws_m + 64;                                  // [8][8]
     consumer_sync();
     const int bg = b * p.Hkv + g;
-    const size_t pbase = ((size_t)bg * p.C + split) * G;
-    if (!c.sm->abort) {
-        for (int e = c.tid; e < G * HD; e += kConsumerThreads) {
+    const int GHD = G * HD;
+    uint64_t* rec = p.part + ((size_t)bg * p.C + split) * (GHD + 2 * G);
+    const uint32_t tag = tag_of(a, l, TAG_PART);
+    if (!c.sm->abort && a.skip_publish != task) {
+        for (int e = 2 * c.tid; e < GHD; e += 2 * kConsumerThreads) {
             const int hl = e / HD, d = e % HD;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ws_m[w * 8 + hl]);
-            float o = 0.f, L = 0.f;
+            float o0 = 0.f, o1 = 0.f, L = 0.f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
                 const float mw = ws_m[w * 8 + hl];
                 const float f = mw == -INFINITY ? 0.f : expf(mw - M);
-                o += f * ws_o[(w * G + hl) * OS + d];
+                const float2 ov = *reinterpret_cast<const float2*>(ws_o + (w * G + hl) * OS + d);
+                o0 += f * ov.x;
+                o1 += f * ov.y;
                 L += f * ws_l[w * 8 + hl];
             }
-            p.part_o[(pbase + hl) * HD + d] = o;
-            if (d == 0) p.part_ml[pbase + hl] = make_float2(M, L);
+            ll_st2(rec + e, o0, o1, tag);
+            if (d == 0) ll_st2(rec + GHD + 2 * hl, M, L, tag);
         }
     }
-    // arrival: the last of the nsplit pieces merges them all
+    consumer_sync();  // the scratch is free for the next piece
+    if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_PART, (uint32_t)split);
+    c_in.tn = c.tn;
+}
+
+// The split-`split` CTA of a (sequence, kv head) merges output dims [j0, j1) of the
+// G heads (flattened h * HD + d) from all nsplit partial records: per head
+// M = max m_s, w_s = exp(m_s - M), L = sum w_s l_s, O = sum w_s o_s / L. Every split
+// takes an equal slice, so the merge costs one round of tagged reads instead of a
+// serial last-arriver pass.
+template <int HD>
+__device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int split, int nsplit) {
+    Ctx c = c_in;
+    const StepArgs& a = *c.a;
+    const Plan& p = a.p;
+    const int G = p.G, GHD = G * HD, RS = GHD + 2 * G;
+    const int task = l * 16 + ST_ATTN;
+    const uint32_t tp = tag_of(a, l, TAG_PART);
+    const int j0 = (int)((long long)split * GHD / nsplit), j1 = (int)((long long)(split + 1) * GHD / nsplit);
+    if (j0 >= j1 || c.sm->abort) return;  // uniform over the CTA
+    const int h0 = j0 / HD, nh = (j1 - 1) / HD - h0 + 1;
+    const uint64_t* rec0 = p.part + (size_t)(b * p.Hkv + g) * p.C * RS;
+    float2* mls = reinterpret_cast<float2*>(c.scratch);     // [nsplit][nh] (m, l)
+    float* fw = c.scratch + 2 * kMaxSplitsG;                // [nsplit][nh] weights
+    float* Ls = fw + kMaxSplitsG;                           // [nh]
     consumer_sync();
-    if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_PART, (uint32_t)nsplit);
-    if (c.tid == 0) {
-        int last = 0;
-        if (!c.sm->abort) {
-            uint32_t* ctr = p.arrivals + ((size_t)l * p.maxB * p.Hkv + bg) * kCounterStride;
-            const uint32_t old = atom_acq_rel_add(ctr, 1u);
-            if (old == (uint32_t)(nsplit - 1)) { last = 1; st_relaxed(ctr, 0u); }
+    // 1) (m, l) of every split for the heads of the slice
+    for (int i = c.tid; i < nsplit * nh; i += kConsumerThreads) {
+        const int si = i / nh, hh = i % nh;
+        uint64_t w0, w1;
+        Spin sp;
+        for (;;) {
+            ll_ld2(rec0 + (size_t)si * RS + GHD + 2 * (h0 + hh), w0, w1);
+            if ((ll_tag(w0) == tp && ll_tag(w1) == tp) || !sp.again(a, c.sm, task)) break;
         }
-        c.sm->bcast = last;
+        mls[i] = make_float2(ll_val(w0), ll_val(w1));
     }
     consumer_sync();
-    if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_ARRIVED, (uint32_t)c.sm->bcast);
-    if (c.sm->bcast) {
-        // 1) all (m, l) of the nsplit partials into shared memory in one parallel pass
-        const size_t base0 = (size_t)bg * p.C * G;
-        float2* mls = reinterpret_cast<float2*>(c.scratch);     // [nsplit][G]
-        float* fw = c.scratch + 2 * kMaxSplitsG;                // [nsplit][G] weights
-        float* Ls = fw + kMaxSplitsG;                           // [G]
-        for (int i = c.tid; i < nsplit * G; i += kConsumerThreads) mls[i] = __ldcg(&p.part_ml[base0 + i]);
-        consumer_sync();
-        if (l == 1) MK_TRACE_C(c, TR_M_ML, 0);
-        // 2) per head (one warp each): M = max m_s, w_s = exp(m_s - M), L = sum w_s l_s
-        if (c.cw < G) {
-            const int hl = c.cw;
-            float M = -INFINITY;
-            for (int i = c.lane; i < nsplit; i += 32) M = fmaxf(M, mls[i * G + hl].x);
+    if (l == 1) MK_TRACE_C(c, TR_M_ML, 0);
+    // 2) per head (one warp each): M, the weights w_s and L
+    if (c.cw < nh) {
+        const int hh = c.cw;
+        float M = -INFINITY;
+        for (int i = c.lane; i < nsplit; i += 32) M = fmaxf(M, mls[i * nh + hh].x);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            float L = 0.f;
-            for (int i = c.lane; i < nsplit; i += 32) {
-                const float2 ml = mls[i * G + hl];
-                const float f = expf(ml.x - M);
-                fw[i * G + hl] = f;
-                L += f * ml.y;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-            if (c.lane == 0) Ls[hl] = L;
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.f;
+        for (int i = c.lane; i < nsplit; i += 32) {
+            const float2 ml = mls[i * nh + hh];
+            const float f = ml.x == -INFINITY ? 0.f : expf(ml.x - M);
+            fw[i * nh + hh] = f;
+            L += f * ml.y;
         }
-        consumer_sync();
-        if (l == 1) MK_TRACE_C(c, TR_M_W, 0);
-        // 3) O = sum_s w_s o_s / L: threads own 4 consecutive dims of one head; the splits
-        //    are dealt to kRep threads per quad and combined with shuffles
-        constexpr int kQuads = 8 * HD / 4;  // upper bound of G * HD / 4
-        const int nquad = G * HD / 4;
-        const int rep = kConsumerThreads / nquad >= 4 ? 4 : kConsumerThreads / nquad >= 2 ? 2 : 1;
-        (void)kQuads;
-        const int quad = c.tid / rep, sub = c.tid % rep;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        int hl = 0, d = 0;
-        if (quad < nquad) {
-            hl = (quad * 4) / HD;
-            d = (quad * 4) % HD;
-            const float4* po = reinterpret_cast<const float4*>(p.part_o + (base0 + hl) * HD + d);
-            const size_t stride4 = (size_t)G * HD / 4;
-            // 8 independent loads in flight per round
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (c.lane == 0) Ls[hh] = L;
+    }
+    consumer_sync();
+    if (l == 1) MK_TRACE_C(c, TR_M_W, 0);
+    // 3) the slice of O: `rep` consecutive lanes per output dim share the splits
+    //    round-robin (8 tagged reads in flight each) and combine them with shuffles
+    const int len = j1 - j0;
+    int rep = 32;
+    while (rep > 1 && rep * len > kConsumerThreads) rep >>= 1;
+    const uint32_t tattn = tag_of(a, l, TAG_ATTN);
+    const bool pub = a.skip_publish != task;
+    for (int jb = 0; jb < len; jb += kConsumerThreads / rep) {
+        const int jj = jb + c.tid / rep, sub = c.tid % rep;
+        float acc = 0.f;
+        int hh = 0;
+        if (jj < len) {
+            const int j = j0 + jj;
+            hh = j / HD - h0;
             for (int s0 = sub; s0 < nsplit; s0 += 8 * rep) {
-                float4 v[8];
+                uint64_t w[8];
+                Spin sp;
+                for (;;) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int si = s0 + j * rep;
-                    v[j] = si < nsplit ? __ldcg(po + (size_t)si * stride4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = 0; k < 8; ++k) {
+                        const int si = s0 + k * rep;
+                        w[k] = si < nsplit ? ll_ld(rec0 + (size_t)si * RS + j) : (uint64_t)tp << 32;
+                    }
+                    bool ok = true;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) ok = ok && ll_tag(w[k]) == tp;
+                    if (ok || !sp.again(a, c.sm, task)) break;
                 }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int si = s0 + j * rep;
-                    const float f = si < nsplit ? fw[si * G + hl] : 0.f;
-                    o.x += f * v[j].x; o.y += f * v[j].y; o.z += f * v[j].z; o.w += f * v[j].w;
+                for (int k = 0; k < 8; ++k) {
+                    const int si = s0 + k * rep;
+                    if (si < nsplit) acc += fw[si * nh + hh] * ll_val(w[k]);
                 }
             }
         }
-        for (int off = 1; off < rep; off <<= 1) {
-            o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
-            o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
-            o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
-            o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
+        for (int off = 1; off < rep; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (jj < len && sub == 0) {
+            const size_t o = (size_t)b * p.Hq * HD + perm_col(g * G * HD + j0 + jj);
+            if (!tagged(a)) p.attnf[o] = acc / Ls[hh];
+            else if (pub) ll_st(p.attn + o, acc / Ls[hh], tattn);
         }
-        if (quad < nquad && sub == 0) {
-            const float inv = 1.0f / Ls[hl];
-            float* dst = p.attn + (size_t)b * p.Hq * HD;
-            const int k = (g * G + hl) * HD + d;
-            dst[perm_col(k)] = o.x * inv;
-            dst[perm_col(k + 1)] = o.y * inv;
-            dst[perm_col(k + 2)] = o.z * inv;
-            dst[perm_col(k + 3)] = o.w * inv;
-        }
-        consumer_sync();
-        if (c.tid == 0 && !c.sm->abort && a.skip_publish != task)
-            red_release_add(p.counters + cnt_stage(l, ST_ATTN) * kCounterStride, 1u);
-        if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_MERGED, 0);
     }
+    consumer_sync();  // the scratch is free again
+    if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_MERGED, 0);
     c_in.tn = c.tn;
 }
 
@@ -1223,19 +1373,46 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
     float* vs = ks + HD;                           // [HD]
     float2* rs = reinterpret_cast<float2*>(vs + HD);  // [HD / 2]
     if (!c.sm->abort) {
-        const float* qrow = p.qkv + (size_t)b * p.qkv_rows + (size_t)g * G * HD;
-        for (int i = c.tid; i < G * HD / 4; i += kConsumerThreads) {
-            const int h = (4 * i) / HD, d = (4 * i) % HD;
-            *reinterpret_cast<float4*>(qs + h * QS + d) = __ldcg(reinterpret_cast<const float4*>(qrow) + i);
-        }
         for (int i = c.tid; i < HD / 2; i += kConsumerThreads) rs[i] = __ldg(rope + i);
-        if (has_last) {
-            const float* kp = p.qkv + (size_t)b * p.qkv_rows + (size_t)(p.Hq + g) * HD;
-            const float* vp = p.qkv + (size_t)b * p.qkv_rows + (size_t)(p.Hq + p.Hkv + g) * HD;
-            for (int i = c.tid; i < HD / 4; i += kConsumerThreads) {
-                reinterpret_cast<float4*>(ks)[i] = __ldcg(reinterpret_cast<const float4*>(kp) + i);
-                reinterpret_cast<float4*>(vs)[i] = __ldcg(reinterpret_cast<const float4*>(vp) + i);
+        // q of the G heads, then (appending piece) k and v: pairs of tagged words, all of
+        // a thread's pairs in flight at once, polled until they carry the QKV tag
+        const uint64_t* row = p.qkv + (size_t)b * p.qkv_rows;
+        const uint32_t tq = tag_of(a, l, TAG_QKV);
+        const int nq = G * HD / 2, nt = nq + (has_last ? HD : 0);
+        constexpr int kPairs = (8 * HD / 2 + HD + kConsumerThreads - 1) / kConsumerThreads;
+        auto src_of = [&](int i) -> const uint64_t* {
+            if (i < nq) return row + (size_t)g * G * HD + 2 * i;
+            const int j = i - nq;
+            return j < HD / 2 ? row + (size_t)(p.Hq + g) * HD + 2 * j
+                              : row + (size_t)(p.Hq + p.Hkv + g) * HD + 2 * (j - HD / 2);
+        };
+        uint64_t w[kPairs][2];
+        Spin sp;
+        for (;;) {
+#pragma unroll
+            for (int k = 0; k < kPairs; ++k) {
+                const int i = c.tid + k * kConsumerThreads;
+                w[k][0] = w[k][1] = (uint64_t)tq << 32;
+                if (i < nt) ll_ld2(src_of(i), w[k][0], w[k][1]);
             }
+            bool ok = true;
+#pragma unroll
+            for (int k = 0; k < kPairs; ++k) ok = ok && ll_tag(w[k][0]) == tq && ll_tag(w[k][1]) == tq;
+            if (ok || !sp.again(a, c.sm, task)) break;
+        }
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) {
+            const int i = c.tid + k * kConsumerThreads;
+            if (i >= nt) continue;
+            const float2 v = make_float2(ll_val(w[k][0]), ll_val(w[k][1]));
+            float* dst;
+            if (i < nq) {
+                dst = qs + ((2 * i) / HD) * QS + (2 * i) % HD;
+            } else {
+                const int j = i - nq;
+                dst = j < HD / 2 ? ks + 2 * j : vs + 2 * (j - HD / 2);
+            }
+            *reinterpret_cast<float2*>(dst) = v;
         }
     }
     if (l == 1) MK_TRACE_C(c, TR_Q_LOADED, 0);
@@ -1436,24 +1613,25 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
     }
     c_in.seq = c.seq;
     c_in.tn = c.tn;
-    attention_finish<HD>(c_in, l, b, g, split, nsplit);
+    attention_finish<HD>(c_in, l, b, g, split);
 }
 
 template <int HD>
 __device__ void attention_stage(Ctx& c, int l, int cta) {
-    bool waited = false;
+    MK_TRACE_C(c, TR_WAIT, l * 16 + ST_ATTN);
+    // every piece first writes its partial record; then each split merges its slice
     for_each_piece(*c.a, c.sm, l, cta, [&](int b, int g, const SeqSpan& sp, int u, int n,
                                           int split, int nsplit) {
-        if (!waited) {
-            MK_TRACE_C(c, TR_WAIT, l * 16 + ST_ATTN);
-            consumer_wait(c, cnt_stage(l, ST_QKV), c.a->stage_target, l * 16 + ST_ATTN);
-            MK_TRACE_C(c, TR_READY, l * 16 + ST_ATTN);
-            waited = true;
-        }
         MK_TRACE_C(c, TR_PIECE, (uint32_t)(b * 256 + g));
         attention_piece<HD>(c, l, b, g, sp, u, n, split, nsplit);
+    });
+    for_each_piece(*c.a, c.sm, l, cta, [&](int b, int g, const SeqSpan&, int, int, int split,
+                                          int nsplit) {
+        attention_merge<HD>(c, l, b, g, split, nsplit);
         MK_TRACE_C(c, TR_MERGE, (uint32_t)(b * 256 + g));
     });
+    // larger batches: every CTA counts its (possibly empty) share of the merges
+    if (!tagged(*c.a)) publish(c, cnt_stage(l, ST_ATTN), l * 16 + ST_ATTN);
 }
 
 // x[b] = E[token b]. Each CTA writes the residual rows it owns (the same rows its O and
@@ -1469,10 +1647,12 @@ __device__ void embed_stage(Ctx& c, int cta) {
             const int b = e / nr, k = a0 + e % nr;
             const int tok = __ldg(a.tokens + b);
             const float v = __bfloat162float(p.embed[(size_t)tok * p.d + k]);
-            p.x[(size_t)b * p.d + perm_col(k)] = v;
+            const size_t o = (size_t)b * p.d + perm_col(k);
+            if (!tagged(a)) p.xf[o] = v;
+            else if (a.skip_publish != -2) ll_st(p.x + o, v, tag_of(a, 0, TAG_EMBED));
             c.sm->xown[b][k - a0] = v;
         }
-    publish(c, cnt_embed(), -2);
+    if (!tagged(a)) publish(c, cnt_embed(), -2);
 }
 
 __device__ void argmax_finish(Ctx& c, int cta) {
@@ -1516,15 +1696,25 @@ template <int HD>
 __device__ void consumer_run(Ctx& c, int cta) {
     const Plan& p = c.a->p;
     if (c.sm->abort) return;  // step inputs rejected (uniform: set before the first barrier)
+    constexpr int kPlanWords = (int)(sizeof(LayerPlan) / 8);
+    auto fetch_plan = [&](int l) {  // layer l's plan into shared memory (slot l & 1)
+        if (c.tid < kPlanWords)
+            reinterpret_cast<uint64_t*>(&c.sm->lp[l & 1])[c.tid] =
+                __ldg(reinterpret_cast<const uint64_t*>(p.layers + l) + c.tid);
+    };
+    fetch_plan(0);
     embed_stage(c, cta);
     for (int l = 0; l < p.L; ++l) {
-        gemv_stage(c, make_gemv(*c.a, G_QKV, l), cta);
+        consumer_sync();  // layer l's plan is in place; slot (l + 1) & 1 is free
+        const LayerPlan& lp = c.sm->lp[l & 1];
+        gemv_stage(c, make_gemv(*c.a, G_QKV, l, lp), cta);
+        if (l + 1 < p.L) fetch_plan(l + 1);  // read at the next layer, after a barrier
         attention_stage<HD>(c, l, cta);
-        gemv_stage(c, make_gemv(*c.a, G_O, l), cta);
-        gemv_stage(c, make_gemv(*c.a, G_GU, l), cta);
-        gemv_stage(c, make_gemv(*c.a, G_DOWN, l), cta);
+        gemv_stage(c, make_gemv(*c.a, G_O, l, lp), cta);
+        gemv_stage(c, make_gemv(*c.a, G_GU, l, lp), cta);
+        gemv_stage(c, make_gemv(*c.a, G_DOWN, l, lp), cta);
     }
-    gemv_stage(c, make_gemv(*c.a, G_LM, 0), cta);
+    gemv_stage(c, make_gemv(*c.a, G_LM, 0, c.sm->lp[0]), cta);
     argmax_finish(c, cta);
     MK_TRACE_C(c, TR_END, 0);
 }
@@ -1542,6 +1732,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         sm->abort = 0;
+        sm->lseq = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm->full[s]), 1);
             mbar_init(smem_u32(&sm->empty[s]), kConsumerWarps);
@@ -1566,13 +1757,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     }
     __syncthreads();
 
-    if (warp == 0) {
+    if (warp == 0 || warp == kConsumerWarps + 1) {
         Producer pr;
         pr.a = &a;
         pr.sm = sm;
         pr.ring_s = smem_u32(ring);
         pr.lane = lane;
-        pr.run<HD>(cta);
+        pr.pf = warp != 0;
+        if (!pr.pf || a.prefetch_slots > 0) pr.run<HD>(cta);
         return;
     }
     Ctx c;

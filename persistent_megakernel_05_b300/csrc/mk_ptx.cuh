@@ -74,6 +74,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
         ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
 }
+// L2 prefetch of a contiguous global range: no shared memory written, no completion
+// to wait for (16-byte aligned address, size a multiple of 16)
+__device__ __forceinline__ void l2_prefetch_1d(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// L2 prefetch of one tensor-map box
+__device__ __forceinline__ void l2_prefetch_2d(const void* tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(tmap), "r"(x), "r"(y) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -104,6 +114,33 @@ __device__ __forceinline__ int ld_volatile_int(const int* p) {
     asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+// ---------------------------------------------------------------- tagged words
+// A 64-bit word holding an fp32 value (low half) and the tag of the write that made it
+// (high half). An aligned 64-bit access is single-copy atomic, so a reader that sees
+// the tag it expects also sees that write's value: the word publishes itself, with no
+// fence and no separate counter between writer and reader.
+__device__ __forceinline__ uint64_t ll_word(float v, uint32_t tag) {
+    return ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+}
+__device__ __forceinline__ void ll_st(uint64_t* p, float v, uint32_t tag) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(ll_word(v, tag)) : "memory");
+}
+__device__ __forceinline__ void ll_st2(uint64_t* p, float v0, float v1, uint32_t tag) {
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};"
+                 ::"l"(p), "l"(ll_word(v0, tag)), "l"(ll_word(v1, tag)) : "memory");
+}
+// two consecutive words (16-byte aligned)
+__device__ __forceinline__ void ll_ld2(const uint64_t* p, uint64_t& w0, uint64_t& w1) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p));
+}
+__device__ __forceinline__ uint64_t ll_ld(const uint64_t* p) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p));
+    return w;
+}
+__device__ __forceinline__ float ll_val(uint64_t w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ uint32_t ll_tag(uint64_t w) { return (uint32_t)(w >> 32); }
+
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
