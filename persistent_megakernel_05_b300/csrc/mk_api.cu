@@ -70,6 +70,8 @@ mk_status validate_desc(const mk_model_desc* d) {
     if (G > 8 || G * d->head_dim > 512) return MK_ERR_INVALID_ARG;
     if ((d->n_q_heads * d->head_dim) % 64) return MK_ERR_INVALID_ARG;
     if (d->vocab < 1) return MK_ERR_INVALID_ARG;
+    // GEMV rows are split over CTAs in 32-bit arithmetic (rows * CTAs < 2^32, CTAs <= 1024)
+    if (d->vocab > (1 << 22) || d->ffn_dim > (1 << 22) || d->d_model > (1 << 22)) return MK_ERR_INVALID_ARG;
     if (d->n_experts != 0) return MK_ERR_INVALID_ARG;  // MoE stages: not in this build yet
     if (d->ffn_dim < 64 || d->ffn_dim % 64) return MK_ERR_INVALID_ARG;
     if (!(d->rms_eps > 0.f) || !(d->rope_theta > 0.f)) return MK_ERR_INVALID_ARG;
@@ -393,6 +395,9 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
     if (!h || !tokens || !positions || !page_table || !seq_lens || !next_tokens)
         return MK_ERR_INVALID_ARG;
     if (batch < 1 || batch > h->desc.max_batch || max_pages_per_seq < 1) return MK_ERR_INVALID_ARG;
+    // the kernel partitions attention units in 32-bit arithmetic
+    if ((uint64_t)batch * h->desc.n_kv_heads * max_pages_per_seq * h->num_ctas >= (1ull << 31))
+        return MK_ERR_INVALID_ARG;
     if (!h->kv) return MK_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     mk::StepArgs a;
@@ -628,6 +633,8 @@ extern "C" mk_status mk_decode_step_noalloc(
         !next_tokens || !status_out || max_pages_per_seq < 1)
         return MK_ERR_INVALID_ARG;
     if (batch < 1 || batch > desc->max_batch) return MK_ERR_INVALID_ARG;
+    if ((uint64_t)batch * desc->n_kv_heads * max_pages_per_seq * 1024u >= (1ull << 31))
+        return MK_ERR_INVALID_ARG;  // 32-bit attention-unit arithmetic (any CTA count <= 1024)
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -776,6 +783,17 @@ extern "C" mk_status mk_decode_step_noalloc(
     return MK_OK;
 }
 
+#ifdef MK_PROF
+// Profile builds only: the per-CTA section cycle sums, and clearing them.
+extern "C" __attribute__((visibility("default"))) int mk_prof_read(void* dst, size_t bytes) {
+    if (bytes > sizeof(mk::g_mk_prof)) bytes = sizeof(mk::g_mk_prof);
+    return (int)cudaMemcpyFromSymbol(dst, mk::g_mk_prof, bytes);
+}
+extern "C" __attribute__((visibility("default"))) int mk_prof_clear() {
+    static unsigned long long zero[mk::kProfCtas][mk::kProfSections];
+    return (int)cudaMemcpyToSymbol(mk::g_mk_prof, zero, sizeof(zero));
+}
+#endif
 #ifdef MK_TRACE
 // Trace builds only: copy the per-CTA timeline of the last step to host memory.
 extern "C" __attribute__((visibility("default"))) int mk_trace_read(void* dst, size_t bytes) {

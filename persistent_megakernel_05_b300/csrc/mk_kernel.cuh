@@ -62,6 +62,28 @@ __device__ __forceinline__ void trace_event(int cta, int& n, int base, uint32_t 
 #define MK_TRACE_C(c, code, arg) do { } while (0)
 #define MK_TRACE_P(pr, code, arg) do { } while (0)
 #endif
+// ---- optional section profile (compile with -DMK_PROF; no code otherwise) ----
+// Consumer thread 0 of every CTA adds the SM cycles since its previous mark to the
+// section named by each mark: a cheap (clock64, no memory traffic) breakdown of where a
+// step's time goes, summed over steps until cleared.
+#ifdef MK_PROF
+constexpr int kProfCtas = 160, kProfSections = 64;
+__device__ unsigned long long g_mk_prof[kProfCtas][kProfSections];
+// sums accumulate in shared memory (no global round trip inside a section) and are
+// flushed to g_mk_prof once at the end of the step
+#define MK_PROF_MARK(c, sec) do { if ((c).tid == 0) { \
+    const long long t_ = clock64(); (c).sm->prof[sec] += t_ - (c).pt; (c).pt = t_; } } while (0)
+#define MK_PROF_BACK(dst, src) ((dst).pt = (src).pt)
+#else
+#define MK_PROF_MARK(c, sec) do { } while (0)
+#define MK_PROF_BACK(dst, src) do { } while (0)
+#endif
+// profile sections: GEMV kind k (QKV, O, GU, DOWN, LM) uses 1 + 4k .. 4 + 4k
+enum ProfSection { PS_OTHER = 0, PS_G_DATA = 1, PS_G_SLOTS = 2, PS_G_EPI = 3, PS_G_END = 4,
+                   PS_A_ENTRY = 21, PS_A_QPOLL = 22, PS_A_QSYNC = 23, PS_A_FRAG = 24, PS_A_LOOP = 25,
+                   PS_A_POST = 26, PS_A_FINISH = 27, PS_M_ML = 28, PS_M_W = 29, PS_M_O = 30,
+                   PS_A_END = 31, PS_EMBED = 32, PS_ARGMAX = 33, PS_TOTAL = 63 };
+
 enum TraceCode { TR_WAIT = 1, TR_READY = 2, TR_DONE = 3, TR_PIECE = 4, TR_MERGE = 5, TR_END = 6,
                  TR_P_STAGE = 11, TR_P_BLOCK = 12, TR_P_GO = 13,
                  TR_S_WAIT = 20, TR_S_FULL = 21, TR_S_REL = 22, TR_S_ISSUE = 23,
@@ -164,7 +186,10 @@ struct Smem {
     int bcast;
     volatile uint32_t lseq;  // ring slots the loader has started filling
     int pad_[5];
-    LayerPlan lp[2];         // consumers' copies of the plans of layers l (l & 1) and l + 1
+    __align__(16) LayerPlan lp[2];  // consumers' copies of the plans of layers l (l & 1) and l + 1
+#ifdef MK_PROF
+    unsigned long long prof[64];
+#endif
     uint64_t full[kStages];
     uint64_t empty[kStages];
     __align__(16) bf16 knew[128];
@@ -182,6 +207,9 @@ struct Ctx {
     uint32_t seq;        // ring sequence number (slot = seq % kStages)
     int cw, lane, tid;   // consumer warp (0..7), lane, consumer thread id (0..255)
     int tn;              // trace events recorded (MK_TRACE builds)
+#ifdef MK_PROF
+    long long pt;        // cycle count at the last profile mark (MK_PROF builds)
+#endif
 };
 
 // ------------------------------------------------------------------ errors / waits
@@ -252,6 +280,20 @@ struct Spin {
     }
 };
 
+// Spin on ONE pair of tagged words until both carry `tag` (false when the wait ends).
+// A thread that needs several words and found one missing waits here on that word, so
+// that a stalled hand-off costs one read per round instead of one per word; then it
+// re-reads the whole set.
+__device__ __forceinline__ bool ll_wait_pair(const uint64_t* p, uint32_t tag, Spin& sp, const StepArgs& a,
+                                             Smem* sm, int task) {
+    for (;;) {
+        if (!sp.again(a, sm, task)) return false;
+        uint64_t w0, w1;
+        ll_ld2(p, w0, w1);
+        if (ll_tag(w0) == tag && ll_tag(w1) == tag) return true;
+    }
+}
+
 // Slow path of every ring wait (one lane): sleep on the barrier phase until it completes
 // (true), the CTA aborts, another CTA latches an error, or `limit_ns` passes, which
 // latches kErrTimeout for `task` (false). Out of line: it is cold code.
@@ -294,8 +336,9 @@ __device__ __forceinline__ void release_slot(Ctx& c) {
 
 // ------------------------------------------------------------------ schedule
 __device__ __forceinline__ void cta_rows(int R, int cta, int C, int& r0, int& r1) {
-    r0 = (int)((long long)cta * R / C);
-    r1 = (int)((long long)(cta + 1) * R / C);
+    // 32-bit unsigned products: R * C < 2^32 for every stage (checked on the host)
+    r0 = (int)((uint32_t)cta * (uint32_t)R / (uint32_t)C);
+    r1 = (int)((uint32_t)(cta + 1) * (uint32_t)R / (uint32_t)C);
 }
 
 struct GemvStage {
@@ -441,22 +484,23 @@ __device__ __forceinline__ SeqSpan seq_span(const Plan& p, const Smem* sm, int l
 template <typename F>
 __device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta, F&& f) {
     const Plan& p = a.p;
-    long long U = 0;
-    for (int b = 0; b < a.B; ++b) U += (long long)p.Hkv * seq_span(p, sm, l, b).np;
-    const int C = p.C;
-    long long u0, u1;
-    if (U >= C) { u0 = (long long)cta * U / C; u1 = (long long)(cta + 1) * U / C; }
-    else { u0 = cta; u1 = cta < U ? cta + 1 : cta; }
+    // 32-bit unsigned unit arithmetic: U * C < 2^31 (checked on the host)
+    uint32_t U = 0;
+    for (int b = 0; b < a.B; ++b) U += (uint32_t)(p.Hkv * seq_span(p, sm, l, b).np);
+    const uint32_t C = (uint32_t)p.C;
+    uint32_t u0, u1;
+    if (U >= C) { u0 = (uint32_t)cta * U / C; u1 = (uint32_t)(cta + 1) * U / C; }
+    else { u0 = cta; u1 = (uint32_t)cta < U ? cta + 1 : cta; }
     if (u0 >= u1) return;
-    auto first_cta = [&](long long s) -> int {
+    auto first_cta = [&](uint32_t s) -> int {
         return U >= C ? (int)(((s + 1) * C - 1) / U) : (int)s;
     };
-    long long s = 0;
+    uint32_t s = 0;
     for (int b = 0; b < a.B; ++b) {
         const SeqSpan sp = seq_span(p, sm, l, b);
         for (int g = 0; g < p.Hkv; ++g) {
-            const long long e = s + sp.np;
-            const long long lo = max(s, u0), hi = min(e, u1);
+            const uint32_t e = s + (uint32_t)sp.np;
+            const uint32_t lo = max(s, u0), hi = min(e, u1);
             if (lo < hi) {
                 const int c0 = first_cta(s);
                 const int nsplit = first_cta(e - 1) - c0 + 1;
@@ -484,6 +528,8 @@ struct Producer {
     // on a dependency and the loader on a full ring. It never blocks anyone and never
     // reports errors: when anything goes wrong it simply stops.
     bool pf = false;
+    // page-table batch cache: ids of logical pages [pt_lp0, pt_lp0 + 32) of sequence pt_b
+    int pt_b = -1, pt_lp0 = 0, pt_ids = -1;
 
     __device__ bool acquire_slot(int task) {
         if (pf) {
@@ -581,15 +627,21 @@ struct Producer {
             const int* pt = a->page_table + (size_t)b * a->max_pages;
             for (int st = 0; st < n; st += PPS) {
                 const int np = min(PPS, n - st);
+                // page ids travel in batches of 32 (lane i holds logical page lp0 + i), kept
+                // across pieces and layers: one page-table read serves every layer that
+                // walks the same pages
+                const int want = sp.p0 + u + st;
+                if (b != pt_b || want < pt_lp0 || want + np > pt_lp0 + 32) {
+                    pt_b = b;
+                    pt_lp0 = want;
+                    pt_ids = want + lane < a->max_pages ? __ldg(pt + want + lane) : -1;
+                }
                 if (!acquire_slot(l * 16 + ST_ATTN)) { ok = false; return; }
                 const int nbox = np * 2 * NB;  // <= 16
                 const int i = lane / (2 * NB), kv = (lane / NB) & 1, bx = lane % NB;
-                int page = 0;
+                const int page = __shfl_sync(0xffffffffu, pt_ids, (want - pt_lp0 + i) & 31);
                 bool bad = false;
-                if (lane < nbox) {
-                    page = __ldg(pt + sp.p0 + u + st + i);
-                    bad = page < 0 || page >= p.num_pages;
-                }
+                if (lane < nbox) bad = page < 0 || page >= p.num_pages;
                 if (__any_sync(0xffffffffu, bad)) {
                     if (lane == 0 && !pf) set_error(p, sm, kErrBadPage, l * 16 + ST_ATTN);
                     ok = false;
@@ -794,7 +846,16 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
         if (!c.sm->abort) {  // poll until every word carries the awaited tag
             Spin sp;
             while (!tags_ok(wn)) {
-                if (!sp.again(a, c.sm, s.task_id)) break;
+                const int col = k0 + 8 * piece;
+                const int base = (col & ~63) + 2 * ((col >> 3) & 7);
+                int miss = 0;  // first pair (b * 4 + t) that is not there yet
+#pragma unroll
+                for (int q = 4 * BP - 1; q >= 0; --q)
+                    if (ll_tag(wn[q >> 2][2 * (q & 3)]) != s.src_tag || ll_tag(wn[q >> 2][2 * (q & 3) + 1]) != s.src_tag)
+                        miss = q;
+                if (!ll_wait_pair(s.src + (size_t)(miss >> 2) * s.K + base + 16 * (miss & 3), s.src_tag, sp, a,
+                                  c.sm, s.task_id))
+                    break;
                 issue(k0, wn);
             }
         }
@@ -843,6 +904,7 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
             }
         }
         if (trace_slots(s)) MK_TRACE_C(c, TR_G_X, 0);
+        if (k0 == 0) MK_PROF_MARK(c, PS_G_DATA + 4 * s.kind);
         uint32_t roff[8];  // byte offset of row r (this lane's piece) inside a slot
 #pragma unroll
         for (int r = 0; r < 8; ++r) roff[r] = (uint32_t)(geo.row_off(r) + 16 * piece);
@@ -895,6 +957,7 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
             if (gb + j < ng) red[(c.cw * kTaskRows + (gb + j) * kGroupRows + r) * BP + b] += v;
         }
     }
+    MK_PROF_MARK(c, PS_G_SLOTS + 4 * s.kind);
     consumer_sync();
     if (trace_slots(s)) MK_TRACE_C(c, TR_G_SUM, 0);
     if (yout)
@@ -996,6 +1059,7 @@ __device__ __forceinline__ void gemv_mma(Ctx& c, const GemvStage& s, int r0, int
                 }
             }
         }
+        if (k0 == 0) MK_PROF_MARK(c, PS_G_DATA + 4 * s.kind);
 #pragma unroll
         for (int ti = 0; ti < 8; ++ti) {
             if (ti < nt) {
@@ -1035,6 +1099,7 @@ __device__ __forceinline__ void gemv_mma(Ctx& c, const GemvStage& s, int r0, int
             }
         }
     }
+    MK_PROF_MARK(c, PS_G_SLOTS + 4 * s.kind);
     // cross-warp reduction: red[w][tile][16 rows][8 cols] in rounds of 4 tiles
     float* red = c.scratch;
 #pragma unroll
@@ -1156,9 +1221,11 @@ __device__ __noinline__ void gemv_task_fma(Ctx& c_in, int kind, int layer, int r
         consumer_sync();
         if (!c.sm->abort) yout_epilogue(c, s, r0, r1, yout);
     }
+    MK_PROF_MARK(c, PS_G_EPI + 4 * s.kind);
     if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
     c_in.seq = c.seq;
     c_in.tn = c.tn;
+    MK_PROF_BACK(c_in, c);
 }
 __device__ __noinline__ void gemv_task_mma(Ctx& c_in, int kind, int layer, int r0, int r1) {
     Ctx c = c_in;
@@ -1168,9 +1235,11 @@ __device__ __noinline__ void gemv_task_mma(Ctx& c_in, int kind, int layer, int r
     gemv_mma(c, s, r0, r1, yout);
     consumer_sync();
     if (!c.sm->abort) yout_epilogue(c, s, r0, r1, yout);
+    MK_PROF_MARK(c, PS_G_EPI + 4 * s.kind);
     if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
     c_in.seq = c.seq;
     c_in.tn = c.tn;
+    MK_PROF_BACK(c_in, c);
 }
 __device__ __forceinline__ void gemv_task(Ctx& c, int kind, int layer, int r0, int r1) {
     const int B = c.a->B;
@@ -1185,6 +1254,7 @@ __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
     int a0, a1;
     cta_rows(s.R, cta, p.C, a0, a1);
     const bool tg = tagged(*c.a);
+    MK_PROF_MARK(c, PS_OTHER);
     if (a0 < a1) {
         MK_TRACE_C(c, TR_WAIT, s.task_id);
         if (!tg) consumer_wait(c, s.cnt_wait, s.task_id);
@@ -1195,6 +1265,7 @@ __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
     }
     if (!tg && s.cnt_pub >= 0) publish(c, s.cnt_pub, s.task_id);
     else consumer_sync();  // every warp is done with the shared scratch of this stage
+    MK_PROF_MARK(c, PS_G_END + 4 * s.kind);
     MK_TRACE_C(c, TR_DONE, s.task_id);
 }
 
@@ -1241,8 +1312,10 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
         }
     }
     consumer_sync();  // the scratch is free for the next piece
+    MK_PROF_MARK(c, PS_A_FINISH);
     if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_PART, (uint32_t)split);
     c_in.tn = c.tn;
+    MK_PROF_BACK(c_in, c);
 }
 
 // The split-`split` CTA of a (sequence, kv head) merges output dims [j0, j1) of the
@@ -1258,7 +1331,8 @@ __device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int
     const int G = p.G, GHD = G * HD, RS = GHD + 2 * G;
     const int task = l * 16 + ST_ATTN;
     const uint32_t tp = tag_of(a, l, TAG_PART);
-    const int j0 = (int)((long long)split * GHD / nsplit), j1 = (int)((long long)(split + 1) * GHD / nsplit);
+    const int j0 = (int)((uint32_t)split * GHD / (uint32_t)nsplit);
+    const int j1 = (int)((uint32_t)(split + 1) * GHD / (uint32_t)nsplit);
     if (j0 >= j1 || c.sm->abort) return;  // uniform over the CTA
     const int h0 = j0 / HD, nh = (j1 - 1) / HD - h0 + 1;
     const uint64_t* rec0 = p.part + (size_t)(b * p.Hkv + g) * p.C * RS;
@@ -1278,6 +1352,7 @@ __device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int
         mls[i] = make_float2(ll_val(w0), ll_val(w1));
     }
     consumer_sync();
+    MK_PROF_MARK(c, PS_M_ML);
     if (l == 1) MK_TRACE_C(c, TR_M_ML, 0);
     // 2) per head (one warp each): M, the weights w_s and L
     if (c.cw < nh) {
@@ -1298,6 +1373,7 @@ __device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int
         if (c.lane == 0) Ls[hh] = L;
     }
     consumer_sync();
+    MK_PROF_MARK(c, PS_M_W);
     if (l == 1) MK_TRACE_C(c, TR_M_W, 0);
     // 3) the slice of O: `rep` consecutive lanes per output dim share the splits
     //    round-robin (8 tagged reads in flight each) and combine them with shuffles
@@ -1322,10 +1398,17 @@ __device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int
                         const int si = s0 + k * rep;
                         w[k] = si < nsplit ? ll_ld(rec0 + (size_t)si * RS + j) : (uint64_t)tp << 32;
                     }
-                    bool ok = true;
+                    int miss = -1;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) ok = ok && ll_tag(w[k]) == tp;
-                    if (ok || !sp.again(a, c.sm, task)) break;
+                    for (int k = 7; k >= 0; --k)
+                        if (ll_tag(w[k]) != tp) miss = k;
+                    if (miss < 0) break;
+                    // wait on the missing word alone, then re-read the batch
+                    const uint64_t* pm = rec0 + (size_t)(s0 + miss * rep) * RS + j;
+                    bool got = false;
+                    while (sp.again(a, c.sm, task))
+                        if (ll_tag(ll_ld(pm)) == tp) { got = true; break; }
+                    if (!got) break;
                 }
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -1342,8 +1425,10 @@ __device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int
         }
     }
     consumer_sync();  // the scratch is free again
+    MK_PROF_MARK(c, PS_M_O);
     if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_MERGED, 0);
     c_in.tn = c.tn;
+    MK_PROF_BACK(c_in, c);
 }
 
 template <int HD>
@@ -1363,6 +1448,7 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
     const int pos = sp.pos, lo = sp.lo;
     const bool has_last = (sp.p0 + u + n - 1) == pos / kPage;
     const float2* rope = p.rope + (size_t)pos * (HD / 2);
+    MK_PROF_MARK(c, PS_A_ENTRY);
 
     // Stage q of the G heads (and the new token's k, v when this piece appends), plus
     // the RoPE row, through shared memory with coalesced loads: one L2 round trip. Rows
@@ -1395,10 +1481,11 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
                 w[k][0] = w[k][1] = (uint64_t)tq << 32;
                 if (i < nt) ll_ld2(src_of(i), w[k][0], w[k][1]);
             }
-            bool ok = true;
+            int miss = -1;
 #pragma unroll
-            for (int k = 0; k < kPairs; ++k) ok = ok && ll_tag(w[k][0]) == tq && ll_tag(w[k][1]) == tq;
-            if (ok || !sp.again(a, c.sm, task)) break;
+            for (int k = kPairs - 1; k >= 0; --k)
+                if (ll_tag(w[k][0]) != tq || ll_tag(w[k][1]) != tq) miss = k;
+            if (miss < 0 || !ll_wait_pair(src_of(c.tid + miss * kConsumerThreads), tq, sp, a, c.sm, task)) break;
         }
 #pragma unroll
         for (int k = 0; k < kPairs; ++k) {
@@ -1416,7 +1503,9 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
         }
     }
     if (l == 1) MK_TRACE_C(c, TR_Q_LOADED, 0);
+    MK_PROF_MARK(c, PS_A_QPOLL);
     consumer_sync();
+    MK_PROF_MARK(c, PS_A_QSYNC);
     if (l == 1) MK_TRACE_C(c, TR_Q_SYNCED, 0);
     // q^T (after RoPE) as the B operand: column gq = query head, k = head dims; hi/lo split.
     // b0b1 of k-step s holds dims 16s + 2t, +1; b2b3 holds 16s + 8 + 2t, +1.
@@ -1455,6 +1544,7 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
     }
     if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_Q, (uint32_t)bg_id(p, b, g));
     consumer_sync();  // the staging area becomes the per-warp P buffers below
+    MK_PROF_MARK(c, PS_A_FRAG);
 
     // Keys in the MMA M dimension: S^T = K q^T (16 keys x 8 head columns) and
     // O^T += V^T P^T (16 dims x 8 head columns), two MMAs (hi/lo) per 16x16 step.
@@ -1586,6 +1676,7 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
         if (l == 1) MK_TRACE_C(c, TR_S_REL, c.seq - 1);
     }
 
+    MK_PROF_MARK(c, PS_A_LOOP);
     if (l == 0) MK_TRACE_C(c, TR_A_LOOP, (uint32_t)n);
     // this warp's softmax state for heads 2t, 2t+1 -> shared memory (rows padded to HD + 8)
     constexpr int OS = HD + 8;
@@ -1611,13 +1702,16 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
             }
         }
     }
+    MK_PROF_MARK(c, PS_A_POST);
     c_in.seq = c.seq;
     c_in.tn = c.tn;
+    MK_PROF_BACK(c_in, c);
     attention_finish<HD>(c_in, l, b, g, split);
 }
 
 template <int HD>
 __device__ void attention_stage(Ctx& c, int l, int cta) {
+    MK_PROF_MARK(c, PS_OTHER);
     MK_TRACE_C(c, TR_WAIT, l * 16 + ST_ATTN);
     // every piece first writes its partial record; then each split merges its slice
     for_each_piece(*c.a, c.sm, l, cta, [&](int b, int g, const SeqSpan& sp, int u, int n,
@@ -1632,6 +1726,7 @@ __device__ void attention_stage(Ctx& c, int l, int cta) {
     });
     // larger batches: every CTA counts its (possibly empty) share of the merges
     if (!tagged(*c.a)) publish(c, cnt_stage(l, ST_ATTN), l * 16 + ST_ATTN);
+    MK_PROF_MARK(c, PS_A_END);
 }
 
 // x[b] = E[token b]. Each CTA writes the residual rows it owns (the same rows its O and
@@ -1696,15 +1791,26 @@ template <int HD>
 __device__ void consumer_run(Ctx& c, int cta) {
     const Plan& p = c.a->p;
     if (c.sm->abort) return;  // step inputs rejected (uniform: set before the first barrier)
-    constexpr int kPlanWords = (int)(sizeof(LayerPlan) / 8);
-    auto fetch_plan = [&](int l) {  // layer l's plan into shared memory (slot l & 1)
-        if (c.tid < kPlanWords)
-            reinterpret_cast<uint64_t*>(&c.sm->lp[l & 1])[c.tid] =
-                __ldg(reinterpret_cast<const uint64_t*>(p.layers + l) + c.tid);
+    static_assert(sizeof(LayerPlan) % 16 == 0, "layer plans copy in 16-byte pieces");
+    constexpr int kPlanChunks = (int)(sizeof(LayerPlan) / 16);
+    // layer l's plan into shared memory (slot l & 1) without stalling the issuing thread;
+    // it waits for its piece just before the barrier that precedes the first read
+    auto fetch_plan = [&](int l) {
+        if (c.tid < kPlanChunks)
+            cp_async_16(smem_u32(&c.sm->lp[l & 1]) + 16 * c.tid,
+                        reinterpret_cast<const uint8_t*>(p.layers + l) + 16 * c.tid);
     };
+#ifdef MK_PROF
+    if (c.tid < 64) c.sm->prof[c.tid] = 0;
+    consumer_sync();
+    const long long t_start = clock64();
+    c.pt = t_start;
+#endif
     fetch_plan(0);
     embed_stage(c, cta);
+    MK_PROF_MARK(c, PS_EMBED);
     for (int l = 0; l < p.L; ++l) {
+        if (c.tid < kPlanChunks) cp_async_wait_all();
         consumer_sync();  // layer l's plan is in place; slot (l + 1) & 1 is free
         const LayerPlan& lp = c.sm->lp[l & 1];
         gemv_stage(c, make_gemv(*c.a, G_QKV, l, lp), cta);
@@ -1716,6 +1822,12 @@ __device__ void consumer_run(Ctx& c, int cta) {
     }
     gemv_stage(c, make_gemv(*c.a, G_LM, 0, c.sm->lp[0]), cta);
     argmax_finish(c, cta);
+    MK_PROF_MARK(c, PS_ARGMAX);
+#ifdef MK_PROF
+    if (c.tid == 0) c.sm->prof[PS_TOTAL] += clock64() - t_start;
+    consumer_sync();
+    if (c.tid < 64 && cta < kProfCtas) g_mk_prof[cta][c.tid] += c.sm->prof[c.tid];
+#endif
     MK_TRACE_C(c, TR_END, 0);
 }
 
