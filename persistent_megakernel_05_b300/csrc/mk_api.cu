@@ -27,7 +27,7 @@ struct mk_handle {
     mk::LayerPlan* d_layers = nullptr;
     float* d_gains = nullptr;
     float2* d_rope = nullptr;
-    void* d_kvmap = nullptr;        // CUtensorMap (128 B, 64-B aligned)
+    CUtensorMap kv_tmap;            // KV pool tensor map, copied into every launch's parameters
     void* kv = nullptr;
     mk_kv_pool pool{};
     uint32_t epoch = 0;             // tag epoch of the last step (1 .. 2^20 - 1, cycling)
@@ -110,7 +110,6 @@ cudaError_t occupancy(int* blocks) {
 void free_handle(mk_handle* h) {
     if (!h) return;
     if (h->kv) cudaFree(h->kv);
-    if (h->d_kvmap) cudaFree(h->d_kvmap);
     if (h->block) cudaFree(h->block);
     if (h->d_layers) cudaFree(h->d_layers);
     if (h->d_gains) cudaFree(h->d_gains);
@@ -303,7 +302,6 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     p.arrivals = (uint32_t*)(base + o_arr);
     p.status = (int*)(base + o_status);
     p.kv = nullptr;
-    p.kv_map = nullptr;
     *out = h;
     return MK_OK;
 }
@@ -346,21 +344,9 @@ mk_status mk_kv_alloc(mk_handle* h, int32_t num_pages, mk_kv_pool* out) {
         h->kv = nullptr;
         return MK_ERR_INTERNAL;
     }
-    if (!h->d_kvmap && cudaMalloc(&h->d_kvmap, sizeof(CUtensorMap)) != cudaSuccess) {
-        cudaGetLastError();
-        cudaFree(h->kv);
-        h->kv = nullptr;
-        return MK_ERR_OOM;
-    }
-    if (cudaMemcpy(h->d_kvmap, &map, sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess) {
-        cudaGetLastError();
-        cudaFree(h->kv);
-        h->kv = nullptr;
-        return MK_ERR_INTERNAL;
-    }
+    h->kv_tmap = map;
     h->plan.kv = (bf16*)h->kv;
     h->plan.num_pages = num_pages;
-    h->plan.kv_map = h->d_kvmap;
     mk_kv_pool& P = h->pool;
     P.base = h->kv;
     P.num_pages = num_pages;
@@ -401,6 +387,7 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
     if (!h->kv) return MK_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     mk::StepArgs a;
+    a.kv_tmap = h->kv_tmap;
     a.p = h->plan;
     a.tokens = tokens;
     a.positions = positions;
@@ -532,7 +519,7 @@ void mk_destroy(mk_handle* h) {
 // ===========================================================================
 // mk_decode_step_noalloc: the same decode-step kernel, with every byte of its
 // scratch (plan tables, norm gains, RoPE table, activations, attention partials,
-// counters, status word, KV tensor map) carved out of one file-scope static device
+// counters, status word) carved out of one file-scope static device
 // array instead of memory from cudaMalloc. It exists for callers that must not
 // allocate device memory: code running where an allocation would synchronise the
 // device or is forbidden (allocator-free runtimes, memory-capped sandboxes, hosts
@@ -655,7 +642,6 @@ extern "C" mk_status mk_decode_step_noalloc(
     // carve the static array
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-    const size_t o_tmap = take(sizeof(CUtensorMap));
     const size_t o_layers = take(sizeof(mk::LayerPlan) * L);
     const size_t o_gains = take(sizeof(float) * (size_t)(2 * L + 1) * d);
     const size_t o_rope = take(sizeof(float2) * (size_t)desc->max_positions * (hd / 2));
@@ -677,7 +663,7 @@ extern "C" mk_status mk_decode_step_noalloc(
     if (off > kNoAllocScratchBytes) return MK_ERR_INVALID_ARG;  // model/batch too large
     unsigned char* base = D->base;
 
-    // KV tensor map, encoded on the host and copied into the array (no allocation)
+    // KV tensor map, encoded on the host; it travels in the kernel parameters
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void**)&encode, 12000,
@@ -696,10 +682,6 @@ extern "C" mk_status mk_decode_step_noalloc(
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return MK_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    if (cudaMemcpyAsync(base + o_tmap, &map, sizeof(map), cudaMemcpyHostToDevice, s) != cudaSuccess) {
-        cudaGetLastError();
-        return MK_ERR_INTERNAL;
-    }
 
     NoAllocSetup su;
     std::memset(&su, 0, sizeof(su));
@@ -753,7 +735,7 @@ extern "C" mk_status mk_decode_step_noalloc(
     p.arrivals = (uint32_t*)(base + o_arr);
     p.status = (int*)(base + o_status);
     p.kv = (bf16*)kv_pool;
-    p.kv_map = base + o_tmap;
+    a.kv_tmap = map;
     a.tokens = tokens;
     a.positions = positions;
     a.page_table = page_table;

@@ -3,21 +3,25 @@
 // Design (pages: "Cohere Megakernel", section "Megakernel ne demek"; "Kog Inference
 // Engine", sections on memory bandwidth and the monokernel):
 //   * one CTA per SM, launched cooperatively so every CTA is resident;
-//   * the step is a fixed list of stages per layer -- QKV tiles, attention key
-//     splits (+ last-arriver merge), O-projection tiles, gate/up tiles, down tiles --
-//     then LM-head tiles and the greedy argmax. Each stage's work is cut into row
-//     tiles (GEMV) or page ranges (attention) that are statically assigned to CTAs;
-//   * stages are ordered by per-stage dependency counters (gpu-scope release/acquire)
-//     and per-(sequence, kv-head) arrival counters, never by a grid-wide barrier;
-//   * warp 0 of every CTA is a TMA producer: it walks the CTA's own task list and
-//     streams every weight row and every KV page the CTA will need into a ring of
-//     shared-memory slots, without waiting on any dependency (weights and old KV rows
-//     never depend on this step's activations), so HBM keeps streaming while the
-//     consumer warps wait on counters;
-//   * warps 1..8 consume: BF16 mma.sync GEMV tiles (weights as the 16-row A operand,
-//     the <= 8 batch rows as the 8-column B operand), flash-decode attention with
-//     online softmax, fused epilogues (RoPE + KV append, residual add, SwiGLU,
-//     partial argmax).
+//   * the step is a fixed list of stages per layer -- QKV tiles, attention key splits
+//     (+ a merge of the splits' partial softmax states), O-projection tiles, gate/up
+//     tiles, down tiles -- then LM-head tiles and the greedy argmax. Each stage's work
+//     is cut into row tiles (GEMV) or page ranges (attention) statically assigned to CTAs;
+//   * stages are ordered by the data itself, never by a grid-wide barrier: up to
+//     kMaxTaggedBatch rows every activation word carries the tag of the write that
+//     produced it (one 64-bit store, no fence), and a reader polls the words it needs;
+//     above that, fp32 activations sit behind per-stage counters (release / acquire);
+//   * warp 0 of every CTA is the loader: it walks the CTA's own task list and streams
+//     every weight row and every KV page the CTA will need into a ring of shared-memory
+//     slots with TMA, without waiting on any dependency (weights and old KV rows never
+//     depend on this step's activations), so HBM keeps streaming while the consumers
+//     wait. It has the SM's scheduler 0 to itself (warps 4 and 8 only exit), so busy
+//     consumer warps never starve it of issue slots;
+//   * eight consumer warps (warps 1-3, 5-7, 9-10 on schedulers 1-3) compute: exact fp32
+//     CUDA-core GEMV for batches up to 4, BF16 mma.sync GEMV tiles above (activations
+//     split hi + lo), flash-decode attention on mma.sync with keys in the M dimension and
+//     online softmax, fused epilogues (RoPE + KV append, residual add, SwiGLU, partial
+//     argmax); warp 11 optionally prefetches the loader's future reads into L2.
 // Every wait is bounded; on an error the kernel latches a status word and winds down
 // (waits become no-ops, in-flight TMA copies are drained) instead of hanging.
 #pragma once
@@ -32,7 +36,14 @@ typedef __nv_bfloat16 bf16;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
-constexpr int kThreads = 64 + kConsumerThreads;   // warp 0 = loader, warp 9 = L2 prefetcher
+// Warp roles. An SM schedules warp w on scheduler w mod 4: the loader (warp 0) keeps
+// scheduler 0 to itself (warps 4 and 8 exit at once), the consumers are warps 1-3, 5-7,
+// 9 and 10, warp 11 is the optional L2 prefetcher.
+constexpr int kWarps = 12;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kPrefetchWarp = 11;
+__device__ __forceinline__ bool idle_warp(int w) { return w == 4 || w == 8; }
+__device__ __forceinline__ int consumer_index(int w) { return w - 1 - (w > 4) - (w > 8); }
 constexpr int kDefaultPrefetchSlots = 0;          // L2 prefetch lead (slots); 0 = off
 constexpr int kStages = 6;                         // shared-memory ring depth
 constexpr int KCW = 2048;                          // GEMV k-chunk: columns of a weight slot
@@ -82,7 +93,8 @@ __device__ unsigned long long g_mk_prof[kProfCtas][kProfSections];
 enum ProfSection { PS_OTHER = 0, PS_G_DATA = 1, PS_G_SLOTS = 2, PS_G_EPI = 3, PS_G_END = 4,
                    PS_A_ENTRY = 21, PS_A_QPOLL = 22, PS_A_QSYNC = 23, PS_A_FRAG = 24, PS_A_LOOP = 25,
                    PS_A_POST = 26, PS_A_FINISH = 27, PS_M_ML = 28, PS_M_W = 29, PS_M_O = 30,
-                   PS_A_END = 31, PS_EMBED = 32, PS_ARGMAX = 33, PS_TOTAL = 63 };
+                   PS_A_END = 31, PS_EMBED = 32, PS_ARGMAX = 33, PS_A_LWAIT = 36, PS_G_SWAIT = 37,
+                   PS_TOTAL = 63 };
 
 enum TraceCode { TR_WAIT = 1, TR_READY = 2, TR_DONE = 3, TR_PIECE = 4, TR_MERGE = 5, TR_END = 6,
                  TR_P_STAGE = 11, TR_P_BLOCK = 12, TR_P_GO = 13,
@@ -131,10 +143,13 @@ struct Plan {
     uint32_t* arrivals;                 // argmax arrival counter
     int* status;                        // [0] code, [1] task
     bf16* kv;                           // paged pool base
-    const void* kv_map;                 // CUtensorMap of the pool as [rows][hd], 128B swizzle
 };
 
 struct StepArgs {
+    // CUtensorMap of the KV pool as [rows][hd] (box 64 x 16, 128B swizzle). It travels in
+    // the kernel parameters (grid-constant), so a TMA copy finds its descriptor in the
+    // parameter space instead of fetching it from global memory.
+    alignas(64) CUtensorMap kv_tmap;
     Plan p;
     const int* tokens;
     const int* positions;
@@ -477,10 +492,14 @@ __device__ __forceinline__ SeqSpan seq_span(const Plan& p, const Smem* sm, int l
     return s;
 }
 
-// Calls f(b, g, first unit in this bg, count, split, nsplit) for each piece of this CTA.
-// Units are (b, g, page) triples in order; CTA c owns [c U / C, (c+1) U / C) (or unit c
-// when U < C). A piece is this CTA's share of one (b, g); its split index is its rank
-// among the CTAs that share that (b, g).
+// Calls f(b, g, first page of the piece within the span, page count, split, nsplit) for
+// each attention piece of this CTA. Work items are (sequence b, kv head g) with np(b)
+// pages each. When there are no more items than CTAs, every item gets CTAs of its own,
+// in proportion to its pages and at least one: with C' = C - W spare CTAs and S_i the
+// pages of the items before item i, item i takes CTAs [i + C' S_i / U, i + 1 + C' S_(i+1) / U)
+// and splits its pages evenly over min(CTAs, pages) of them. No CTA then carries the
+// fixed cost of two pieces (those CTAs would finish last and every merge would wait for
+// them). With more items than CTAs, (b, g, page) units are dealt out in contiguous ranges.
 template <typename F>
 __device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta, F&& f) {
     const Plan& p = a.p;
@@ -488,13 +507,32 @@ __device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta
     uint32_t U = 0;
     for (int b = 0; b < a.B; ++b) U += (uint32_t)(p.Hkv * seq_span(p, sm, l, b).np);
     const uint32_t C = (uint32_t)p.C;
-    uint32_t u0, u1;
-    if (U >= C) { u0 = (uint32_t)cta * U / C; u1 = (uint32_t)(cta + 1) * U / C; }
-    else { u0 = cta; u1 = (uint32_t)cta < U ? cta + 1 : cta; }
+    const uint32_t W = (uint32_t)(a.B * p.Hkv);
+    if (W <= C) {
+        const uint32_t Cp = C - W;
+        uint32_t S = 0, i = 0;
+        for (int b = 0; b < a.B; ++b) {
+            const SeqSpan sp = seq_span(p, sm, l, b);
+            for (int g = 0; g < p.Hkv; ++g, ++i) {
+                const uint32_t c0 = i + Cp * S / U;
+                S += (uint32_t)sp.np;
+                const uint32_t c1 = i + 1 + Cp * S / U;
+                if ((uint32_t)cta < c1) {
+                    const int nsplit = min((int)(c1 - c0), sp.np), k = cta - (int)c0;
+                    if (k < nsplit) {
+                        const int u0 = (int)((uint32_t)k * sp.np / nsplit);
+                        const int u1 = (int)((uint32_t)(k + 1) * sp.np / nsplit);
+                        f(b, g, sp, u0, u1 - u0, k, nsplit);
+                    }
+                    return;
+                }
+            }
+        }
+        return;
+    }
+    const uint32_t u0 = (uint32_t)cta * U / C, u1 = (uint32_t)(cta + 1) * U / C;
     if (u0 >= u1) return;
-    auto first_cta = [&](uint32_t s) -> int {
-        return U >= C ? (int)(((s + 1) * C - 1) / U) : (int)s;
-    };
+    auto first_cta = [&](uint32_t s) -> int { return (int)(((s + 1) * C - 1) / U); };
     uint32_t s = 0;
     for (int b = 0; b < a.B; ++b) {
         const SeqSpan sp = seq_span(p, sm, l, b);
@@ -652,8 +690,8 @@ struct Producer {
                 __syncwarp();
                 if (lane < nbox) {
                     const int row = (((l * p.num_pages + page) * 2 + kv) * p.Hkv + g) * kPage;
-                    if (pf) l2_prefetch_2d(p.kv_map, bx * 64, row);
-                    else tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, p.kv_map, bx * 64, row,
+                    if (pf) l2_prefetch_2d(&a->kv_tmap, bx * 64, row);
+                    else tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, &a->kv_tmap, bx * 64, row,
                                      bar, policy);
                 }
                 if (l == 1 && !pf) MK_TRACE_P(*this, TR_S_ISSUE, seq);
@@ -666,7 +704,7 @@ struct Producer {
     template <int HD>
     __device__ __noinline__ void run(int cta) {
         policy = policy_evict_first();
-        if (lane == 0) prefetch_tmap(a->p.kv_map);
+        if (lane == 0) prefetch_tmap(&a->kv_tmap);
         const Plan& p = a->p;
         bool ok = !sm->abort;
         for (int l = 0; l < p.L && ok; ++l) {
@@ -918,7 +956,9 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
                 if (gi < ng) {
                     const int nr = group_rows(s, n, gi, ngate);
                     if (trace_slots(s)) MK_TRACE_C(c, TR_S_WAIT, c.seq);
+                    MK_PROF_MARK(c, PS_G_SLOTS + 4 * s.kind);
                     const bool ok = wait_full_at(c, c.seq, s.task_id);
+                    MK_PROF_MARK(c, PS_G_SWAIT);
                     if (trace_slots(s)) MK_TRACE_C(c, TR_S_FULL, c.seq);
                     uint4 wr[8];
 #pragma unroll
@@ -1554,126 +1594,139 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
     float oacc[NMT][4];
 #pragma unroll
     for (int i = 0; i < NMT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-    float* pbuf = c.scratch + c.cw * 16 * 9;  // P[16 keys][9] for this warp (fp32)
-    // warp groups: a 32 KB slot holds PPS pages; WPS warps take one page each, and the
-    // 8 / WPS groups take consecutive slots in turn
-    constexpr int WPS = PPS < kConsumerWarps ? PPS : kConsumerWarps;
-    constexpr int NGRP = kConsumerWarps / WPS;
-    const int grp = c.cw / WPS, wpage = c.cw % WPS;
+    float* pbuf = c.scratch + c.cw * 32 * 9;  // P[32 keys][9] for this warp (fp32)
+    // Windows of 16 pages: warp w takes pages 2w and 2w + 1 (one ring slot holds PPS
+    // pages) and processes the two together, so two independent MMA chains hide each
+    // other's latency. Every warp waits for and releases every slot of the window in
+    // order (a slot is handed back only after its data has arrived).
+    constexpr int WIN = 2 * kConsumerWarps;
     const int lrow8 = c.lane & 7, lmi = c.lane >> 3;
+    const int pa = 2 * c.cw, mys = pa / PPS;
 
-    int sidx = 0;
-    for (int st = 0; st < n; st += PPS, ++sidx) {
-        const int np = min(PPS, n - st);
-        if (l == 1) MK_TRACE_C(c, TR_S_WAIT, c.seq);
-        const bool ok = wait_full(c, task);
-        if (l == 1) MK_TRACE_C(c, TR_S_FULL, c.seq);
-        const uint32_t slot = c.ring_s + (c.seq % kStages) * kSlotBytes;
-        if (has_last && st + np == n) {
-            // splice the new row into the last page and append it to the pool
-            if (c.cw == 0 && ok) {
-                const int pi = np - 1, row = pos % kPage;
-                const int page = __ldg(a.page_table + (size_t)b * a.max_pages + pos / kPage);
-                if (page >= 0 && page < p.num_pages) {
-                    if (c.lane < 2 * NCH) {
-                        const int kv = c.lane / NCH, ch = c.lane % NCH;
-                        const uint4 val = *reinterpret_cast<const uint4*>((kv ? c.sm->vnew : c.sm->knew) + ch * 8);
-                        const uint32_t box = slot + pi * 64 * HD + kv * 32 * HD + (ch >> 3) * 2048;
-                        const uint32_t dst = box + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
-                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(val.x),
-                                     "r"(val.y), "r"(val.z), "r"(val.w) : "memory");
-                        bf16* gdst = p.kv + ((((size_t)l * p.num_pages + page) * 2 + kv) * p.Hkv + g) *
-                                                kPage * HD + (size_t)row * HD + ch * 8;
-                        *reinterpret_cast<uint4*>(gdst) = val;
+    for (int w0 = 0; w0 < n; w0 += WIN) {
+        const int nw = min(WIN, n - w0), nsl = (nw + PPS - 1) / PPS;
+        for (int j = 0; j < nsl; ++j) {
+            MK_PROF_MARK(c, PS_A_LOOP);
+            const bool ok = wait_full_at(c, c.seq + j, task);
+            MK_PROF_MARK(c, PS_A_LWAIT);
+            if (j == mys && pa < nw && ok && !c.sm->abort) {
+                const uint32_t slot = c.ring_s + ((c.seq + j) % kStages) * kSlotBytes;
+                const uint32_t kbA = slot + (pa % PPS) * 64 * HD, kbB = kbA + 64 * HD;
+                const int keyA = (sp.p0 + u + w0 + pa) * kPage, keyB = keyA + kPage;
+                const bool hasB = pa + 1 < nw;
+                if (has_last && (w0 + pa == n - 1 || (hasB && w0 + pa + 1 == n - 1))) {
+                    // splice the new row into the last page and append it to the pool
+                    const uint32_t kb = w0 + pa == n - 1 ? kbA : kbB;
+                    const int row = pos % kPage;
+                    const int page = __ldg(a.page_table + (size_t)b * a.max_pages + pos / kPage);
+                    if (page >= 0 && page < p.num_pages) {
+                        if (c.lane < 2 * NCH) {
+                            const int kv = c.lane / NCH, ch = c.lane % NCH;
+                            const uint4 val = *reinterpret_cast<const uint4*>((kv ? c.sm->vnew : c.sm->knew) + ch * 8);
+                            const uint32_t box = kb + kv * 32 * HD + (ch >> 3) * 2048;
+                            const uint32_t dst = box + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+                            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(val.x),
+                                         "r"(val.y), "r"(val.z), "r"(val.w) : "memory");
+                            bf16* gdst = p.kv + ((((size_t)l * p.num_pages + page) * 2 + kv) * p.Hkv + g) *
+                                                    kPage * HD + (size_t)row * HD + ch * 8;
+                            *reinterpret_cast<uint4*>(gdst) = val;
+                        }
+                    } else {
+                        set_error(p, c.sm, kErrBadPage, task);
                     }
-                } else {
-                    set_error(p, c.sm, kErrBadPage, task);
+                    fence_proxy_async_smem();  // generic writes before the slot's next TMA fill
+                    __syncwarp();
                 }
-                fence_proxy_async_smem();
-            }
-            consumer_sync();
-        }
-        if (ok && !c.sm->abort && (sidx % NGRP) == grp) {
-            for (int pi = wpage; pi < np; pi += WPS) {
-                const uint32_t kbase = slot + pi * 64 * HD;
-                const uint32_t vbase = kbase + 32 * HD;
-                const int kbase_key = (sp.p0 + u + st + pi) * kPage;
-                const bool vA = kbase_key + gq >= lo && kbase_key + gq <= pos;        // key g
-                const bool vB = kbase_key + gq + 8 >= lo && kbase_key + gq + 8 <= pos;  // key g + 8
-                // S^T = K q^T: A = K rows (keys) via ldmatrix, B = q^T
-                float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+                // S^T = K q^T for both pages: A = K rows (keys) via ldmatrix, B = q^T; four
+                // accumulator chains (page A / B x hi / lo)
+                float shA[4] = {0.f, 0.f, 0.f, 0.f}, slA[4] = {0.f, 0.f, 0.f, 0.f};
+                float shB[4] = {0.f, 0.f, 0.f, 0.f}, slB[4] = {0.f, 0.f, 0.f, 0.f};
                 {
                     const int krow = lrow8 + (lmi & 1) * 8;
 #pragma unroll
                     for (int s = 0; s < NKS; ++s) {
                         const int ch = 2 * s + (lmi >> 1);
-                        uint32_t a0, a1, a2, a3;
-                        ldmatrix_x4(kbase + (ch >> 3) * 2048 + krow * 128 + (((ch & 7) ^ (krow & 7)) << 4),
-                                    a0, a1, a2, a3);
-                        mma_16816(sh, a0, a1, a2, a3, qa[s][0], qa[s][1]);
-                        mma_16816(sl, a0, a1, a2, a3, ql[s][0], ql[s][1]);
+                        const uint32_t off = (ch >> 3) * 2048 + krow * 128 + (((ch & 7) ^ (krow & 7)) << 4);
+                        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                        ldmatrix_x4(kbA + off, a0, a1, a2, a3);
+                        ldmatrix_x4(kbB + off, b0, b1, b2, b3);  // (page B may be past the piece: masked)
+                        mma_16816(shA, a0, a1, a2, a3, qa[s][0], qa[s][1]);
+                        mma_16816(shB, b0, b1, b2, b3, qa[s][0], qa[s][1]);
+                        mma_16816(slA, a0, a1, a2, a3, ql[s][0], ql[s][1]);
+                        mma_16816(slB, b0, b1, b2, b3, ql[s][0], ql[s][1]);
                     }
                 }
-                // scores: [key g][head 2t], [g][2t+1], [g+8][2t], [g+8][2t+1]
-                float sc[4];
+                // scores of keys A+g, A+g+8, B+g, B+g+8 (index 4 * page + 2 * (g + 8) + head)
+                auto valid = [&](int key) { return key >= lo && key <= pos; };
+                const bool okB = hasB;
+                float sc[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const bool v = e < 2 ? vA : vB;
-                    sc[e] = v ? (sh[e] + sl[e]) * p.scale : -INFINITY;
+                    sc[e] = valid(keyA + gq + (e >> 1) * 8) ? (shA[e] + slA[e]) * p.scale : -INFINITY;
+                    sc[4 + e] = okB && valid(keyB + gq + (e >> 1) * 8) ? (shB[e] + slB[e]) * p.scale : -INFINITY;
                 }
-                float pv[4];
+                float pv[8];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    float mb = fmaxf(sc[hh], sc[2 + hh]);
+                    float mb = fmaxf(fmaxf(sc[hh], sc[2 + hh]), fmaxf(sc[4 + hh], sc[6 + hh]));
                     mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
                     mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
                     mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
                     const float m_new = fmaxf(m_run[hh], mb);
-                    float corr = 1.f, p0 = 0.f, p1 = 0.f;
+                    float corr = 1.f;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) pv[2 * k + hh] = 0.f;
                     if (m_new != -INFINITY) {
                         corr = expf(m_run[hh] - m_new);
-                        p0 = expf(sc[hh] - m_new);
-                        p1 = expf(sc[2 + hh] - m_new);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) pv[2 * k + hh] = expf(sc[2 * k + hh] - m_new);
                     }
                     m_run[hh] = m_new;
-                    l_run[hh] = l_run[hh] * corr + p0 + p1;
-                    pv[hh] = p0;
-                    pv[2 + hh] = p1;
+                    l_run[hh] = l_run[hh] * corr + ((pv[hh] + pv[2 + hh]) + (pv[4 + hh] + pv[6 + hh]));
 #pragma unroll
                     for (int mt = 0; mt < NMT; ++mt) { oacc[mt][hh] *= corr; oacc[mt][2 + hh] *= corr; }
                 }
-                // P^T as the B operand (keys x heads): transpose through this warp's buffer
-                pbuf[gq * 9 + 2 * t] = pv[0];
-                pbuf[gq * 9 + 2 * t + 1] = pv[1];
-                pbuf[(gq + 8) * 9 + 2 * t] = pv[2];
-                pbuf[(gq + 8) * 9 + 2 * t + 1] = pv[3];
+                // P^T as the B operand (32 keys x heads): transpose through this warp's buffer
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int key = gq + 8 * k;  // A: g, g+8; B: 16+g, 24+g
+                    pbuf[key * 9 + 2 * t] = pv[2 * k];
+                    pbuf[key * 9 + 2 * t + 1] = pv[2 * k + 1];
+                }
                 __syncwarp();
-                uint32_t pbh0, pbl0, pbh1, pbl1;
-                split_bf16x2(pbuf[(2 * t) * 9 + gq], pbuf[(2 * t + 1) * 9 + gq], pbh0, pbl0);
-                split_bf16x2(pbuf[(2 * t + 8) * 9 + gq], pbuf[(2 * t + 9) * 9 + gq], pbh1, pbl1);
+                uint32_t ph[2][2], pl[2][2];  // [page][b0b1 | b2b3]
+#pragma unroll
+                for (int pg = 0; pg < 2; ++pg) {
+                    split_bf16x2(pbuf[(16 * pg + 2 * t) * 9 + gq], pbuf[(16 * pg + 2 * t + 1) * 9 + gq], ph[pg][0], pl[pg][0]);
+                    split_bf16x2(pbuf[(16 * pg + 2 * t + 8) * 9 + gq], pbuf[(16 * pg + 2 * t + 9) * 9 + gq], ph[pg][1], pl[pg][1]);
+                }
                 __syncwarp();
-                // keys 2t, 2t+1 / 2t+8, 2t+9 of V^T: zero the invalid ones (garbage-safe)
-                const int k2 = kbase_key + 2 * t;
-                const uint32_t mlo = ((k2 >= lo && k2 <= pos) ? 0x0000ffffu : 0u) |
-                                     ((k2 + 1 >= lo && k2 + 1 <= pos) ? 0xffff0000u : 0u);
-                const uint32_t mhi = ((k2 + 8 >= lo && k2 + 8 <= pos) ? 0x0000ffffu : 0u) |
-                                     ((k2 + 9 >= lo && k2 + 9 <= pos) ? 0xffff0000u : 0u);
+                // keys 2t, 2t+1 / 2t+8, 2t+9 of each page's V^T: zero the invalid ones
+                auto vmask = [&](int k0) {
+                    return (valid(k0) ? 0x0000ffffu : 0u) | (valid(k0 + 1) ? 0xffff0000u : 0u);
+                };
+                const uint32_t mloA = vmask(keyA + 2 * t), mhiA = vmask(keyA + 2 * t + 8);
+                const uint32_t mloB = okB ? vmask(keyB + 2 * t) : 0u, mhiB = okB ? vmask(keyB + 2 * t + 8) : 0u;
                 // O^T += V^T P^T: A = V^T (dims x keys) via ldmatrix.trans of the V rows
                 const int vrow = lrow8 + (lmi >> 1) * 8;
 #pragma unroll
                 for (int mt = 0; mt < NMT; ++mt) {
                     const int ch = 2 * mt + (lmi & 1);
-                    uint32_t a0, a1, a2, a3;
-                    ldmatrix_x4_trans(vbase + (ch >> 3) * 2048 + vrow * 128 + (((ch & 7) ^ (vrow & 7)) << 4),
-                                      a0, a1, a2, a3);
-                    a0 &= mlo; a1 &= mlo; a2 &= mhi; a3 &= mhi;
-                    mma_16816(oacc[mt], a0, a1, a2, a3, pbh0, pbh1);
-                    mma_16816(oacc[mt], a0, a1, a2, a3, pbl0, pbl1);
+                    const uint32_t off = 32 * HD + (ch >> 3) * 2048 + vrow * 128 + (((ch & 7) ^ (vrow & 7)) << 4);
+                    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                    ldmatrix_x4_trans(kbA + off, a0, a1, a2, a3);
+                    ldmatrix_x4_trans(kbB + off, b0, b1, b2, b3);
+                    a0 &= mloA; a1 &= mloA; a2 &= mhiA; a3 &= mhiA;
+                    b0 &= mloB; b1 &= mloB; b2 &= mhiB; b3 &= mhiB;
+                    mma_16816(oacc[mt], a0, a1, a2, a3, ph[0][0], ph[0][1]);
+                    mma_16816(oacc[mt], a0, a1, a2, a3, pl[0][0], pl[0][1]);
+                    mma_16816(oacc[mt], b0, b1, b2, b3, ph[1][0], ph[1][1]);
+                    mma_16816(oacc[mt], b0, b1, b2, b3, pl[1][0], pl[1][1]);
                 }
             }
+            release_at(c, c.seq + j);
         }
-        release_slot(c);
-        if (l == 1) MK_TRACE_C(c, TR_S_REL, c.seq - 1);
+        c.seq += nsl;
     }
 
     MK_PROF_MARK(c, PS_A_LOOP);
@@ -1869,7 +1922,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     }
     __syncthreads();
 
-    if (warp == 0 || warp == kConsumerWarps + 1) {
+    if (idle_warp(warp)) return;
+    if (warp == 0 || warp == kPrefetchWarp) {
         Producer pr;
         pr.a = &a;
         pr.sm = sm;
@@ -1886,9 +1940,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     c.scratch = scratch;
     c.ring_s = smem_u32(ring);
     c.seq = 0;
-    c.cw = warp - 1;
+    c.cw = consumer_index(warp);
     c.lane = lane;
-    c.tid = threadIdx.x - 32;
+    c.tid = c.cw * 32 + lane;
     c.tn = 0;
     consumer_run<HD>(c, cta);
 }
