@@ -244,11 +244,23 @@ MK_API mk_status mk_decode_step_noalloc(const mk_model_desc *desc, const mk_weig
  *   MK_BUF_ATTN  attention output of the last layer (input of the O projection),
  *                [max_batch][n_q_heads * head_dim], permuted columns
  *   MK_BUF_H     SwiGLU activations of the last layer (input of the down projection),
- *                [max_batch][ffn_dim], permuted columns
+ *                [max_batch][ffn_dim], permuted columns; for a MoE model
+ *                [max_batch][n_experts * expert_ffn_dim], where slot j of the routed
+ *                union (ascending expert id) holds columns [j*Fe, (j+1)*Fe), already
+ *                multiplied by the row's routing weight (0 for an expert it did not pick)
+ *   MK_BUF_ROUTE router logits of the last layer, [max_batch][n_experts], tagged words
+ *   MK_BUF_MOE_UNION  int32 [n_layers]: experts in each layer's routed union (last step)
  * Permuted columns: logical column k is stored at
  *   (k & ~63) | ((k & 7) >> 1) << 4 | ((k & 63) >> 3) << 1 | (k & 1).
  * *dev_ptr receives the device address (read-only use), *bytes its size. */
-typedef enum mk_buffer { MK_BUF_X = 1, MK_BUF_QKV = 2, MK_BUF_ATTN = 3, MK_BUF_H = 4 } mk_buffer;
+typedef enum mk_buffer {
+    MK_BUF_X = 1,
+    MK_BUF_QKV = 2,
+    MK_BUF_ATTN = 3,
+    MK_BUF_H = 4,
+    MK_BUF_ROUTE = 5,
+    MK_BUF_MOE_UNION = 6
+} mk_buffer;
 MK_API mk_status mk_debug_buffer(const mk_handle *h, int32_t which, void **dev_ptr,
                                  int64_t *bytes);
 

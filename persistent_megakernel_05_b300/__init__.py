@@ -35,7 +35,7 @@ ABI_SYMBOLS = ("mk_create", "mk_kv_alloc", "mk_kv_free", "mk_decode_step", "mk_s
                "mk_status_reset", "mk_set_option", "mk_get_info", "mk_debug_buffer",
                "mk_status_string", "mk_destroy", "mk_decode_step_noalloc")
 MK_NOALLOC_SCRATCH_BYTES = 8 << 20
-MK_BUF_X, MK_BUF_QKV, MK_BUF_ATTN, MK_BUF_H = 1, 2, 3, 4
+MK_BUF_X, MK_BUF_QKV, MK_BUF_ATTN, MK_BUF_H, MK_BUF_ROUTE, MK_BUF_MOE_UNION = 1, 2, 3, 4, 5, 6
 
 
 class MkError(RuntimeError):
@@ -287,12 +287,17 @@ class DecodeModel:
         import torch
         ptr, nbytes = mk_debug_buffer(self.handle, which)
         cfg = self.cfg
+        if which == MK_BUF_MOE_UNION:
+            t = torch.as_tensor(_CudaArray(ptr, (nbytes // 4,), "<i4"), device=f"cuda:{self.device}")
+            return t.cpu().numpy().copy()
+        h_width = cfg.n_experts * cfg.expert_ffn_dim if cfg.is_moe else cfg.ffn_dim
         width = {MK_BUF_X: cfg.d_model, MK_BUF_QKV: (cfg.n_q_heads + 2 * cfg.n_kv_heads) * cfg.head_dim,
-                 MK_BUF_ATTN: cfg.n_q_heads * cfg.head_dim, MK_BUF_H: cfg.ffn_dim}[which]
+                 MK_BUF_ATTN: cfg.n_q_heads * cfg.head_dim, MK_BUF_H: h_width,
+                 MK_BUF_ROUTE: cfg.n_experts}[which]
         step = nbytes // (cfg.max_batch * width * 4)  # 2: tagged words (value in the low half)
         t = torch.as_tensor(_CudaArray(ptr, (nbytes // 4,), "<f4"), device=f"cuda:{self.device}")
         a = t.cpu().numpy()[0::step].reshape(cfg.max_batch, -1).copy()
-        if which != MK_BUF_QKV:
+        if which not in (MK_BUF_QKV, MK_BUF_ROUTE):
             idx = np.array([perm_col(k) for k in range(a.shape[1])])
             a = a[:, idx]
         return a

@@ -72,8 +72,15 @@ mk_status validate_desc(const mk_model_desc* d) {
     if (d->vocab < 1) return MK_ERR_INVALID_ARG;
     // GEMV rows are split over CTAs in 32-bit arithmetic (rows * CTAs < 2^32, CTAs <= 1024)
     if (d->vocab > (1 << 22) || d->ffn_dim > (1 << 22) || d->d_model > (1 << 22)) return MK_ERR_INVALID_ARG;
-    if (d->n_experts != 0) return MK_ERR_INVALID_ARG;  // MoE stages: not in this build yet
-    if (d->ffn_dim < 64 || d->ffn_dim % 64) return MK_ERR_INVALID_ARG;
+    if (d->n_experts < 0 || d->n_experts > mk::kMaxExperts) return MK_ERR_INVALID_ARG;
+    if (d->n_experts > 0) {
+        // MoE: top-k of E experts, each a SwiGLU of width expert_ffn_dim (one k-chunk)
+        if (d->top_k < 1 || d->top_k > d->n_experts) return MK_ERR_INVALID_ARG;
+        if (d->expert_ffn_dim < 64 || d->expert_ffn_dim % 64 || d->expert_ffn_dim > mk::KCW)
+            return MK_ERR_INVALID_ARG;
+    } else if (d->ffn_dim < 64 || d->ffn_dim % 64) {
+        return MK_ERR_INVALID_ARG;
+    }
     if (!(d->rms_eps > 0.f) || !(d->rope_theta > 0.f)) return MK_ERR_INVALID_ARG;
     if (d->sliding_window < 0) return MK_ERR_INVALID_ARG;
     if (d->max_batch < 1 || d->max_batch > mk::kMaxBatch) return MK_ERR_INVALID_ARG;
@@ -86,8 +93,9 @@ mk_status validate_weights(const mk_model_desc* d, const mk_weights* w) {
     if (!w || !w->embed || !w->final_norm || !w->lm_head || !w->layers) return MK_ERR_INVALID_ARG;
     for (int l = 0; l < d->n_layers; ++l) {
         const mk_layer_weights& L = w->layers[l];
-        if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.mlp_norm || !L.w_gate ||
-            !L.w_up || !L.w_down)
+        if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.mlp_norm) return MK_ERR_INVALID_ARG;
+        if (d->n_experts > 0 ? (!L.router || !L.exp_gate || !L.exp_up || !L.exp_down)
+                             : (!L.w_gate || !L.w_up || !L.w_down))
             return MK_ERR_INVALID_ARG;
     }
     return MK_OK;
@@ -196,6 +204,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     const int G = Hq / Hkv, F = desc->ffn_dim, V = desc->vocab, maxB = desc->max_batch;
     const int C = h->num_ctas;
     const int qkv_rows = (Hq + 2 * Hkv) * hd;
+    const int E = desc->n_experts, Fe = desc->expert_ffn_dim;
+    const int hrow = E > 0 ? E * Fe : F;  // SwiGLU row: dense width, or every expert's slot
 
     // ---- scratch arena
     size_t off = 0;
@@ -204,11 +214,13 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     const size_t o_x = take(8 * (size_t)maxB * d);
     const size_t o_qkv = take(8 * (size_t)maxB * qkv_rows);
     const size_t o_attn = take(8 * (size_t)maxB * Hq * hd);
-    const size_t o_h = take(8 * (size_t)maxB * F);
+    const size_t o_h = take(8 * (size_t)maxB * hrow);
     const size_t o_part = take(8 * (size_t)maxB * Hkv * C * (G * hd + 2 * G));
+    const size_t o_route = take(8 * (size_t)maxB * (E > 0 ? E : 1));
+    const size_t o_union = take(sizeof(int) * (size_t)L);
     const size_t o_xf = take(sizeof(float) * (size_t)maxB * d);
     const size_t o_attnf = take(sizeof(float) * (size_t)maxB * Hq * hd);
-    const size_t o_hf = take(sizeof(float) * (size_t)maxB * F);
+    const size_t o_hf = take(sizeof(float) * (size_t)maxB * hrow);
     const size_t o_am = take(sizeof(float2) * (size_t)C * maxB);
     h->counters_words = (size_t)(1 + L * mk::kStagesPerLayer) * mk::kCounterStride;
     h->arrivals_words = (size_t)mk::kCounterStride;
@@ -261,10 +273,13 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
         lp[l].wq = (const bf16*)W.wq; lp[l].wk = (const bf16*)W.wk; lp[l].wv = (const bf16*)W.wv;
         lp[l].wo = (const bf16*)W.wo; lp[l].w_gate = (const bf16*)W.w_gate;
         lp[l].w_up = (const bf16*)W.w_up; lp[l].w_down = (const bf16*)W.w_down;
+        lp[l].router = (const bf16*)W.router; lp[l].exp_gate = (const bf16*)W.exp_gate;
+        lp[l].exp_up = (const bf16*)W.exp_up; lp[l].exp_down = (const bf16*)W.exp_down;
         lp[l].attn_gain = h->d_gains + (size_t)(2 * l) * d;
         lp[l].mlp_gain = h->d_gains + (size_t)(2 * l + 1) * d;
         lp[l].sliding = h->sliding[l];
-        wbytes += 2LL * ((int64_t)qkv_rows * d + (int64_t)d * Hq * hd + 3LL * F * d + 2LL * d);
+        const int64_t mlp = E > 0 ? (int64_t)E * d + 3LL * E * Fe * d : 3LL * F * d;
+        wbytes += 2LL * ((int64_t)qkv_rows * d + (int64_t)d * Hq * hd + mlp + 2LL * d);
     }
     wbytes += 2LL * ((int64_t)V * d + d);
     h->weight_bytes = wbytes;
@@ -278,6 +293,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
 
     mk::Plan& p = h->plan;
     p.L = L; p.d = d; p.Hq = Hq; p.Hkv = Hkv; p.hd = hd; p.G = G; p.F = F; p.V = V;
+    p.E = E; p.topk = desc->top_k; p.Fe = Fe; p.hrow = hrow;
     p.window = desc->sliding_window; p.max_pos = desc->max_positions; p.maxB = maxB;
     p.num_pages = 0;
     p.eps = desc->rms_eps;
@@ -294,6 +310,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     p.attn = (uint64_t*)(base + o_attn);
     p.h = (uint64_t*)(base + o_h);
     p.part = (uint64_t*)(base + o_part);
+    p.route = (uint64_t*)(base + o_route);
+    p.moe_union = (int*)(base + o_union);
     p.xf = (float*)(base + o_xf);
     p.attnf = (float*)(base + o_attnf);
     p.hf = (float*)(base + o_hf);
@@ -501,7 +519,17 @@ mk_status mk_debug_buffer(const mk_handle* h, int32_t which, void** dev_ptr, int
             return MK_OK;
         case MK_BUF_H:
             *dev_ptr = tg ? (void*)p.h : (void*)p.hf;
-            *bytes = (tg ? 8 : 4) * B * p.F;
+            *bytes = (tg ? 8 : 4) * B * p.hrow;
+            return MK_OK;
+        case MK_BUF_ROUTE:
+            if (p.E == 0) return MK_ERR_INVALID_ARG;
+            *dev_ptr = p.route;
+            *bytes = 8 * B * p.E;
+            return MK_OK;
+        case MK_BUF_MOE_UNION:
+            if (p.E == 0) return MK_ERR_INVALID_ARG;
+            *dev_ptr = p.moe_union;
+            *bytes = 4 * (int64_t)p.L;
             return MK_OK;
     }
     return MK_ERR_INVALID_ARG;
@@ -636,6 +664,8 @@ extern "C" mk_status mk_decode_step_noalloc(
     const int maxB = desc->max_batch, C = D->num_sms;
     if ((d + C - 1) / C > mk::kMaxOwnRows) return MK_ERR_INVALID_ARG;
     const int qkv_rows = (Hq + 2 * Hkv) * hd;
+    const int E = desc->n_experts, Fe = desc->expert_ffn_dim;
+    const int hrow = E > 0 ? E * Fe : F;
     const int64_t rows = (int64_t)L * num_pages * 2 * Hkv * mk::kPage;
     if (rows >= (1LL << 31)) return MK_ERR_INVALID_ARG;
 
@@ -648,15 +678,17 @@ extern "C" mk_status mk_decode_step_noalloc(
     const size_t o_am = take(sizeof(float2) * (size_t)C * maxB);
     const size_t o_xf = take(sizeof(float) * (size_t)maxB * d);
     const size_t o_attnf = take(sizeof(float) * (size_t)maxB * Hq * hd);
-    const size_t o_hf = take(sizeof(float) * (size_t)maxB * F);
+    const size_t o_hf = take(sizeof(float) * (size_t)maxB * hrow);
+    const size_t o_union = take(sizeof(int) * (size_t)L);
     // cleared every call (every call runs with tag epoch 1 and counter epoch 1): the
     // tagged activations and attention partials, the counters and the status word
     const size_t o_zero = off;
     const size_t o_x = take(8 * (size_t)maxB * d);
     const size_t o_qkv = take(8 * (size_t)maxB * qkv_rows);
     const size_t o_attn = take(8 * (size_t)maxB * Hq * hd);
-    const size_t o_h = take(8 * (size_t)maxB * F);
+    const size_t o_h = take(8 * (size_t)maxB * hrow);
     const size_t o_part = take(8 * (size_t)maxB * Hkv * C * (G * hd + 2 * G));
+    const size_t o_route = take(8 * (size_t)maxB * (E > 0 ? E : 1));
     const size_t o_cnt = take(sizeof(uint32_t) * (size_t)(1 + L * mk::kStagesPerLayer) * mk::kCounterStride);
     const size_t o_arr = take(sizeof(uint32_t) * mk::kCounterStride);
     const size_t o_status = take(sizeof(int) * 4);
@@ -692,6 +724,8 @@ extern "C" mk_status mk_decode_step_noalloc(
         lp.wq = (const bf16*)W.wq; lp.wk = (const bf16*)W.wk; lp.wv = (const bf16*)W.wv;
         lp.wo = (const bf16*)W.wo; lp.w_gate = (const bf16*)W.w_gate;
         lp.w_up = (const bf16*)W.w_up; lp.w_down = (const bf16*)W.w_down;
+        lp.router = (const bf16*)W.router; lp.exp_gate = (const bf16*)W.exp_gate;
+        lp.exp_up = (const bf16*)W.exp_up; lp.exp_down = (const bf16*)W.exp_down;
         lp.attn_gain = gains + (size_t)(2 * l) * d;
         lp.mlp_gain = gains + (size_t)(2 * l + 1) * d;
         lp.sliding = (desc->layer_is_sliding && desc->layer_is_sliding[l]) ? 1 : 0;
@@ -711,6 +745,7 @@ extern "C" mk_status mk_decode_step_noalloc(
     mk::StepArgs a;
     mk::Plan& p = a.p;
     p.L = L; p.d = d; p.Hq = Hq; p.Hkv = Hkv; p.hd = hd; p.G = G; p.F = F; p.V = V;
+    p.E = E; p.topk = desc->top_k; p.Fe = Fe; p.hrow = hrow;
     p.window = desc->sliding_window; p.max_pos = desc->max_positions; p.maxB = maxB;
     p.num_pages = num_pages;
     p.eps = desc->rms_eps;
@@ -727,6 +762,8 @@ extern "C" mk_status mk_decode_step_noalloc(
     p.attn = (uint64_t*)(base + o_attn);
     p.h = (uint64_t*)(base + o_h);
     p.part = (uint64_t*)(base + o_part);
+    p.route = (uint64_t*)(base + o_route);
+    p.moe_union = (int*)(base + o_union);
     p.xf = (float*)(base + o_xf);
     p.attnf = (float*)(base + o_attnf);
     p.hf = (float*)(base + o_hf);

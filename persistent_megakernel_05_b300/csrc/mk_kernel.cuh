@@ -54,6 +54,7 @@ constexpr int kMaxBatch = 8;
 constexpr int kPage = 16;
 constexpr int kTaskRows = 128;                     // <= 16 row groups of 8 per GEMV task
 constexpr int kMaxLayers = 128;
+constexpr int kMaxExperts = 64;                    // MoE: experts per layer (one warp routes a row)
 constexpr int kCounterStride = 32;                 // u32 words per counter (128 B apart)
 constexpr int kStagesPerLayer = 8;                 // counter slots per layer
 constexpr int kMaxOwnRows = 32;                    // residual rows a CTA owns: ceil(d / CTAs) <= 32
@@ -89,12 +90,12 @@ __device__ unsigned long long g_mk_prof[kProfCtas][kProfSections];
 #define MK_PROF_MARK(c, sec) do { } while (0)
 #define MK_PROF_BACK(dst, src) do { } while (0)
 #endif
-// profile sections: GEMV kind k (QKV, O, GU, DOWN, LM) uses 1 + 4k .. 4 + 4k
+// profile sections: GEMV kind k (QKV, O, GU, DOWN, LM, ROUTE) uses 1 + 4k .. 4 + 4k
 enum ProfSection { PS_OTHER = 0, PS_G_DATA = 1, PS_G_SLOTS = 2, PS_G_EPI = 3, PS_G_END = 4,
-                   PS_A_ENTRY = 21, PS_A_QPOLL = 22, PS_A_QSYNC = 23, PS_A_FRAG = 24, PS_A_LOOP = 25,
-                   PS_A_POST = 26, PS_A_FINISH = 27, PS_M_ML = 28, PS_M_W = 29, PS_M_O = 30,
-                   PS_A_END = 31, PS_EMBED = 32, PS_ARGMAX = 33, PS_A_LWAIT = 36, PS_G_SWAIT = 37,
-                   PS_TOTAL = 63 };
+                   PS_A_ENTRY = 25, PS_A_QPOLL = 26, PS_A_QSYNC = 27, PS_A_FRAG = 28, PS_A_LOOP = 29,
+                   PS_A_POST = 30, PS_A_FINISH = 31, PS_M_ML = 32, PS_M_W = 33, PS_M_O = 34,
+                   PS_A_END = 35, PS_EMBED = 36, PS_ARGMAX = 37, PS_A_LWAIT = 38, PS_G_SWAIT = 39,
+                   PS_MOE_ROUTE = 40, PS_TOTAL = 63 };
 
 enum TraceCode { TR_WAIT = 1, TR_READY = 2, TR_DONE = 3, TR_PIECE = 4, TR_MERGE = 5, TR_END = 6,
                  TR_P_STAGE = 11, TR_P_BLOCK = 12, TR_P_GO = 13,
@@ -107,11 +108,12 @@ enum TraceCode { TR_WAIT = 1, TR_READY = 2, TR_DONE = 3, TR_PIECE = 4, TR_MERGE 
 constexpr int kErrInvalid = 1, kErrBadPage = 5, kErrTimeout = 6, kErrInternal = 7;
 
 // stage ids (task id = layer * 16 + stage id)
-enum StageId { ST_QKV = 0, ST_ATTN = 1, ST_O = 2, ST_GU = 3, ST_DOWN = 4 };
-enum GemvKind { G_QKV = 0, G_O = 1, G_GU = 2, G_DOWN = 3, G_LM = 4 };
+enum StageId { ST_QKV = 0, ST_ATTN = 1, ST_O = 2, ST_GU = 3, ST_DOWN = 4, ST_ROUTE = 5 };
+enum GemvKind { G_QKV = 0, G_O = 1, G_GU = 2, G_DOWN = 3, G_LM = 4, G_ROUTE = 5 };
 
 struct LayerPlan {
     const bf16 *wq, *wk, *wv, *wo, *w_gate, *w_up, *w_down;
+    const bf16 *router, *exp_gate, *exp_up, *exp_down;  // MoE layers: [E][d], [E][Fe][d] x2, [E][d][Fe]
     const float *attn_gain, *mlp_gain;  // fp32, permuted column order
     int sliding;
     int pad_;
@@ -119,6 +121,8 @@ struct LayerPlan {
 
 struct Plan {
     int L, d, Hq, Hkv, hd, G, F, V, window, max_pos, maxB, num_pages;
+    int E, topk, Fe;                    // MoE: experts, routed per row, expert width (E = 0: dense)
+    int hrow;                           // row stride of the SwiGLU activations: max(F, E * Fe)
     float eps, scale;                   // scale = 1/sqrt(hd)
     int C;                              // CTAs in the launch
     int qkv_rows;                       // (Hq + 2 Hkv) * hd
@@ -131,7 +135,9 @@ struct Plan {
     uint64_t* x;                        // [maxB][d]  residual stream, permuted
     uint64_t* qkv;                      // [maxB][qkv_rows] natural order, pre-RoPE
     uint64_t* attn;                     // [maxB][Hq*hd] permuted
-    uint64_t* h;                        // [maxB][F] permuted
+    uint64_t* h;                        // [maxB][hrow] permuted (MoE: routed-weighted, by union slot)
+    uint64_t* route;                    // [maxB][E] router logits (MoE)
+    int* moe_union;                     // [L] experts in each layer's routed union, last step
     uint64_t* part;                     // [maxB*Hkv][C] records: o [G][hd], then (m, l) [G]
     // batches above kMaxTaggedBatch: x, attn, h as plain fp32 (same layouts), published
     // by per-stage counters with release / acquire ordering instead of tags
@@ -179,7 +185,7 @@ __device__ __forceinline__ int cnt_stage(int l, int s) { return 1 + l * kStagesP
 // Tags of the tagged-word writes: (epoch, layer, producer). Two consecutive writes of a
 // word never carry the same tag, so a stale word is never taken for the awaited one.
 enum TagCode { TAG_EMBED = 0, TAG_QKV = 1, TAG_PART = 2, TAG_ATTN = 3, TAG_O = 4, TAG_GU = 5,
-               TAG_DOWN = 6 };
+               TAG_DOWN = 6, TAG_ROUTE = 7 };
 __device__ __forceinline__ uint32_t tag_of(const StepArgs& a, int l, int code) {
     return (a.epoch << 12) | ((uint32_t)l << 3) | (uint32_t)code;
 }
@@ -202,6 +208,11 @@ struct Smem {
     volatile uint32_t lseq;  // ring slots the loader has started filling
     int pad_[5];
     __align__(16) LayerPlan lp[2];  // consumers' copies of the plans of layers l (l & 1) and l + 1
+    // MoE routing of the current layer, written by the consumers, read by the loader too
+    volatile int moe_ready;            // layer + 1 whose routing is below
+    int moe_nu;                        // experts in the union of the batch rows' routes
+    int moe_uni[kMaxExperts];          // that union, ascending expert id
+    float moe_w[kMaxBatch][kMaxExperts];  // routing weight of union slot j for row b (0: not routed)
 #ifdef MK_PROF
     unsigned long long prof[64];
 #endif
@@ -358,6 +369,12 @@ __device__ __forceinline__ void cta_rows(int R, int cta, int C, int& r0, int& r1
 
 struct GemvStage {
     int kind, layer, R, K, task_id;
+    int ldw;                     // elements between consecutive weight rows
+    int kcw;                     // columns per k-chunk (one ring slot holds 8 rows of a chunk)
+    int lds;                     // elements between source rows
+    int moe;                     // 0 dense; 1 MoE gate/up over the routed union; 2 MoE down
+    int Fe;                      // MoE expert width
+    const int* uni;              // MoE: the routed union (ascending expert id), in shared memory
     uint32_t src_tag, out_tag;   // tag awaited on every source word / written on the outputs
     const bf16 *w0, *w1, *w2;
     int split1, split2;          // QKV: row boundaries between wq / wk / wv
@@ -367,8 +384,9 @@ struct GemvStage {
     const float* gain;           // permuted fp32 gain or null (no norm)
 };
 
-// `lp` is layer l's plan (the consumers keep a copy in shared memory)
-__device__ GemvStage make_gemv(const StepArgs& a, int kind, int l, const LayerPlan& lp) {
+// `lp` is layer l's plan (the consumers keep a copy in shared memory); `sm` supplies the
+// routed union of a MoE layer (read only for its gate/up and down stages)
+__device__ GemvStage make_gemv(const StepArgs& a, int kind, int l, const LayerPlan& lp, const Smem* sm) {
     const Plan& p = a.p;
     GemvStage s;
     s.kind = kind;
@@ -377,10 +395,15 @@ __device__ GemvStage make_gemv(const StepArgs& a, int kind, int l, const LayerPl
     s.split1 = s.split2 = 0;
     s.gain = nullptr;
     s.out_tag = 0;
+    s.kcw = KCW;
+    s.moe = 0;
+    s.Fe = p.Fe;
+    s.uni = nullptr;
     if (kind == G_LM) {
         s.R = p.V; s.K = p.d; s.w0 = p.lm_head; s.src = p.x; s.srcf = p.xf; s.gain = p.final_gain;
         s.task_id = p.L * 16; s.src_tag = tag_of(a, p.L - 1, TAG_DOWN);
         s.cnt_wait = cnt_stage(p.L - 1, ST_DOWN); s.cnt_pub = -1;
+        s.ldw = s.lds = s.K;
         return s;
     }
     switch (kind) {
@@ -400,25 +423,46 @@ __device__ GemvStage make_gemv(const StepArgs& a, int kind, int l, const LayerPl
             s.out_tag = tag_of(a, l, TAG_O);
             s.cnt_wait = cnt_stage(l, ST_ATTN); s.cnt_pub = cnt_stage(l, ST_O);
             break;
+        case G_ROUTE:  // router logits of a MoE layer (always tagged words)
+            s.R = p.E; s.K = p.d; s.w0 = lp.router; s.src = p.x; s.srcf = p.xf;
+            s.gain = lp.mlp_gain; s.task_id = l * 16 + ST_ROUTE;
+            s.src_tag = tag_of(a, l, TAG_O);
+            s.out_tag = tag_of(a, l, TAG_ROUTE);
+            s.cnt_wait = cnt_stage(l, ST_O); s.cnt_pub = -1;
+            break;
         case G_GU:
-            s.R = p.F; s.K = p.d; s.w0 = lp.w_gate; s.w1 = lp.w_up; s.src = p.x; s.srcf = p.xf;
+            s.K = p.d; s.src = p.x; s.srcf = p.xf;
             s.gain = lp.mlp_gain; s.task_id = l * 16 + ST_GU;
             s.src_tag = tag_of(a, l, TAG_O);
             s.out_tag = tag_of(a, l, TAG_GU);
             s.cnt_wait = cnt_stage(l, ST_O); s.cnt_pub = cnt_stage(l, ST_GU);
+            if (p.E > 0) {  // rows = (union slot, expert row) pairs
+                s.moe = 1; s.uni = sm->moe_uni; s.R = sm->moe_nu * p.Fe;
+                s.w0 = lp.exp_gate; s.w1 = lp.exp_up;
+            } else {
+                s.R = p.F; s.w0 = lp.w_gate; s.w1 = lp.w_up;
+            }
             break;
         default:  // G_DOWN
-            s.R = p.d; s.K = p.F; s.w0 = lp.w_down; s.src = p.h; s.srcf = p.hf;
+            s.R = p.d; s.src = p.h; s.srcf = p.hf;
             s.task_id = l * 16 + ST_DOWN;
             s.src_tag = tag_of(a, l, TAG_GU);
             s.out_tag = tag_of(a, l, TAG_DOWN);
             s.cnt_wait = cnt_stage(l, ST_GU); s.cnt_pub = cnt_stage(l, ST_DOWN);
-            break;
+            if (p.E > 0) {  // k-chunk j = the Fe columns of union slot j's expert
+                s.moe = 2; s.uni = sm->moe_uni; s.K = sm->moe_nu * p.Fe;
+                s.w0 = lp.exp_down; s.kcw = p.Fe; s.ldw = p.Fe; s.lds = p.hrow;
+                return s;
+            }
+            s.K = p.F; s.w0 = lp.w_down;
+            s.ldw = s.K; s.lds = p.hrow;
+            return s;
     }
+    s.ldw = s.lds = s.K;
     return s;
 }
-__device__ __forceinline__ GemvStage make_gemv(const StepArgs& a, int kind, int l) {
-    return make_gemv(a, kind, l, a.p.layers[kind == G_LM ? 0 : l]);
+__device__ __forceinline__ GemvStage make_gemv(const StepArgs& a, int kind, int l, const Smem* sm) {
+    return make_gemv(a, kind, l, a.p.layers[kind == G_LM ? 0 : l], sm);
 }
 
 // stages whose individual ring slots are traced in MK_TRACE builds
@@ -438,25 +482,31 @@ __device__ __forceinline__ int group_rows(const GemvStage& s, int n, int gi, int
     const int base = kGroupRows * (s.kind == G_GU ? (gi % ngate) : gi);
     return min(kGroupRows, n - base);
 }
-// weight row i of row group gi, as a pointer to its first column
+// weight row i of row group gi, as a pointer to its first column (of k-chunk 0)
 __device__ __forceinline__ const bf16* gemv_row(const GemvStage& s, int r0, int gi, int ngate, int i) {
     if (s.kind == G_GU) {
         const bool up = gi >= ngate;
-        const int r = r0 + kGroupRows * (up ? gi - ngate : gi) + i;
-        return (up ? s.w1 : s.w0) + (size_t)r * s.K;
+        int r = r0 + kGroupRows * (up ? gi - ngate : gi) + i;
+        if (s.moe) r = s.uni[r / s.Fe] * s.Fe + r % s.Fe;  // (union slot, row) -> expert row
+        return (up ? s.w1 : s.w0) + (size_t)r * s.ldw;
     }
     const int r = r0 + kGroupRows * gi + i;
     if (s.kind == G_QKV) {
-        if (r < s.split1) return s.w0 + (size_t)r * s.K;
-        if (r < s.split2) return s.w1 + (size_t)(r - s.split1) * s.K;
-        return s.w2 + (size_t)(r - s.split2) * s.K;
+        if (r < s.split1) return s.w0 + (size_t)r * s.ldw;
+        if (r < s.split2) return s.w1 + (size_t)(r - s.split1) * s.ldw;
+        return s.w2 + (size_t)(r - s.split2) * s.ldw;
     }
-    return s.w0 + (size_t)r * s.K;
+    return s.w0 + (size_t)r * s.ldw;
+}
+// element offset of k-chunk k0 within a weight row: the column itself, or for the MoE
+// down projection the start of union slot k0 / Fe's expert matrix
+__device__ __forceinline__ size_t chunk_base(const GemvStage& s, int k0) {
+    return s.moe == 2 ? (size_t)s.uni[k0 / s.Fe] * s.R * s.Fe : (size_t)k0;
 }
 
 // Shared-memory geometry of one weight slot (8 rows x kc columns of k-chunk k0).
-// When a whole row fits in a chunk (K <= KCW), rpc consecutive rows travel in one
-// contiguous copy of up to 8 KB; otherwise each row segment is its own copy. Copies are
+// When a chunk is a whole weight row, rpc consecutive rows travel in one contiguous copy
+// of up to 8 KB; otherwise each row segment is its own copy. Copies are
 // 16 B apart so that 8 rows read by ldmatrix fall into distinct (or at most 2-way
 // shared) bank groups.
 struct SlotGeom {
@@ -465,12 +515,12 @@ struct SlotGeom {
         return (r >> rpc_log2) * cpitch + (r & (rpc - 1)) * rowb;
     }
 };
-__device__ __forceinline__ SlotGeom slot_geom(int K, int k0) {
+__device__ __forceinline__ SlotGeom slot_geom(const GemvStage& s, int k0) {
     SlotGeom g;
-    g.kc = min(KCW, K - k0);
+    g.kc = min(s.kcw, s.K - k0);
     int lg = 0;
-    if (K <= KCW) {
-        const int r = 4096 / K;
+    if (g.kc == s.ldw) {
+        const int r = 4096 / g.kc;
         lg = r >= 8 ? 3 : r >= 4 ? 2 : r >= 2 ? 1 : 0;
     }
     g.rpc_log2 = lg;
@@ -621,8 +671,9 @@ struct Producer {
             const int r1 = min(a1, r0 + tr);
             const int n = r1 - r0;
             const int ng = num_groups(s, n), ngate = s.kind == G_GU ? ng / 2 : ng;
-            for (int k0 = 0; k0 < s.K; k0 += KCW) {
-                const SlotGeom geo = slot_geom(s.K, k0);
+            for (int k0 = 0; k0 < s.K; k0 += s.kcw) {
+                const SlotGeom geo = slot_geom(s, k0);
+                const size_t cb = chunk_base(s, k0);
                 for (int gi = 0; gi < ng; ++gi) {
                     if (!acquire_slot(s.task_id)) return false;
                     const int nr = group_rows(s, n, gi, ngate);
@@ -633,14 +684,14 @@ struct Producer {
                     if (lane < ncop) {
                         const int i0 = lane * geo.rpc;
                         const int cnt = min(geo.rpc, nr - i0);
-                        const bf16* p0 = gemv_row(s, r0, gi, ngate, i0) + k0;
-                        const bf16* p1 = gemv_row(s, r0, gi, ngate, i0 + cnt - 1) + k0;
+                        const bf16* p0 = gemv_row(s, r0, gi, ngate, i0) + cb;
+                        const bf16* p1 = gemv_row(s, r0, gi, ngate, i0 + cnt - 1) + cb;
                         const uint32_t d0 = dst + lane * geo.cpitch;
-                        if (p1 == p0 + (size_t)(cnt - 1) * s.K) {
+                        if (p1 == p0 + (size_t)(cnt - 1) * s.ldw) {
                             copy(d0, p0, (uint32_t)(cnt * geo.kc * 2), bar);
                         } else {  // the rows straddle two weight tensors (q|k|v)
                             for (int i = 0; i < cnt; ++i)
-                                copy(d0 + i * geo.kc * 2, gemv_row(s, r0, gi, ngate, i0 + i) + k0,
+                                copy(d0 + i * geo.kc * 2, gemv_row(s, r0, gi, ngate, i0 + i) + cb,
                                      (uint32_t)(geo.kc * 2), bar);
                         }
                     }
@@ -701,6 +752,32 @@ struct Producer {
         return ok;
     }
 
+    // A MoE layer's expert rows depend on its routing, which this CTA's consumers compute
+    // from the router logits: wait until they publish it (bounded; on abort or time-out
+    // the loader stops, and the consumers report the cause).
+    __device__ bool wait_route(int l) {
+        int ok = 1;
+        if (lane == 0) {
+            uint64_t t0 = 0;
+            for (int it = 0; sm->moe_ready != l + 1; ++it) {
+                if (sm->abort) { ok = 0; break; }
+                __nanosleep(64);
+                if ((it & 63) == 63) {
+                    const uint64_t now = globaltimer();
+                    if (t0 == 0) t0 = now;
+                    else if ((long long)(now - t0) > 4 * a->timeout_ns) {
+                        if (!pf) set_error(a->p, sm, kErrTimeout, l * 16 + ST_ROUTE);
+                        ok = 0;
+                        break;
+                    }
+                }
+            }
+            __threadfence_block();
+        }
+        __syncwarp();
+        return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    }
+
     template <int HD>
     __device__ __noinline__ void run(int cta) {
         policy = policy_evict_first();
@@ -708,13 +785,17 @@ struct Producer {
         const Plan& p = a->p;
         bool ok = !sm->abort;
         for (int l = 0; l < p.L && ok; ++l) {
-            ok = ok && gemv(make_gemv(*a, G_QKV, l), cta);
+            ok = ok && gemv(make_gemv(*a, G_QKV, l, sm), cta);
             ok = ok && attention<HD>(l, cta);
-            ok = ok && gemv(make_gemv(*a, G_O, l), cta);
-            ok = ok && gemv(make_gemv(*a, G_GU, l), cta);
-            ok = ok && gemv(make_gemv(*a, G_DOWN, l), cta);
+            ok = ok && gemv(make_gemv(*a, G_O, l, sm), cta);
+            if (p.E > 0) {
+                ok = ok && gemv(make_gemv(*a, G_ROUTE, l, sm), cta);
+                ok = ok && wait_route(l);
+            }
+            ok = ok && gemv(make_gemv(*a, G_GU, l, sm), cta);
+            ok = ok && gemv(make_gemv(*a, G_DOWN, l, sm), cta);
         }
-        if (ok) gemv(make_gemv(*a, G_LM, 0), cta);
+        if (ok) gemv(make_gemv(*a, G_LM, 0, sm), cta);
         // drain: never leave a copy in flight into shared memory
         if (lane == 0 && !pf) {
             const uint32_t first = seq > (uint32_t)kStages ? seq - kStages : 0;
@@ -743,7 +824,7 @@ __device__ __forceinline__ void rms_scale(Ctx& c, const GemvStage& s) {
     for (int b = 0; b < a.B; ++b) {
         float ss = 0.f;
         if (tagged(a)) {
-            const uint64_t* row = s.src + (size_t)b * K;
+            const uint64_t* row = s.src + (size_t)b * s.lds;
             for (int k0 = c.tid * 2; k0 < K; k0 += kConsumerThreads * 8) {
                 uint64_t w[4][2];
                 Spin sp;
@@ -768,7 +849,7 @@ __device__ __forceinline__ void rms_scale(Ctx& c, const GemvStage& s) {
             }
         } else {
             for (int k = c.tid * 4; k < K; k += kConsumerThreads * 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(s.srcf + (size_t)b * K + k));
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(s.srcf + (size_t)b * s.lds + k));
                 ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             }
         }
@@ -854,13 +935,13 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
     auto issue = [&](int k0, uint64_t (&w)[BP][8]) {
         const int col = k0 + 8 * piece;
         const int base = (col & ~63) + 2 * ((col >> 3) & 7);  // permuted pair (t = 0)
-        const bool has = piece < (min(KCW, s.K - k0) >> 3);
+        const bool has = piece < (min(s.kcw, s.K - k0) >> 3);
 #pragma unroll
         for (int b = 0; b < BP; ++b)
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 w[b][2 * t] = w[b][2 * t + 1] = (uint64_t)s.src_tag << 32;
-                if (b < B && has) ll_ld2(s.src + (size_t)b * s.K + base + 16 * t, w[b][2 * t], w[b][2 * t + 1]);
+                if (b < B && has) ll_ld2(s.src + (size_t)b * s.lds + base + 16 * t, w[b][2 * t], w[b][2 * t + 1]);
             }
     };
     auto tags_ok = [&](const uint64_t (&w)[BP][8]) {
@@ -876,8 +957,8 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
     constexpr bool kAhead = BP == 1;
     uint64_t wn[BP][8];
     issue(0, wn);
-    for (int k0 = 0; k0 < s.K; k0 += KCW) {
-        const SlotGeom geo = slot_geom(s.K, k0);
+    for (int k0 = 0; k0 < s.K; k0 += s.kcw) {
+        const SlotGeom geo = slot_geom(s, k0);
         const bool has_p = piece < (geo.kc >> 3);
         float xv[BP][8];
         if (!kAhead && k0 > 0) issue(k0, wn);
@@ -891,7 +972,7 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
                 for (int q = 4 * BP - 1; q >= 0; --q)
                     if (ll_tag(wn[q >> 2][2 * (q & 3)]) != s.src_tag || ll_tag(wn[q >> 2][2 * (q & 3) + 1]) != s.src_tag)
                         miss = q;
-                if (!ll_wait_pair(s.src + (size_t)(miss >> 2) * s.K + base + 16 * (miss & 3), s.src_tag, sp, a,
+                if (!ll_wait_pair(s.src + (size_t)(miss >> 2) * s.lds + base + 16 * (miss & 3), s.src_tag, sp, a,
                                   c.sm, s.task_id))
                     break;
                 issue(k0, wn);
@@ -901,7 +982,7 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
         for (int b = 0; b < BP; ++b)
 #pragma unroll
             for (int i = 0; i < 8; ++i) xv[b][i] = (b < B && has_p) ? ll_val(wn[b][i]) : 0.f;
-        if (kAhead && k0 + KCW < s.K) issue(k0 + KCW, wn);
+        if (kAhead && k0 + s.kcw < s.K) issue(k0 + s.kcw, wn);
         const int col = k0 + 8 * piece;
         const int base = (col & ~63) + 2 * ((col >> 3) & 7);  // permuted pair (t = 0)
         if (s.gain) {
@@ -1047,12 +1128,20 @@ __device__ __forceinline__ void fma_epilogue(Ctx& c, const GemvStage& s, int r0,
             }
             break;
         }
-        default: {  // G_GU
+        case G_ROUTE:
+            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+                const int r = e / B, b = e % B;
+                const float y = ysum(r, b);
+                if (pub) ll_st(p.route + (size_t)b * p.E + r0 + r, y, s.out_tag);
+            }
+            break;
+        default: {  // G_GU (MoE: scaled by the row's routing weight of the union slot)
             const int up0 = kGroupRows * (num_groups(s, n) >> 1);
             for (int e = c.tid; e < n * B; e += kConsumerThreads) {
                 const int r = e / B, b = e % B;
-                const float y = silu(ysum(r, b)) * ysum(up0 + r, b);
-                if (pub) ll_st(p.h + (size_t)b * p.F + perm_col(r0 + r), y, s.out_tag);
+                float y = silu(ysum(r, b)) * ysum(up0 + r, b);
+                if (s.moe) y *= c.sm->moe_w[b][(r0 + r) / s.Fe];
+                if (pub) ll_st(p.h + (size_t)b * p.hrow + perm_col(r0 + r), y, s.out_tag);
             }
             break;
         }
@@ -1075,8 +1164,8 @@ __device__ __forceinline__ void gemv_mma(Ctx& c, const GemvStage& s, int r0, int
     // chunk X (second slot), 16-23 rows 0-7 chunk X+1, 24-31 rows 8-15 chunk X+1
     const int lrow = c.lane & 7, lhalf = (c.lane >> 3) & 1, lch = c.lane >> 4;
 
-    for (int k0 = 0; k0 < s.K; k0 += KCW) {
-        const SlotGeom geo = slot_geom(s.K, k0);
+    for (int k0 = 0; k0 < s.K; k0 += s.kcw) {
+        const SlotGeom geo = slot_geom(s, k0);
         const int nblk = geo.kc >> 6;
         uint32_t bfr[4][4][4];  // [block][k-step][hi b0b1, hi b2b3, lo b0b1, lo b2b3]
 #pragma unroll
@@ -1086,7 +1175,7 @@ __device__ __forceinline__ void gemv_mma(Ctx& c, const GemvStage& s, int r0, int
             for (int i = 0; i < 4; ++i) bfr[jj][i][0] = bfr[jj][i][1] = bfr[jj][i][2] = bfr[jj][i][3] = 0u;
             if (j < nblk && has_b && !c.sm->abort) {
                 const int col = k0 + 64 * j + 16 * t;
-                const float4* src = reinterpret_cast<const float4*>(s.srcf + (size_t)g * s.K + col);
+                const float4* src = reinterpret_cast<const float4*>(s.srcf + (size_t)g * s.lds + col);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     float4 v = __ldcg(src + i);
@@ -1206,12 +1295,20 @@ __device__ __forceinline__ void yout_epilogue(Ctx& c, const GemvStage& s, int r0
                 const int r = e / B, b = e % B;
                 const float yg = yout[r * 8 + b];
                 const float yu = yout[(up0 + r) * 8 + b];
-                const size_t o = (size_t)b * p.F + perm_col(r0 + r);
-                if (!tagged(a)) p.hf[o] = silu(yg) * yu;
-                else if (pub) ll_st(p.h + o, silu(yg) * yu, s.out_tag);
+                float y = silu(yg) * yu;
+                if (s.moe) y *= c.sm->moe_w[b][(r0 + r) / s.Fe];
+                const size_t o = (size_t)b * p.hrow + perm_col(r0 + r);
+                if (!tagged(a)) p.hf[o] = y;
+                else if (pub) ll_st(p.h + o, y, s.out_tag);
             }
             break;
         }
+        case G_ROUTE:
+            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+                const int r = e / B, b = e % B;
+                if (pub) ll_st(p.route + (size_t)b * p.E + r0 + r, yout[r * 8 + b], s.out_tag);
+            }
+            break;
         default: {  // G_LM: logits + running argmax (warp w handles batch row w)
             if (a.logits)
                 for (int e = c.tid; e < n * B; e += kConsumerThreads) {
@@ -1250,7 +1347,7 @@ template <int BP>
 __device__ __noinline__ void gemv_task_fma(Ctx& c_in, int kind, int layer, int r0, int r1) {
     Ctx c = c_in;
     const StepArgs& a = *c.a;
-    const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[layer & 1]);
+    const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[layer & 1], c.sm);
     const bool fused = fused_norm_stage(a, s);
     if (s.kind != G_LM) {
         gemv_fma<BP>(c, s, r0, r1, nullptr, fused);
@@ -1270,7 +1367,7 @@ __device__ __noinline__ void gemv_task_fma(Ctx& c_in, int kind, int layer, int r
 __device__ __noinline__ void gemv_task_mma(Ctx& c_in, int kind, int layer, int r0, int r1) {
     Ctx c = c_in;
     const StepArgs& a = *c.a;
-    const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[layer & 1]);
+    const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[layer & 1], c.sm);
     float* yout = c.scratch + kConsumerWarps * kTaskRows * 4;  // [128 vrows][8]
     gemv_mma(c, s, r0, r1, yout);
     consumer_sync();
@@ -1840,6 +1937,94 @@ __device__ void argmax_finish(Ctx& c, int cta) {
     }
 }
 
+// MoE routing of layer l (every CTA, identically): warp b polls row b's E router logits,
+// takes softmax probabilities p (max-subtracted), picks the top-k by p (lowest expert id
+// on ties) with weights p / sum of the picked p; then the union over the batch rows, in
+// ascending expert id, goes to shared memory for the consumers' and the loader's stages.
+// ("Kog Inference Engine", MoE paragraphs; the softmax-top-k reading of the router.)
+__device__ __noinline__ void moe_route(Ctx& c_in, int l) {
+    Ctx c = c_in;
+    const StepArgs& a = *c.a;
+    const Plan& p = a.p;
+    const int E = p.E, task = l * 16 + ST_ROUTE;
+    float* sel = c.scratch;  // [B][64]: routing weight by expert id, -1 = not routed
+    if (c.cw < a.B && !c.sm->abort) {
+        const int b = c.cw;
+        const uint32_t tag = tag_of(a, l, TAG_ROUTE);
+        const uint64_t* row = p.route + (size_t)b * E;
+        float v0 = -INFINITY, v1 = -INFINITY;
+        {
+            const int e0 = c.lane, e1 = c.lane + 32;
+            uint64_t w0 = (uint64_t)tag << 32, w1 = (uint64_t)tag << 32;
+            Spin sp;
+            for (;;) {
+                if (e0 < E) w0 = ll_ld(row + e0);
+                if (e1 < E) w1 = ll_ld(row + e1);
+                if ((ll_tag(w0) == tag && ll_tag(w1) == tag) || !sp.again(a, c.sm, task)) break;
+            }
+            if (e0 < E) v0 = ll_val(w0);
+            if (e1 < E) v1 = ll_val(w1);
+        }
+        float m = fmaxf(v0, v1);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float p0 = c.lane < E ? expf(v0 - m) : 0.f, p1 = c.lane + 32 < E ? expf(v1 - m) : 0.f;
+        float z = p0 + p1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        p0 /= z;
+        p1 /= z;
+        bool t0 = c.lane >= E, t1 = c.lane + 32 >= E;  // taken (or absent)
+        float picked = 0.f;
+        for (int i = 0; i < p.topk; ++i) {
+            float bv = -1.f;
+            int bi = 0x7fffffff;
+            if (!t0) { bv = p0; bi = c.lane; }
+            if (!t1 && p1 > bv) { bv = p1; bi = c.lane + 32; }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            }
+            if (bi == c.lane) t0 = true;
+            if (bi == c.lane + 32) t1 = true;
+            picked += bv;
+        }
+        sel[b * 64 + c.lane] = (c.lane < E && t0) ? p0 / picked : -1.f;
+        sel[b * 64 + c.lane + 32] = (c.lane + 32 < E && t1) ? p1 / picked : -1.f;
+    }
+    consumer_sync();
+    if (c.cw == 0) {
+        // union over the rows, ascending expert id: slot = rank among the routed ids
+        bool in0 = false, in1 = false;
+        for (int b = 0; b < a.B; ++b) {
+            in0 = in0 || sel[b * 64 + c.lane] >= 0.f;
+            in1 = in1 || sel[b * 64 + c.lane + 32] >= 0.f;
+        }
+        const uint32_t m0 = __ballot_sync(0xffffffffu, in0), m1 = __ballot_sync(0xffffffffu, in1);
+        const uint32_t below = (1u << c.lane) - 1u;
+        const int s0 = __popc(m0 & below), s1 = __popc(m0) + __popc(m1 & below);
+        if (in0) c.sm->moe_uni[s0] = c.lane;
+        if (in1) c.sm->moe_uni[s1] = c.lane + 32;
+        for (int b = 0; b < kMaxBatch; ++b) {
+            if (in0) c.sm->moe_w[b][s0] = b < a.B ? fmaxf(sel[b * 64 + c.lane], 0.f) : 0.f;
+            if (in1) c.sm->moe_w[b][s1] = b < a.B ? fmaxf(sel[b * 64 + c.lane + 32], 0.f) : 0.f;
+        }
+        if (c.lane == 0) {
+            c.sm->moe_nu = __popc(m0) + __popc(m1);
+            if (blockIdx.x == 0) p.moe_union[l] = __popc(m0) + __popc(m1);
+        }
+    }
+    consumer_sync();
+    MK_PROF_MARK(c, PS_MOE_ROUTE);
+    if (c.tid == 0) {
+        __threadfence_block();  // the routing above before the flag the loader waits on
+        c.sm->moe_ready = l + 1;
+    }
+    MK_PROF_BACK(c_in, c);
+}
+
 template <int HD>
 __device__ void consumer_run(Ctx& c, int cta) {
     const Plan& p = c.a->p;
@@ -1866,14 +2051,18 @@ __device__ void consumer_run(Ctx& c, int cta) {
         if (c.tid < kPlanChunks) cp_async_wait_all();
         consumer_sync();  // layer l's plan is in place; slot (l + 1) & 1 is free
         const LayerPlan& lp = c.sm->lp[l & 1];
-        gemv_stage(c, make_gemv(*c.a, G_QKV, l, lp), cta);
+        gemv_stage(c, make_gemv(*c.a, G_QKV, l, lp, c.sm), cta);
         if (l + 1 < p.L) fetch_plan(l + 1);  // read at the next layer, after a barrier
         attention_stage<HD>(c, l, cta);
-        gemv_stage(c, make_gemv(*c.a, G_O, l, lp), cta);
-        gemv_stage(c, make_gemv(*c.a, G_GU, l, lp), cta);
-        gemv_stage(c, make_gemv(*c.a, G_DOWN, l, lp), cta);
+        gemv_stage(c, make_gemv(*c.a, G_O, l, lp, c.sm), cta);
+        if (p.E > 0) {
+            gemv_stage(c, make_gemv(*c.a, G_ROUTE, l, lp, c.sm), cta);
+            moe_route(c, l);
+        }
+        gemv_stage(c, make_gemv(*c.a, G_GU, l, lp, c.sm), cta);
+        gemv_stage(c, make_gemv(*c.a, G_DOWN, l, lp, c.sm), cta);
     }
-    gemv_stage(c, make_gemv(*c.a, G_LM, 0, c.sm->lp[0]), cta);
+    gemv_stage(c, make_gemv(*c.a, G_LM, 0, c.sm->lp[0], c.sm), cta);
     argmax_finish(c, cta);
     MK_PROF_MARK(c, PS_ARGMAX);
 #ifdef MK_PROF
@@ -1898,6 +2087,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     if (threadIdx.x == 0) {
         sm->abort = 0;
         sm->lseq = 0;
+        sm->moe_ready = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm->full[s]), 1);
             mbar_init(smem_u32(&sm->empty[s]), kConsumerWarps);
