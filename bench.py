@@ -72,18 +72,28 @@ def profiled_traffic():
     return int(m_traffic.group(1))
 
 
-def algorithmic_bytes(cfg, batch, positions_per_layer_lo, positions):
-    """Bytes a decode step must move: every weight once (embedding: only the B rows),
-    the cached K/V rows attended (keys [lo, pos-1] per layer and row), the new K/V
+def algorithmic_bytes(cfg, batch, positions_per_layer_lo, positions, moe_union=None, kv_rows=None):
+    """Bytes a decode step must move: every weight once (embedding: only the B rows; a
+    MoE layer: its router and the experts in the union of the rows' routes, counts per
+    layer in `moe_union`), the cached K/V rows attended (keys [lo, pos-1] per layer and
+    row; `kv_rows` overrides the count, e.g. a shared prefix read once), the new K/V
     rows written, and the fp32 logits written."""
     d, hd, Hq, Hkv = cfg.d_model, cfg.head_dim, cfg.n_q_heads, cfg.n_kv_heads
-    per_layer = (Hq + 2 * Hkv) * hd * d + d * Hq * hd + 3 * cfg.ffn_dim * d + 2 * d
-    weights = 2 * (cfg.n_layers * per_layer + cfg.vocab * d + d + batch * d)
+    attn = (Hq + 2 * Hkv) * hd * d + d * Hq * hd + 2 * d
+    if cfg.is_moe:
+        experts = sum(cfg.n_experts * d + u * 3 * cfg.expert_ffn_dim * d for u in moe_union)
+        layer_params = cfg.n_layers * attn + experts
+    else:
+        layer_params = cfg.n_layers * (attn + 3 * cfg.ffn_dim * d)
+    weights = 2 * (layer_params + cfg.vocab * d + d + batch * d)
     row = 2 * Hkv * hd * 2  # K and V of one position, one layer
     kv_read = 0
-    for l in range(cfg.n_layers):
-        for b in range(batch):
-            kv_read += (positions[b] - positions_per_layer_lo[l][b]) * row
+    if kv_rows is not None:
+        kv_read = kv_rows * row
+    else:
+        for l in range(cfg.n_layers):
+            for b in range(batch):
+                kv_read += (positions[b] - positions_per_layer_lo[l][b]) * row
     kv_write = cfg.n_layers * batch * row
     return weights + kv_read + kv_write + batch * cfg.vocab * 4
 
@@ -302,6 +312,96 @@ def e2e_loop(S, cfg, steps, warmup):
     return B * steps / wall, h2d, d2h
 
 
+# ------------------------------------------------------------------ the other model configs
+def other_config(mk, local, name, B, ctx, steps, warmup, prefix_pages=0, private_pages=0):
+    """One more decode workload on its own seeded weights: B rows at context ~ctx (or
+    rows sharing a page-aligned prefix run), greedy tokens fed back on device. Returns
+    tokens/s, per-step time, and the achieved GB/s over the algorithmic bytes (a MoE
+    layer counts the experts of its measured routed union)."""
+    import torch
+    import synth
+    cfg = synth.CONFIGS[name]
+    dev = f"cuda:{local}"
+    seed = {"moe-64x768": 3, "dense-8b": 4 if not prefix_pages else 5}[name]
+    W = synth.make_weights(cfg, seed, device=dev)
+    rng = np.random.default_rng(seed)
+    total = warmup + steps
+    if prefix_pages:
+        npages = prefix_pages + B * private_pages + 2
+        maxp = prefix_pages + private_pages
+        pt = synth.prefix_shared_page_tables(rng, npages, B, prefix_pages, private_pages, maxp)
+        start = np.array([prefix_pages * 16 + 256 + 100 * b for b in range(B)], np.int64)
+    else:
+        per = (ctx + total + 15) // 16 + 1
+        npages = B * per + 2
+        pt = synth.random_page_tables(rng, npages, [per] * B, per)
+        start = np.full(B, ctx, np.int64)
+    model = mk.DecodeModel(cfg, W, npages, device=local)
+    synth.fill_normal_bf16_(model.kv(), seed + 100)
+    pos = torch.tensor(np.stack([start + t for t in range(total)]).astype(np.int32), device=dev)
+    toks = torch.zeros((total + 1, B), dtype=torch.int32, device=dev)
+    toks[0] = torch.tensor(synth.random_tokens(rng, cfg.vocab, B), device=dev)
+    ptd = torch.tensor(pt, device=dev)
+    sl = pos + 1
+
+    def run(t0, n, union_log=None):
+        for t in range(t0, t0 + n):
+            model.step(toks[t], pos[t], ptd, sl[t], toks[t + 1], None)
+            if union_log is not None:
+                ptr, nbytes = mk.mk_debug_buffer(model.handle, mk.MK_BUF_MOE_UNION)
+                src = torch.as_tensor(mk._CudaArray(ptr, (cfg.n_layers,), "<i4"), device=dev)
+                union_log[t - t0].copy_(src, non_blocking=True)
+
+    run(0, warmup)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    run(warmup, steps)
+    ev1.record()
+    torch.cuda.synchronize()
+    code, task = model.status()
+    if code != 0:
+        raise RuntimeError(f"{name} B={B} steps failed: status {code} task {task}")
+    ms = ev0.elapsed_time(ev1) / steps
+    unions = None
+    if cfg.is_moe:
+        # replay the same steps (same tokens, positions, pages: the same routing) and log
+        # each step's per-layer routed union
+        log = torch.zeros((steps, cfg.n_layers), dtype=torch.int32, device=dev)
+        run(warmup, steps, log)
+        torch.cuda.synchronize()
+        unions = log.cpu().numpy()
+    row = 2 * cfg.n_kv_heads * cfg.head_dim * 2
+    byts, naive = 0, 0
+    for i in range(steps):
+        p = [int(x) for x in pos[warmup + i].tolist()]
+        lo = [[0] * B for _ in range(cfg.n_layers)]
+        un = unions[i].tolist() if unions is not None else None
+        if prefix_pages:
+            shared = prefix_pages * 16
+            rows = cfg.n_layers * (shared + sum(x - shared for x in p))
+            byts += algorithmic_bytes(cfg, B, lo, p, un, kv_rows=rows)
+        else:
+            byts += algorithmic_bytes(cfg, B, lo, p, un)
+        naive += algorithmic_bytes(cfg, B, lo, p, un)
+    gbs = byts / steps / (ms / 1000.0) / 1e9
+    out = {"tokens_per_s": round(B * 1000.0 / ms, 2), "ms_per_step": round(ms, 4), "steps": steps,
+           "batch": B, "hbm_gbs": round(gbs, 1), "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+           "algorithmic_bytes_per_step": int(byts / steps)}
+    if prefix_pages:
+        out["naive_bytes_per_step"] = int(naive / steps)
+        out["workload"] = (f"{name}, batch {B} sharing a {prefix_pages * 16}-token prefix page run, "
+                           f"{private_pages * 16}-token private runs; prefix KV counted once in the bytes")
+    else:
+        out["workload"] = f"{name}, batch {B}, {ctx}-token seeded paged KV per row"
+    if unions is not None:
+        out["mean_routed_union_per_layer"] = round(float(unions.mean()), 2)
+    model.close()
+    del W
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ CPU baseline (oracle)
 def oracle_sample(cfg, W_cpu, kv_host, pt, budget_s=20.0, max_steps=16, B=1):
     """Times the CPU oracle, as it stands, on a bounded sample of the same workload:
@@ -380,6 +480,7 @@ def main():
     ap.add_argument("--no-batch8", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the MoE and 8B lines")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run the 2B shapes with this many layers")
     args = ap.parse_args()
@@ -482,6 +583,22 @@ def main():
                                      "2 sequences replaced by fresh 512-token contexts every 64 steps"}
         S8["model"].close()
         del S8
+    # the MoE and 8B configs (secondary lines; each on its own seeded weights)
+    if not args.no_extra:
+        del W
+        S["model"].close()
+        torch.cuda.empty_cache()
+        extra = {}
+        for key, kw in (("moe_b1", dict(name="moe-64x768", B=1, ctx=4096, steps=128)),
+                        ("moe_b8", dict(name="moe-64x768", B=8, ctx=4096, steps=128)),
+                        ("dense8b_b1", dict(name="dense-8b", B=1, ctx=32768, steps=128)),
+                        ("dense8b_b4_prefix", dict(name="dense-8b", B=4, ctx=0, steps=128,
+                                                   prefix_pages=1024, private_pages=64))):
+            extra[key] = other_config(mk, local, warmup=args.warmup, **kw)
+            extra[key]["frac_of_measured_peak"] = round(extra[key]["hbm_gbs"] / peak, 4)
+        out["other_configs"] = extra
+        W = synth.make_weights(cfg, 1, device=f"cuda:{local}")
+        S = setup_b1(cfg, W, local, total, mk)
     # end to end through host buffers
     if not args.no_e2e:
         e2e_steps = min(args.steps, 512)

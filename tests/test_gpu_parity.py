@@ -188,3 +188,28 @@ def test_dense2b_batch8_ragged_sliding(dense2b_weights):
     check_logits(g_lg, g_nx, o_lg, o_nx, what="2B b8")
     check_kv(pair)
     pair.close()
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_dense_8b_shapes_two_layers(B):
+    """The 8B decoder's shapes (d 4096: two k-chunks per row, so the norm statistics come
+    from a separate pass; 32/8 heads of 128; ffn 14336) with two layers. Batch 4 shares a
+    page-aligned prefix run, each row with private pages after it."""
+    cfg = synth.DENSE_8B.with_(n_layers=2, max_positions=2048)
+    npages = 40 + 8 * B
+    pair = Pair(cfg, seed=14, num_pages=npages, kv_seed=6)
+    rng = np.random.default_rng(14)
+    if B == 1:
+        pos = np.array([500], np.int32)
+        pt = synth.random_page_tables(rng, npages, [500 // 16 + 2], max_pages=500 // 16 + 2)
+    else:
+        prefix = 24  # 384 shared tokens
+        pt = synth.prefix_shared_page_tables(rng, npages, B, prefix, 4, max_pages=prefix + 4)
+        pos = (prefix * 16 + rng.integers(0, 48, size=B)).astype(np.int32)
+    toks = synth.random_tokens(rng, cfg.vocab, B)
+    for s in range(2):
+        g_lg, g_nx, o_lg, o_nx = pair.step(toks, pos + s, pt)
+        check_logits(g_lg, g_nx, o_lg, o_nx, what=f"B={B} step {s}")
+        toks = g_nx
+    check_kv(pair)
+    pair.close()
