@@ -102,7 +102,8 @@ enum TraceCode { TR_WAIT = 1, TR_READY = 2, TR_DONE = 3, TR_PIECE = 4, TR_MERGE 
                  TR_S_WAIT = 20, TR_S_FULL = 21, TR_S_REL = 22, TR_S_ISSUE = 23,
                  TR_A_Q = 30, TR_A_LOOP = 31, TR_A_PART = 32, TR_A_ARRIVED = 33, TR_A_MERGED = 34,
                  TR_G_NORM = 40, TR_G_X = 41, TR_G_SUM = 42, TR_G_EPI = 43,
-                 TR_Q_LOADED = 50, TR_Q_SYNCED = 51, TR_Q_FRAG = 52, TR_M_ML = 53, TR_M_W = 54, TR_M_O = 55 };
+                 TR_Q_LOADED = 50, TR_Q_SYNCED = 51, TR_Q_FRAG = 52, TR_M_ML = 53, TR_M_W = 54, TR_M_O = 55,
+                 TR_R_POLLED = 60, TR_R_DONE = 61 };
 
 // error codes (same values as mk_status)
 constexpr int kErrInvalid = 1, kErrBadPage = 5, kErrTimeout = 6, kErrInternal = 7;
@@ -207,6 +208,11 @@ struct Smem {
     int bcast;
     volatile uint32_t lseq;  // ring slots the loader has started filling
     int pad_[5];
+    // The step arguments, copied from the kernel parameters at entry: every field read
+    // during the step is then a shared-memory read. Reads of the parameters through a
+    // pointer were served from a cache the instruction stream of this large kernel keeps
+    // evicting, and cost a global round trip each (a routing pass of ~2 us took ~12 us).
+    StepArgs args;
     __align__(16) LayerPlan lp[2];  // consumers' copies of the plans of layers l (l & 1) and l + 1
     // MoE routing of the current layer, written by the consumers, read by the loader too
     volatile int moe_ready;            // layer + 1 whose routing is below
@@ -611,6 +617,7 @@ struct Producer {
     uint64_t policy;
     int lane;
     int tn = 0;  // trace events recorded (MK_TRACE builds)
+    const CUtensorMap* tmap;  // the KV tensor map, in the kernel parameters
     // Prefetch mode: the same schedule walked ahead of the loader, each copy replaced by
     // an L2 prefetch of its source, so that HBM keeps streaming while the consumers wait
     // on a dependency and the loader on a full ring. It never blocks anyone and never
@@ -741,8 +748,8 @@ struct Producer {
                 __syncwarp();
                 if (lane < nbox) {
                     const int row = (((l * p.num_pages + page) * 2 + kv) * p.Hkv + g) * kPage;
-                    if (pf) l2_prefetch_2d(&a->kv_tmap, bx * 64, row);
-                    else tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, &a->kv_tmap, bx * 64, row,
+                    if (pf) l2_prefetch_2d(tmap, bx * 64, row);
+                    else tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, tmap, bx * 64, row,
                                      bar, policy);
                 }
                 if (l == 1 && !pf) MK_TRACE_P(*this, TR_S_ISSUE, seq);
@@ -781,7 +788,7 @@ struct Producer {
     template <int HD>
     __device__ __noinline__ void run(int cta) {
         policy = policy_evict_first();
-        if (lane == 0) prefetch_tmap(&a->kv_tmap);
+        if (lane == 0) prefetch_tmap(tmap);
         const Plan& p = a->p;
         bool ok = !sm->abort;
         for (int l = 0; l < p.L && ok; ++l) {
@@ -1398,7 +1405,11 @@ __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
         if (s.gain && !fused_norm_stage(*c.a, s)) rms_scale(c, s);
         if (trace_slots(s)) MK_TRACE_C(c, TR_G_NORM, 0);
         const int tr = task_rows(s.kind);
-        for (int r0 = a0; r0 < a1; r0 += tr) gemv_task(c, s.kind, s.layer, r0, min(a1, r0 + tr));
+        for (int r0 = a0; r0 < a1; r0 += tr) {
+            // a task's epilogue reads every warp's partials; the next task clears them
+            if (r0 > a0) consumer_sync();
+            gemv_task(c, s.kind, s.layer, r0, min(a1, r0 + tr));
+        }
     }
     if (!tg && s.cnt_pub >= 0) publish(c, s.cnt_pub, s.task_id);
     else consumer_sync();  // every warp is done with the shared scratch of this stage
@@ -1965,6 +1976,7 @@ __device__ __noinline__ void moe_route(Ctx& c_in, int l) {
             if (e0 < E) v0 = ll_val(w0);
             if (e1 < E) v1 = ll_val(w1);
         }
+        if (l == 1) MK_TRACE_C(c, TR_R_POLLED, 0);
         float m = fmaxf(v0, v1);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -2018,10 +2030,12 @@ __device__ __noinline__ void moe_route(Ctx& c_in, int l) {
     }
     consumer_sync();
     MK_PROF_MARK(c, PS_MOE_ROUTE);
+    if (l == 1) MK_TRACE_C(c, TR_R_DONE, 0);
     if (c.tid == 0) {
         __threadfence_block();  // the routing above before the flag the loader waits on
         c.sm->moe_ready = l + 1;
     }
+    c_in.tn = c.tn;
     MK_PROF_BACK(c_in, c);
 }
 
@@ -2074,7 +2088,7 @@ __device__ void consumer_run(Ctx& c, int cta) {
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ StepArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ StepArgs a_param) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
@@ -2083,6 +2097,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     Smem* sm = reinterpret_cast<Smem*>(ring + kStages * kSlotBytes + kScratchBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
+    {
+        static_assert(sizeof(StepArgs) % 16 == 0, "step arguments copy in 16-byte pieces");
+        const uint4* src = reinterpret_cast<const uint4*>(&a_param);
+        uint4* dst = reinterpret_cast<uint4*>(&sm->args);
+        for (int i = threadIdx.x; i < (int)(sizeof(StepArgs) / 16); i += kThreads) dst[i] = src[i];
+    }
+    __syncthreads();
+    const StepArgs& a = sm->args;
 
     if (threadIdx.x == 0) {
         sm->abort = 0;
@@ -2116,6 +2138,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     if (warp == 0 || warp == kPrefetchWarp) {
         Producer pr;
         pr.a = &a;
+        pr.tmap = &a_param.kv_tmap;
         pr.sm = sm;
         pr.ring_s = smem_u32(ring);
         pr.lane = lane;

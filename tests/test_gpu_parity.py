@@ -213,3 +213,19 @@ def test_dense_8b_shapes_two_layers(B):
         toks = g_nx
     check_kv(pair)
     pair.close()
+
+
+def test_ffn_rows_span_several_tasks_per_cta():
+    """An FFN wide enough that each CTA's gate/up rows are cut into several GEMV tasks:
+    each task's epilogue reads all warps' partials before the next task clears them
+    (this once raced: the SwiGLU output was wrong in about 1 step in 4)."""
+    cfg = synth.TINY.with_(name="tiny-wide-ffn", ffn_dim=12288, n_layers=1)
+    pair = Pair(cfg, seed=15, num_pages=16, kv_seed=2)
+    rng = np.random.default_rng(15)
+    pt = synth.random_page_tables(rng, 16, [4], max_pages=4)
+    toks = synth.random_tokens(rng, cfg.vocab, 1)
+    for s in range(12):
+        g_lg, g_nx, o_lg, o_nx = pair.step(toks, [20 + s], pt)
+        check_logits(g_lg, g_nx, o_lg, o_nx, what=f"step {s}")
+        toks = g_nx
+    pair.close()
