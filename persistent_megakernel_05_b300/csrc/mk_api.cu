@@ -75,7 +75,7 @@ mk_status validate_desc(const mk_model_desc* d) {
     if (d->n_experts < 0 || d->n_experts > mk::kMaxExperts) return MK_ERR_INVALID_ARG;
     if (d->n_experts > 0) {
         // MoE: top-k of E experts, each a SwiGLU of width expert_ffn_dim (one k-chunk)
-        if (d->top_k < 1 || d->top_k > d->n_experts) return MK_ERR_INVALID_ARG;
+        if (d->top_k < 1 || d->top_k > d->n_experts || d->top_k > mk::kMaxTopK) return MK_ERR_INVALID_ARG;
         if (d->expert_ffn_dim < 64 || d->expert_ffn_dim % 64 || d->expert_ffn_dim > mk::KCW)
             return MK_ERR_INVALID_ARG;
     } else if (d->ffn_dim < 64 || d->ffn_dim % 64) {

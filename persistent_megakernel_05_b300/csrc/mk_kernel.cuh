@@ -55,6 +55,7 @@ constexpr int kPage = 16;
 constexpr int kTaskRows = 128;                     // <= 16 row groups of 8 per GEMV task
 constexpr int kMaxLayers = 128;
 constexpr int kMaxExperts = 64;                    // MoE: experts per layer (one warp routes a row)
+constexpr int kMaxTopK = 16;                       // MoE: experts routed per row
 constexpr int kCounterStride = 32;                 // u32 words per counter (128 B apart)
 constexpr int kStagesPerLayer = 8;                 // counter slots per layer
 constexpr int kMaxOwnRows = 32;                    // residual rows a CTA owns: ceil(d / CTAs) <= 32
@@ -1959,8 +1960,11 @@ __device__ __noinline__ void moe_route(Ctx& c_in, int l) {
     const Plan& p = a.p;
     const int E = p.E, task = l * 16 + ST_ROUTE;
     float* sel = c.scratch;  // [B][64]: routing weight by expert id, -1 = not routed
-    if (c.cw < a.B && !c.sm->abort) {
-        const int b = c.cw;
+    // Every warp routes a row (warp w takes row w mod B; only the first B warps write).
+    // A lone routing warp next to warps parked at a CTA barrier ran ~8x slower.
+    if (!c.sm->abort) {
+        const int b = c.cw % a.B;
+        const bool writer = c.cw < a.B;
         const uint32_t tag = tag_of(a, l, TAG_ROUTE);
         const uint64_t* row = p.route + (size_t)b * E;
         float v0 = -INFINITY, v1 = -INFINITY;
@@ -1986,25 +1990,32 @@ __device__ __noinline__ void moe_route(Ctx& c_in, int l) {
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         p0 /= z;
         p1 /= z;
-        bool t0 = c.lane >= E, t1 = c.lane + 32 >= E;  // taken (or absent)
-        float picked = 0.f;
-        for (int i = 0; i < p.topk; ++i) {
-            float bv = -1.f;
-            int bi = 0x7fffffff;
-            if (!t0) { bv = p0; bi = c.lane; }
-            if (!t1 && p1 > bv) { bv = p1; bi = c.lane + 32; }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-            if (bi == c.lane) t0 = true;
-            if (bi == c.lane + 32) t1 = true;
-            picked += bv;
+        // (a shuffle-chain selection ran several times slower here than standalone)
+        float* pw = c.scratch + 8 * 64 + c.cw * 64;             // this warp's p, by expert
+        int* ids = reinterpret_cast<int*>(c.scratch + 16 * 64) + c.cw * kMaxTopK;
+        // Top-k by rank: an expert's rank is the number of experts ahead of it (larger p,
+        // or equal p and a lower id); it is picked when its rank is below k. The picked
+        // p are then summed in rank order, the order in which a greedy selection takes them.
+        pw[c.lane] = c.lane < E ? p0 : -1.f;
+        pw[c.lane + 32] = c.lane + 32 < E ? p1 : -1.f;
+        __syncwarp();
+        int r0 = 0, r1 = 0;
+        for (int e = 0; e < E; ++e) {
+            const float v = pw[e];
+            r0 += (v > p0 || (v == p0 && e < c.lane)) ? 1 : 0;
+            r1 += (v > p1 || (v == p1 && e < c.lane + 32)) ? 1 : 0;
         }
-        sel[b * 64 + c.lane] = (c.lane < E && t0) ? p0 / picked : -1.f;
-        sel[b * 64 + c.lane + 32] = (c.lane + 32 < E && t1) ? p1 / picked : -1.f;
+        const int topk = p.topk;
+        const bool t0 = c.lane < E && r0 < topk, t1 = c.lane + 32 < E && r1 < topk;
+        if (t0) ids[r0] = c.lane;
+        if (t1) ids[r1] = c.lane + 32;
+        __syncwarp();
+        float picked = 0.f;
+        for (int r = 0; r < topk; ++r) picked += pw[ids[r]];
+        if (writer) {
+            sel[b * 64 + c.lane] = (c.lane < E && t0) ? p0 / picked : -1.f;
+            sel[b * 64 + c.lane + 32] = (c.lane + 32 < E && t1) ? p1 / picked : -1.f;
+        }
     }
     consumer_sync();
     if (c.cw == 0) {
