@@ -76,6 +76,12 @@ def lib():
         L.or_route.argtypes = [_f32p, ctypes.c_int32, ctypes.c_int32, _i32p, _f32p]
         L.or_argmax.restype = ctypes.c_int32
         L.or_argmax.argtypes = [_f32p, ctypes.c_int32]
+        L.or_philox4x32_10.argtypes = [_P(ctypes.c_uint32), _P(ctypes.c_uint32), _P(ctypes.c_uint32)]
+        L.or_gumbel.restype = ctypes.c_float
+        L.or_gumbel.argtypes = [ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+        L.or_sample_gumbel.restype = ctypes.c_int32
+        L.or_sample_gumbel.argtypes = [_f32p, ctypes.c_int32, ctypes.c_float, ctypes.c_uint64,
+                                       ctypes.c_int32, ctypes.c_int32]
         L.or_matvec.argtypes = [_u16p, _f32p, ctypes.c_int32, ctypes.c_int32, _f32p]
         L.or_f32_to_bf16.restype = ctypes.c_uint16
         L.or_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -148,9 +154,11 @@ class OracleModel:
         self.m = m
 
     def decode_step(self, kv: np.ndarray, tokens, positions, page_table, seq_lens,
-                    nthreads: Optional[int] = None):
+                    nthreads: Optional[int] = None, temperature: float = 0.0, seed: int = 0):
         """One decode step; appends into ``kv`` (uint16, pool layout) in place.
-        Returns (logits [B, vocab] float32, next_tokens [B] int32)."""
+        Returns (logits [B, vocab] float32, next_tokens [B] int32). temperature > 0
+        samples the next tokens from softmax(logits / T) (Gumbel-max, Philox draws keyed
+        by ``seed``, counter (token, position, row)); else greedy."""
         cfg = self.cfg
         assert kv.dtype == np.uint16 and kv.flags.c_contiguous
         num_pages = kv.shape[1]
@@ -168,6 +176,9 @@ class OracleModel:
                                   _ptr(nxt, _i32p), nthreads or default_threads())
         if rc != 0:
             raise ValueError(f"oracle decode_step returned {rc}")
+        if temperature > 0.0:  # Gumbel-max sampling from softmax(logits / T)
+            for b in range(B):
+                nxt[b] = sample_gumbel(logits[b], temperature, seed, int(positions[b]), b)
         return logits, nxt
 
     def forward_full(self, tokens, nthreads: Optional[int] = None) -> np.ndarray:
@@ -234,3 +245,21 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     x = _c(x, np.float32).ravel()
     f = lib().or_f32_to_bf16
     return np.array([f(float(v)) for v in x], np.uint16)
+
+
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 block: four 32-bit counter words, two key words -> four words."""
+    c = (ctypes.c_uint32 * 4)(*[int(x) & 0xFFFFFFFF for x in ctr])
+    k = (ctypes.c_uint32 * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+    o = (ctypes.c_uint32 * 4)()
+    lib().or_philox4x32_10(c, k, o)
+    return [int(x) for x in o]
+
+
+def gumbel(seed: int, token: int, pos: int, row: int) -> float:
+    return float(lib().or_gumbel(seed, token, pos, row))
+
+
+def sample_gumbel(logits, temperature: float, seed: int, pos: int, row: int) -> int:
+    v = _c(logits, np.float32)
+    return int(lib().or_sample_gumbel(_ptr(v, _f32p), v.shape[0], temperature, seed, pos, row))

@@ -28,7 +28,8 @@
  * attention special cases (single key, uniform scores, one-hot), agreement with an
  * independent float64 NumPy twin and with torch library routines (rms_norm,
  * scaled_dot_product_attention with GQA, silu), cached decode == full recompute,
- * paged == contiguous, page-permutation invariance, MoE reductions, argmax ties.
+ * paged == contiguous, page-permutation invariance, MoE reductions, argmax ties,
+ * Philox4x32-10 known-answer vectors, Gumbel-max sample frequencies = softmax(z / T).
  */
 #include <math.h>
 #include <stdint.h>
@@ -169,6 +170,54 @@ void or_route(const float *logits, int32_t E, int32_t k, int32_t *ids, float *w)
     for (int32_t i = 0; i < k; i++) w[i] = w[i] / sel;
     free(p);
     free(taken);
+}
+
+/* ---------- temperature sampling (Gumbel-max over a counter-based generator) ----------
+ * Sampling from softmax(logits / T) equals taking argmax_i (logits_i / T + g_i) with g_i
+ * independent standard Gumbel draws, g = -log(-log u), u uniform on (0, 1). The draws
+ * come from Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+ * as 1, 2, 3", SC 2011), keyed by the 64-bit seed, with counter (token id, position,
+ * batch row, 0): no state, so the kernel and this oracle draw the same u for the same
+ * (seed, position, row, token). u = (top 24 bits of word 0 + 0.5) / 2^24, in fp32. */
+void or_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int r = 0; r < 10; r++) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0, p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+float or_gumbel(uint64_t seed, int32_t token, int32_t pos, int32_t row) {
+    const uint32_t ctr[4] = {(uint32_t)token, (uint32_t)pos, (uint32_t)row, 0u};
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t o[4];
+    or_philox4x32_10(ctr, key, o);
+    const float u = ((float)(o[0] >> 8) + 0.5f) * (1.0f / 16777216.0f);
+    return -logf(-logf(u));
+}
+
+/* index of the largest logits_i / T + g_i (lowest index on ties) */
+int32_t or_sample_gumbel(const float *logits, int32_t n, float temperature, uint64_t seed, int32_t pos,
+                         int32_t row) {
+    int32_t best = 0;
+    float bv = -INFINITY;
+    for (int32_t i = 0; i < n; i++) {
+        const float z = logits[i] / temperature + or_gumbel(seed, i, pos, row);
+        if (z > bv) { bv = z; best = i; }
+    }
+    return best;
 }
 
 /* Greedy: index of the largest value, the lowest index among equal maxima. */

@@ -413,3 +413,40 @@ def test_oracle_rejects_bad_inputs(tiny_run):
         om.decode_step(kv, [1], [3], pt, [3])               # seq_len != pos + 1
     with pytest.raises(ValueError):
         om.decode_step(kv, [1], [3], np.array([[9, 1]], np.int32), [4])  # bad page id
+
+
+# ---------------------------------------------------------------- temperature sampling
+def test_philox4x32_10_known_answer_vectors():
+    """Philox4x32-10 (Salmon et al., SC 2011): the published known-answer vectors."""
+    assert oracle.philox4x32_10([0, 0, 0, 0], [0, 0]) == [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
+    f = 0xFFFFFFFF
+    assert oracle.philox4x32_10([f, f, f, f], [f, f]) == [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]
+    assert oracle.philox4x32_10([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344],
+                                [0xA4093822, 0x299F31D0]) == [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]
+
+
+def test_gumbel_draws_have_the_standard_gumbel_moments():
+    """mean = Euler-Mascheroni constant, variance = pi^2 / 6."""
+    g = np.array([oracle.gumbel(7, t, 3, 0) for t in range(40000)])
+    assert abs(g.mean() - 0.5772156649) < 0.03
+    assert abs(g.var() - np.pi ** 2 / 6) < 0.08
+
+
+def test_gumbel_max_samples_follow_softmax_over_temperature():
+    """argmax(z / T + Gumbel) is an exact draw from softmax(z / T): empirical frequencies
+    over many counters match it."""
+    z = np.array([1.0, 0.2, -0.5, 0.9, 0.0], np.float32)
+    for T in (0.7, 1.5):
+        n = 20000
+        counts = np.zeros(len(z))
+        for pos in range(n):
+            counts[oracle.sample_gumbel(z, T, 11, pos, 2)] += 1
+        p = np.exp(z / T) / np.exp(z / T).sum()
+        assert np.abs(counts / n - p).max() < 0.015, (T, counts / n, p)
+
+
+def test_gumbel_max_at_tiny_temperature_is_the_argmax():
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        z = rng.normal(size=300).astype(np.float32)
+        assert oracle.sample_gumbel(z, 1e-4, 3, 17, 0) == int(np.argmax(z))
