@@ -182,6 +182,16 @@ typedef enum mk_option {
 } mk_option;
 MK_API mk_status mk_set_option(mk_handle *h, mk_option opt, int64_t value);
 
+/* Next-token rule from the next step on. temperature == 0 (the default): greedy argmax
+ * (lowest index on ties). temperature > 0: a draw from softmax(logits / temperature),
+ * taken as argmax_i (logits_i / temperature + g_i) with g_i = -log(-log u_i) standard
+ * Gumbel noise; u_i comes from Philox4x32-10 with key = seed (low word first) and counter
+ * (token i, positions[b], row b, 0), u = (top 24 bits of word 0 + 0.5) / 2^24. The draw is
+ * a function of (seed, position, row, token) only, so a step can be replayed exactly.
+ * The logits written by mk_decode_step stay the raw logits. Negative or non-finite
+ * temperatures: MK_ERR_INVALID_ARG. mk_decode_step_noalloc is always greedy. */
+MK_API mk_status mk_set_sampling(mk_handle *h, float temperature, uint64_t seed);
+
 /* Read-only facts about a handle (for schedulers and benchmarks). */
 typedef struct mk_info {
     int32_t num_ctas;          /* persistent CTAs per launch (one per SM) */

@@ -79,6 +79,8 @@ def lib():
         L.or_philox4x32_10.argtypes = [_P(ctypes.c_uint32), _P(ctypes.c_uint32), _P(ctypes.c_uint32)]
         L.or_gumbel.restype = ctypes.c_float
         L.or_gumbel.argtypes = [ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+        L.or_gumbel_scores.argtypes = [_f32p, ctypes.c_int32, ctypes.c_float, ctypes.c_uint64,
+                                       ctypes.c_int32, ctypes.c_int32, _f32p]
         L.or_sample_gumbel.restype = ctypes.c_int32
         L.or_sample_gumbel.argtypes = [_f32p, ctypes.c_int32, ctypes.c_float, ctypes.c_uint64,
                                        ctypes.c_int32, ctypes.c_int32]
@@ -258,6 +260,14 @@ def philox4x32_10(ctr, key):
 
 def gumbel(seed: int, token: int, pos: int, row: int) -> float:
     return float(lib().or_gumbel(seed, token, pos, row))
+
+
+def gumbel_scores(logits, temperature: float, seed: int, pos: int, row: int) -> np.ndarray:
+    """logits / T + the Gumbel draw of every token (their argmax is the sampled token)."""
+    v = _c(logits, np.float32)
+    z = np.empty_like(v)
+    lib().or_gumbel_scores(_ptr(v, _f32p), v.shape[0], temperature, seed, pos, row, _ptr(z, _f32p))
+    return z
 
 
 def sample_gumbel(logits, temperature: float, seed: int, pos: int, row: int) -> int:

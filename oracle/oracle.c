@@ -208,6 +208,12 @@ float or_gumbel(uint64_t seed, int32_t token, int32_t pos, int32_t row) {
     return -logf(-logf(u));
 }
 
+/* z_i = logits_i / T + g_i for every token i */
+void or_gumbel_scores(const float *logits, int32_t n, float temperature, uint64_t seed, int32_t pos,
+                      int32_t row, float *z) {
+    for (int32_t i = 0; i < n; i++) z[i] = logits[i] / temperature + or_gumbel(seed, i, pos, row);
+}
+
 /* index of the largest logits_i / T + g_i (lowest index on ties) */
 int32_t or_sample_gumbel(const float *logits, int32_t n, float temperature, uint64_t seed, int32_t pos,
                          int32_t row) {

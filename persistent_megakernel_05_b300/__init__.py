@@ -33,7 +33,7 @@ MK_OPT_PREFETCH_SLOTS = 3
 # exported symbols of include/mk.h
 ABI_SYMBOLS = ("mk_create", "mk_kv_alloc", "mk_kv_free", "mk_decode_step", "mk_status_sync",
                "mk_status_reset", "mk_set_option", "mk_get_info", "mk_debug_buffer",
-               "mk_status_string", "mk_destroy", "mk_decode_step_noalloc")
+               "mk_status_string", "mk_destroy", "mk_decode_step_noalloc", "mk_set_sampling")
 MK_NOALLOC_SCRATCH_BYTES = 8 << 20
 MK_BUF_X, MK_BUF_QKV, MK_BUF_ATTN, MK_BUF_H, MK_BUF_ROUTE, MK_BUF_MOE_UNION = 1, 2, 3, 4, 5, 6
 
@@ -113,6 +113,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mk_status_reset.argtypes = [_vp]
     L.mk_set_option.restype = ctypes.c_int
     L.mk_set_option.argtypes = [_vp, ctypes.c_int, i64]
+    L.mk_set_sampling.restype = ctypes.c_int
+    L.mk_set_sampling.argtypes = [_vp, ctypes.c_float, ctypes.c_uint64]
     L.mk_get_info.restype = ctypes.c_int
     L.mk_get_info.argtypes = [_vp, _P(mk_info)]
     L.mk_debug_buffer.restype = ctypes.c_int
@@ -179,6 +181,11 @@ def mk_status_reset(handle: int):
 
 def mk_set_option(handle: int, opt: int, value: int):
     _check(load().mk_set_option(handle, opt, int(value)), "mk_set_option")
+
+
+def mk_set_sampling(handle: int, temperature: float, seed: int):
+    _check(load().mk_set_sampling(handle, float(temperature), int(seed) & (2 ** 64 - 1)),
+           "mk_set_sampling")
 
 
 def mk_get_info(handle: int) -> mk_info:
@@ -328,6 +335,10 @@ class DecodeModel:
 
     def set_option(self, opt: int, value: int):
         mk_set_option(self.handle, opt, value)
+
+    def set_sampling(self, temperature: float, seed: int = 0):
+        """temperature 0: greedy; > 0: draw from softmax(logits / temperature)."""
+        mk_set_sampling(self.handle, temperature, seed)
 
     def close(self):
         if getattr(self, "handle", None):

@@ -33,6 +33,8 @@ struct mk_handle {
     uint32_t epoch = 0;             // tag epoch of the last step (1 .. 2^20 - 1, cycling)
     uint32_t cnt_epoch = 0;         // steps since the counters were last zeroed
     int last_batch = 0;             // batch of the last step (selects the activation format)
+    float temperature = 0.f;        // next-token rule: 0 greedy, > 0 Gumbel-max sampling
+    uint64_t seed = 0;
     long long timeout_ns = 1000000000LL;
     int skip_publish = -1;
     int prefetch_slots = mk::kDefaultPrefetchSlots;
@@ -424,6 +426,9 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
     a.skip_publish = h->skip_publish;
     a.prefetch_slots = h->prefetch_slots;
     a.timeout_ns = h->timeout_ns;
+    a.temperature = h->temperature;
+    a.seed_lo = (uint32_t)h->seed;
+    a.seed_hi = (uint32_t)(h->seed >> 32);
     void* args[] = {&a};
     const void* fn = h->hd == 128 ? (const void*)mk::decode_step_kernel<128>
                                   : (const void*)mk::decode_step_kernel<64>;
@@ -489,6 +494,13 @@ mk_status mk_set_option(mk_handle* h, mk_option opt, int64_t value) {
             return MK_OK;
     }
     return MK_ERR_INVALID_ARG;
+}
+
+mk_status mk_set_sampling(mk_handle* h, float temperature, uint64_t seed) {
+    if (!h || !std::isfinite(temperature) || temperature < 0.f) return MK_ERR_INVALID_ARG;
+    h->temperature = temperature;
+    h->seed = seed;
+    return MK_OK;
 }
 
 mk_status mk_get_info(const mk_handle* h, mk_info* out) {
@@ -786,6 +798,8 @@ extern "C" mk_status mk_decode_step_noalloc(
     a.skip_publish = -1;
     a.prefetch_slots = mk::kDefaultPrefetchSlots;
     a.timeout_ns = 1000000000LL;
+    a.temperature = 0.f;  // greedy
+    a.seed_lo = a.seed_hi = 0;
     void* args[] = {&a};
     const void* fn = hd == 128 ? (const void*)mk::decode_step_kernel<128>
                                : (const void*)mk::decode_step_kernel<64>;

@@ -169,6 +169,8 @@ struct StepArgs {
     int B;
     uint32_t epoch;                     // step number mod 2^20, never 0: high bits of every tag
     uint32_t stage_target;              // counter target of every stage: steps since reset * C
+    float temperature;                  // 0: greedy; > 0: Gumbel-max sampling
+    uint32_t seed_lo, seed_hi;          // Philox key of the sampling draws
     int skip_publish;                   // task id whose outputs are never written, or -1
     int prefetch_slots;                 // L2 prefetch lead over the loader, in slots (0 = off)
     long long timeout_ns;
@@ -875,6 +877,35 @@ __device__ __forceinline__ void rms_scale(Ctx& c, const GemvStage& s) {
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC 2011), word 0 of the output block: the
+// counter-based generator of the sampling draws (no state; the same value for the same
+// (key, counter) on any thread, CTA or step).
+__device__ __forceinline__ uint32_t philox4x32_10_w0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                     uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return c0;
+}
+// logit / T + standard Gumbel draw for (token, position, row): the value whose argmax
+// is a draw from softmax(logits / T)
+__device__ __forceinline__ float gumbel_score(const StepArgs& a, float logit, int token, int pos, int row) {
+    const uint32_t x = philox4x32_10_w0((uint32_t)token, (uint32_t)pos, (uint32_t)row, 0u, a.seed_lo, a.seed_hi);
+    const float u = ((float)(x >> 8) + 0.5f) * (1.0f / 16777216.0f);
+    return logit / a.temperature - logf(-logf(u));
+}
 __device__ __forceinline__ int cta_of(const Ctx&) { return blockIdx.x; }
 
 // the small-batch path computes the RMSNorm statistics from its own activation loads
@@ -1325,10 +1356,13 @@ __device__ __forceinline__ void yout_epilogue(Ctx& c, const GemvStage& s, int r0
                 }
             if (c.cw < B) {
                 const int b = c.cw;
+                const bool sample = a.temperature > 0.f;
+                const int pos = c.sm->pos[b];
                 float bv = -INFINITY;
                 int bi = 0x7fffffff;
                 for (int r = c.lane; r < n; r += 32) {
-                    const float v = yout[r * 8 + b];
+                    float v = yout[r * 8 + b];
+                    if (sample) v = gumbel_score(a, v, r0 + r, pos, b);
                     if (v > bv) { bv = v; bi = r0 + r; }
                 }
 #pragma unroll

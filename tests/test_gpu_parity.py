@@ -229,3 +229,36 @@ def test_ffn_rows_span_several_tasks_per_cta():
         check_logits(g_lg, g_nx, o_lg, o_nx, what=f"step {s}")
         toks = g_nx
     pair.close()
+
+
+def test_temperature_sampling_draws_match_the_oracle():
+    """Temperature sampling (Gumbel-max over Philox draws keyed by seed, counter = token,
+    position, row): the kernel's token is the oracle's draw wherever the oracle's top-2
+    scores differ by more than 0.1; the logits output stays the raw logits."""
+    import oracle
+    cfg = synth.TINY
+    T, seed = 0.8, 0x1234ABCD5678
+    pair = Pair(cfg, seed=16, num_pages=32, kv_seed=4)
+    pair.gpu.set_sampling(T, seed)
+    rng = np.random.default_rng(16)
+    B = 3
+    pos = np.array([5, 40, 77], np.int32)
+    pages = [int(p) // 16 + 2 for p in pos]
+    pt = synth.random_page_tables(rng, 32, pages, max_pages=max(pages))
+    toks = synth.random_tokens(rng, cfg.vocab, B)
+    compared = differs = 0
+    for s in range(10):
+        g_lg, g_nx, o_lg, o_nx = pair.step(toks, pos + s, pt)
+        assert np.abs(g_lg - o_lg).max() <= 3e-2
+        for b in range(B):
+            z = oracle.gumbel_scores(o_lg[b], T, seed, int(pos[b] + s), b)
+            top2 = np.partition(z, -2)[-2:]
+            if top2[1] - top2[0] > 0.1:
+                assert g_nx[b] == int(np.argmax(z)), (s, b)
+                compared += 1
+            differs += int(g_nx[b] != int(np.argmax(g_lg[b])))
+        toks = g_nx
+    assert compared >= 20
+    assert differs > 0  # at T = 0.8 some draws are not the greedy token
+    pair.gpu.set_sampling(0.0, 0)
+    pair.close()
