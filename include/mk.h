@@ -5,8 +5,10 @@
  * transformer LM for 1..8 sequences as ONE persistent CUDA kernel: RMSNorm, QKV
  * projection, RoPE, paged-KV GQA attention (optionally sliding-window), output
  * projection + residual, SwiGLU MLP or softmax-top-k MoE, final norm, LM head and
- * greedy argmax. Work is a task graph of GEMV row tiles and attention key splits,
- * ordered by dependency counters instead of grid-wide barriers.
+ * greedy argmax (or temperature sampling, mk_set_sampling). Work is a task graph of
+ * GEMV row tiles and attention key splits, ordered by the data instead of grid-wide
+ * barriers: up to batch 4 every stage output is a tagged word its readers poll; above
+ * that, per-stage dependency counters.
  *
  * Source of the operation (pages, by title and section):
  *   "Cohere, Megakernel sunum sistemini acik kaynak yapti", section
@@ -124,7 +126,8 @@ typedef struct mk_kv_pool {
 /* Creates a handle on `device`: checks the GPU (sm_103, cooperative launch),
  * copies the descriptor, records the weight pointers, uploads the RoPE table
  * (cos/sin computed on the host in double), and allocates the step scratch
- * (activations, attention partials, dependency counters, status word).
+ * (activations, attention partials, dependency counters, status word; the KV tensor
+ * map is made by mk_kv_alloc).
  * Returns MK_ERR_INVALID_ARG for an unsupported shape, MK_ERR_NO_DEVICE /
  * MK_ERR_UNSUPPORTED_DEVICE for the GPU checks, MK_ERR_OOM if scratch cannot be
  * allocated. On error *out is NULL and nothing is leaked. */
@@ -211,7 +214,7 @@ MK_API mk_status mk_get_info(const mk_handle *h, mk_info *out);
  * input and output themselves, including the KV pool.
  *
  * All scratch (norm gains, RoPE table, layer table, activations, attention partials,
- * dependency counters, status word, KV tensor map) lives in one file-scope static
+ * dependency counters, status word) lives in one file-scope static
  * device array of MK_NOALLOC_SCRATCH_BYTES (8 MiB), which every GPU that loads this
  * library holds until the process exits. Descriptors whose scratch does not fit
  * (roughly: max_batch * n_kv_heads * 148 * (n_q_heads/n_kv_heads) * head_dim * 4 bytes

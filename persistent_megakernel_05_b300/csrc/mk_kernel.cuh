@@ -1504,8 +1504,8 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, in
 // The split-`split` CTA of a (sequence, kv head) merges output dims [j0, j1) of the
 // G heads (flattened h * HD + d) from all nsplit partial records: per head
 // M = max m_s, w_s = exp(m_s - M), L = sum w_s l_s, O = sum w_s o_s / L. Every split
-// takes an equal slice, so the merge costs one round of tagged reads instead of a
-// serial last-arriver pass.
+// takes an equal slice, so the merge is spread over all the item's CTAs instead of
+// one CTA merging every split.
 template <int HD>
 __device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int split, int nsplit) {
     Ctx c = c_in;
