@@ -825,55 +825,68 @@ struct Producer {
 };
 
 // ------------------------------------------------------------------ consumer pieces
-// rstd[b] = 1 / sqrt(mean(src[b]^2) + eps); fixed summation order. Small batches read
-// the tagged rows (4 pairs in flight per thread and round), larger ones the fp32 rows.
-__device__ __forceinline__ void rms_scale(Ctx& c, const GemvStage& s) {
+// rstd[b] = 1 / sqrt(mean(src[b]^2) + eps); fixed summation order. Every k-step reads
+// all the batch rows at once, so the whole pass costs K / 1024 read latencies, not one
+// per row and k-step. Small batches read the tagged rows, larger ones the fp32 rows.
+__device__ __noinline__ void rms_scale(Ctx& c_in, const GemvStage& s) {
+    Ctx c = c_in;
     const StepArgs& a = *c.a;
-    const int K = s.K;
+    const int K = s.K, B = a.B;
     float* red = c.scratch;
-    for (int b = 0; b < a.B; ++b) {
-        float ss = 0.f;
-        if (tagged(a)) {
-            const uint64_t* row = s.src + (size_t)b * s.lds;
-            for (int k0 = c.tid * 2; k0 < K; k0 += kConsumerThreads * 8) {
-                uint64_t w[4][2];
-                Spin sp;
-                for (;;) {
-                    bool ok = true;
+    float ss[kMaxBatch];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int k = k0 + j * kConsumerThreads * 2;
-                        w[j][0] = w[j][1] = (uint64_t)s.src_tag << 32;
-                        if (k < K) ll_ld2(row + k, w[j][0], w[j][1]);
-                    }
+    for (int b = 0; b < kMaxBatch; ++b) ss[b] = 0.f;
+    if (tagged(a)) {  // B <= kMaxTaggedBatch: pairs of tagged words
+        for (int k = c.tid * 2; k < K; k += kConsumerThreads * 2) {
+            uint64_t w[kMaxTaggedBatch][2];
+            Spin sp;
+            for (;;) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) ok = ok && ll_tag(w[j][0]) == s.src_tag && ll_tag(w[j][1]) == s.src_tag;
-                    if (ok || !sp.again(a, c.sm, s.task_id)) break;
+                for (int b = 0; b < kMaxTaggedBatch; ++b) {
+                    w[b][0] = w[b][1] = (uint64_t)s.src_tag << 32;
+                    if (b < B) ll_ld2(s.src + (size_t)b * s.lds + k, w[b][0], w[b][1]);
                 }
+                int miss = -1;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (k0 + j * kConsumerThreads * 2 < K) {
-                        const float v0 = ll_val(w[j][0]), v1 = ll_val(w[j][1]);
-                        ss += v0 * v0 + v1 * v1;
-                    }
+                for (int b = kMaxTaggedBatch - 1; b >= 0; --b)
+                    if (ll_tag(w[b][0]) != s.src_tag || ll_tag(w[b][1]) != s.src_tag) miss = b;
+                if (miss < 0 || !ll_wait_pair(s.src + (size_t)miss * s.lds + k, s.src_tag, sp, a, c.sm, s.task_id))
+                    break;
             }
-        } else {
-            for (int k = c.tid * 4; k < K; k += kConsumerThreads * 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(s.srcf + (size_t)b * s.lds + k));
-                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+            for (int b = 0; b < kMaxTaggedBatch; ++b) {
+                const float v0 = ll_val(w[b][0]), v1 = ll_val(w[b][1]);
+                if (b < B) ss[b] += v0 * v0 + v1 * v1;
             }
         }
+    } else {
+        for (int k = c.tid * 4; k < K; k += kConsumerThreads * 4) {
+            float4 v[kMaxBatch];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (c.lane == 0) red[b * kConsumerWarps + c.cw] = ss;
+            for (int b = 0; b < kMaxBatch; ++b)
+                v[b] = b < B ? __ldcg(reinterpret_cast<const float4*>(s.srcf + (size_t)b * s.lds + k))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int b = 0; b < kMaxBatch; ++b) ss[b] += v[b].x * v[b].x + v[b].y * v[b].y + v[b].z * v[b].z + v[b].w * v[b].w;
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < kMaxBatch; ++b) {
+        if (b >= B) break;
+        float t = ss[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (c.lane == 0) red[b * kConsumerWarps + c.cw] = t;
     }
     consumer_sync();
-    if (c.tid < a.B) {
-        float ss = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) ss += red[c.tid * kConsumerWarps + w];
-        c.sm->rstd[c.tid] = rsqrtf(ss / (float)K + a.p.eps);
+    if (c.tid < B) {
+        float t = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) t += red[c.tid * kConsumerWarps + w];
+        c.sm->rstd[c.tid] = rsqrtf(t / (float)K + a.p.eps);
     }
     consumer_sync();
+    c_in.tn = c.tn;
+    MK_PROF_BACK(c_in, c);
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
