@@ -152,6 +152,49 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ replicas (N > 1)
+def init_replicas(backend=None):
+    """One process per GPU, each a full replica of the decode path (the step does not
+    shard). Reads RANK / WORLD_SIZE / LOCAL_RANK from the environment and, for N > 1,
+    joins the process group: NCCL on GPUs, gloo where there is no GPU. Returns
+    (rank, world, local_rank, torch.distributed or None)."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world <= 1:
+        return rank, world, local, None
+    import torch
+    import torch.distributed as dist_mod
+    if backend is None:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist_mod.init_process_group(backend)
+    return rank, world, local, dist_mod
+
+
+def max_over_ranks(x, dist, device="cpu"):
+    """The largest of every rank's x (the slowest replica's time); x itself at N = 1."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, rows, steps, elapsed_ms):
+    """Tokens per second of the whole job: every replica decodes `rows` tokens a step for
+    `steps` steps, over the slowest replica's elapsed time."""
+    return world * rows * steps / (elapsed_ms / 1000.0)
+
+
+def emit(line, rank):
+    """Rank 0 alone prints the JSON line."""
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ workloads
 def setup_b1(cfg, W, device, steps_total, mk):
     import torch
@@ -266,7 +309,8 @@ def timed_region(one, warmup, steps, dist):
 def e2e_loop(S, cfg, steps, warmup):
     """End to end through the public API: every step copies its inputs from pinned
     host memory, runs mk_decode_step, and reads the next tokens back to the host
-    (which feeds them to the following step)."""
+    (which feeds them to the following step). Returns the wall time (s) of the timed
+    steps and the bytes copied each way per step."""
     import torch
     model = S["model"]
     B = S["B"]
@@ -309,7 +353,7 @@ def e2e_loop(S, cfg, steps, warmup):
     for i in range(steps):
         one(warmup + i)
     wall = time.perf_counter() - t0
-    return B * steps / wall, h2d, d2h
+    return wall, h2d, d2h
 
 
 # ------------------------------------------------------------------ the other model configs
@@ -457,7 +501,7 @@ def reference_arm(args, rank, world):
     val = done / el
     sample = (f"{done} of {args.steps} requested decode steps of the dense-2b batch-1 workload "
               f"(90 s budget), plain C fp32 oracle, OpenMP over output rows")
-    print(json.dumps({
+    emit({
         "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
         "n_gpus": world, "steps": done, "warmup": min(args.warmup, 1),
         "ms_per_step": 1000.0 * el / max(done, 1), "higher_is_better": True, "scaling": "weak",
@@ -467,7 +511,7 @@ def reference_arm(args, rank, world):
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }), flush=True)
+    }, rank)
 
 
 # ------------------------------------------------------------------ main
@@ -487,16 +531,7 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist_mod
-        import torch
-        torch.cuda.set_device(local)
-        dist_mod.init_process_group("nccl")
-        dist = dist_mod
+    rank, world, local, dist = init_replicas()
 
     if args.impl == "reference":
         reference_arm(args, rank, world)
@@ -523,12 +558,9 @@ def main():
     code, task = S["model"].status()
     if code != 0:
         raise RuntimeError(f"timed steps failed: status {code} task {task}")
-    if dist:
-        t = torch.tensor([elapsed_ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, f"cuda:{local}")
     ms = elapsed_ms / args.steps
-    value = world * 1 * args.steps / (elapsed_ms / 1000.0)
+    value = whole_job_value(world, 1, args.steps, elapsed_ms)
     lo = [[0] for _ in range(cfg.n_layers)]
     pos_mean = CTX + (CYCLE - 1) / 2.0
     algo = algorithmic_bytes(cfg, 1, lo, [pos_mean])
@@ -563,6 +595,7 @@ def main():
         S8 = setup_b8(cfg8, W, local, args.warmup + steps8, mk)
         one8, st8, en8 = run_device_loop(S8, steps8, args.warmup, cfg8, batch8=True)
         el8, _ = timed_region(one8, args.warmup, steps8, dist)
+        el8 = max_over_ranks(el8, dist, f"cuda:{local}")
         code, task = S8["model"].status()
         if code != 0:
             raise RuntimeError(f"batch-8 steps failed: status {code} task {task}")
@@ -575,7 +608,7 @@ def main():
                    for l in range(cfg8.n_layers)]
             bytes8 += algorithmic_bytes(cfg8, 8, los, [int(x) for x in p])
         ach8 = bytes8 / (sum(per8) / 1000.0) / 1e9
-        out["batch8"] = {"value": round(world * 8 * steps8 / (el8 / 1000.0), 2), "unit": "tokens/s",
+        out["batch8"] = {"value": round(whole_job_value(world, 8, steps8, el8), 2), "unit": "tokens/s",
                          "steps": steps8, "ms_per_step": round(el8 / steps8, 4),
                          "hbm_gbs": round(ach8, 1), "pct_of_8tbs": round(100 * ach8 / NOMINAL_HBM_GBS, 2),
                          "frac_of_measured_peak": round(ach8 / peak, 4),
@@ -602,8 +635,10 @@ def main():
     # end to end through host buffers
     if not args.no_e2e:
         e2e_steps = min(args.steps, 512)
-        val, h2d, d2h = e2e_loop(S, cfg, e2e_steps, args.warmup)
-        out["e2e"] = {"value": round(world * val, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        wall, h2d, d2h = e2e_loop(S, cfg, e2e_steps, args.warmup)
+        wall = max_over_ranks(wall, dist, f"cuda:{local}")
+        val = whole_job_value(world, S["B"], e2e_steps, 1000.0 * wall)
+        out["e2e"] = {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                       "path": "pinned host inputs -> cudaMemcpyAsync -> mk_decode_step -> next token to host, sync every step"}
     # CPU baseline: the oracle on the host cores (rank 0, N = 1 only)
@@ -613,8 +648,7 @@ def main():
         kv_host = synth.bf16_bits(S["model"].kv()).copy()
         out["cpu_baseline"] = oracle_sample(cfg, W_cpu, kv_host, S["pt_host"])
     S["model"].close()
-    if rank == 0:
-        print(json.dumps(out), flush=True)
+    emit(out, rank)
     if dist:
         dist.destroy_process_group()
 
