@@ -381,6 +381,8 @@ def other_config(mk, local, name, B, ctx, steps, warmup, prefix_pages=0, private
         pt = synth.random_page_tables(rng, npages, [per] * B, per)
         start = np.full(B, ctx, np.int64)
     model = mk.DecodeModel(cfg, W, npages, device=local)
+    if prefix_pages:  # the rows' shared prefix is read once per kv head for the batch
+        model.set_shared_prefix([0] * B, [prefix_pages] * B)
     synth.fill_normal_bf16_(model.kv(), seed + 100)
     pos = torch.tensor(np.stack([start + t for t in range(total)]).astype(np.int32), device=dev)
     toks = torch.zeros((total + 1, B), dtype=torch.int32, device=dev)
@@ -434,8 +436,9 @@ def other_config(mk, local, name, B, ctx, steps, warmup, prefix_pages=0, private
            "algorithmic_bytes_per_step": int(byts / steps)}
     if prefix_pages:
         out["naive_bytes_per_step"] = int(naive / steps)
-        out["workload"] = (f"{name}, batch {B} sharing a {prefix_pages * 16}-token prefix page run, "
-                           f"{private_pages * 16}-token private runs; prefix KV counted once in the bytes")
+        out["workload"] = (f"{name}, batch {B} sharing a {prefix_pages * 16}-token prefix page run "
+                           f"(declared: read once per kv head), {private_pages * 16}-token private runs; "
+                           f"prefix KV counted once in the bytes")
     else:
         out["workload"] = f"{name}, batch {B}, {ctx}-token seeded paged KV per row"
     if unions is not None:

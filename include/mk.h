@@ -195,6 +195,28 @@ MK_API mk_status mk_set_option(mk_handle *h, mk_option opt, int64_t value);
  * temperatures: MK_ERR_INVALID_ARG. mk_decode_step_noalloc is always greedy. */
 MK_API mk_status mk_set_sampling(mk_handle *h, float temperature, uint64_t seed);
 
+/* Shared prefixes (cascade attention) for the next steps of batch `batch`. Source: the
+ * prefix cache of "Cohere, Megakernel sunum sistemini acik kaynak yapti", section
+ * "Sinirlar acikca yazilmis", and the shared prefix caches of concurrent sessions in
+ * "Magnitude: Donanimiza Gore Kernel Ayarlayan Kendi Kendini Derleyen Bir Cikarim
+ * Motoru", section "Bellek ve eszamanlilik icin ne anlama geliyor?".
+ *   leader[batch]        (host) row b shares its prefix with row leader[b]: leader[b] <= b
+ *                        and leader[leader[b]] == leader[b]; a row with leader[b] == b and
+ *                        no other member is a group of one (no sharing)
+ *   shared_pages[batch]  (host) the caller guarantees that logical pages
+ *                        [0, shared_pages[b]) of row b's page table hold the same page ids
+ *                        as those of row leader[b]; equal within a group
+ * At most 16 / (n_q_heads / n_kv_heads) rows per group (two 8-wide query column tiles).
+ * In every layer where all rows of a group attend the whole prefix (no sliding window
+ * cuts into it) and each row's current page lies after it, the prefix K/V pages are
+ * read once per kv head for the whole group (through the leader's page table) instead
+ * of once per row; elsewhere the rows attend on their own. Results do not depend on it
+ * beyond fp32 summation order. batch == 0 clears the groups (leader and shared_pages
+ * may be NULL). While groups are declared, mk_decode_step with another batch size
+ * returns MK_ERR_INVALID_ARG. Errors: MK_ERR_INVALID_ARG for any violated rule above. */
+MK_API mk_status mk_set_shared_prefix(mk_handle *h, int32_t batch, const int32_t *leader,
+                                      const int32_t *shared_pages);
+
 /* Read-only facts about a handle (for schedulers and benchmarks). */
 typedef struct mk_info {
     int32_t num_ctas;          /* persistent CTAs per launch (one per SM) */

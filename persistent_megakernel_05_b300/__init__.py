@@ -33,7 +33,8 @@ MK_OPT_PREFETCH_SLOTS = 3
 # exported symbols of include/mk.h
 ABI_SYMBOLS = ("mk_create", "mk_kv_alloc", "mk_kv_free", "mk_decode_step", "mk_status_sync",
                "mk_status_reset", "mk_set_option", "mk_get_info", "mk_debug_buffer",
-               "mk_status_string", "mk_destroy", "mk_decode_step_noalloc", "mk_set_sampling")
+               "mk_status_string", "mk_destroy", "mk_decode_step_noalloc", "mk_set_sampling",
+               "mk_set_shared_prefix")
 MK_NOALLOC_SCRATCH_BYTES = 8 << 20
 MK_BUF_X, MK_BUF_QKV, MK_BUF_ATTN, MK_BUF_H, MK_BUF_ROUTE, MK_BUF_MOE_UNION = 1, 2, 3, 4, 5, 6
 
@@ -115,6 +116,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mk_set_option.argtypes = [_vp, ctypes.c_int, i64]
     L.mk_set_sampling.restype = ctypes.c_int
     L.mk_set_sampling.argtypes = [_vp, ctypes.c_float, ctypes.c_uint64]
+    L.mk_set_shared_prefix.restype = ctypes.c_int
+    L.mk_set_shared_prefix.argtypes = [_vp, i32, _P(i32), _P(i32)]
     L.mk_get_info.restype = ctypes.c_int
     L.mk_get_info.argtypes = [_vp, _P(mk_info)]
     L.mk_debug_buffer.restype = ctypes.c_int
@@ -186,6 +189,21 @@ def mk_set_option(handle: int, opt: int, value: int):
 def mk_set_sampling(handle: int, temperature: float, seed: int):
     _check(load().mk_set_sampling(handle, float(temperature), int(seed) & (2 ** 64 - 1)),
            "mk_set_sampling")
+
+
+def mk_set_shared_prefix(handle: int, leader, shared_pages):
+    """leader[b], shared_pages[b] for each row of the batch (host lists); empty lists
+    clear the groups."""
+    B = len(leader)
+    if len(shared_pages) != B:
+        raise ValueError("leader and shared_pages differ in length")
+    if B == 0:
+        _check(load().mk_set_shared_prefix(handle, 0, None, None), "mk_set_shared_prefix")
+        return
+    arr = ctypes.c_int32 * B
+    _check(load().mk_set_shared_prefix(handle, B, arr(*[int(x) for x in leader]),
+                                       arr(*[int(x) for x in shared_pages])),
+           "mk_set_shared_prefix")
 
 
 def mk_get_info(handle: int) -> mk_info:
@@ -339,6 +357,12 @@ class DecodeModel:
     def set_sampling(self, temperature: float, seed: int = 0):
         """temperature 0: greedy; > 0: draw from softmax(logits / temperature)."""
         mk_set_sampling(self.handle, temperature, seed)
+
+    def set_shared_prefix(self, leader=(), shared_pages=()):
+        """Rows b with the same leader[b] share logical pages [0, shared_pages[b]) of their
+        page tables; their prefix K/V is read once per kv head for the group. No
+        arguments: clear."""
+        mk_set_shared_prefix(self.handle, list(leader), list(shared_pages))
 
     def close(self):
         if getattr(self, "handle", None):

@@ -38,6 +38,9 @@ struct mk_handle {
     long long timeout_ns = 1000000000LL;
     int skip_publish = -1;
     int prefetch_slots = mk::kDefaultPrefetchSlots;
+    int pf_batch = 0;               // batch the shared-prefix groups were declared for (0: none)
+    int pf_lead[mk::kMaxBatch] = {};
+    int pf_pages[mk::kMaxBatch] = {};
     int num_ctas = 0;
     int hd = 0;
     int64_t weight_bytes = 0;
@@ -405,6 +408,8 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
     if ((uint64_t)batch * h->desc.n_kv_heads * max_pages_per_seq * h->num_ctas >= (1ull << 31))
         return MK_ERR_INVALID_ARG;
     if (!h->kv) return MK_ERR_INVALID_ARG;
+    // declared shared-prefix groups describe the rows of one batch size
+    if (h->pf_batch != 0 && h->pf_batch != batch) return MK_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
     mk::StepArgs a;
     a.kv_tmap = h->kv_tmap;
@@ -429,6 +434,11 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
     a.temperature = h->temperature;
     a.seed_lo = (uint32_t)h->seed;
     a.seed_hi = (uint32_t)(h->seed >> 32);
+    a.pf_on = h->pf_batch != 0;
+    for (int b = 0; b < mk::kMaxBatch; ++b) {
+        a.pf_lead[b] = h->pf_batch ? h->pf_lead[b] : -1;
+        a.pf_pages[b] = h->pf_batch ? h->pf_pages[b] : 0;
+    }
     void* args[] = {&a};
     const void* fn = h->hd == 128 ? (const void*)mk::decode_step_kernel<128>
                                   : (const void*)mk::decode_step_kernel<64>;
@@ -500,6 +510,35 @@ mk_status mk_set_sampling(mk_handle* h, float temperature, uint64_t seed) {
     if (!h || !std::isfinite(temperature) || temperature < 0.f) return MK_ERR_INVALID_ARG;
     h->temperature = temperature;
     h->seed = seed;
+    return MK_OK;
+}
+
+mk_status mk_set_shared_prefix(mk_handle* h, int32_t batch, const int32_t* leader,
+                               const int32_t* shared_pages) {
+    if (!h) return MK_ERR_INVALID_ARG;
+    if (batch == 0) {
+        h->pf_batch = 0;
+        return MK_OK;
+    }
+    if (batch < 1 || batch > h->desc.max_batch || !leader || !shared_pages) return MK_ERR_INVALID_ARG;
+    int lead[mk::kMaxBatch], pages[mk::kMaxBatch], size[mk::kMaxBatch] = {};
+    for (int b = 0; b < batch; ++b) {
+        const int L = leader[b];
+        // a row joins the group of an earlier (or the same) row that leads its own group
+        if (L < 0 || L > b || leader[L] != L) return MK_ERR_INVALID_ARG;
+        if (shared_pages[b] < 0 || shared_pages[b] != shared_pages[L]) return MK_ERR_INVALID_ARG;
+        lead[b] = L;
+        pages[b] = shared_pages[b];
+        ++size[L];
+    }
+    const int G = h->desc.n_q_heads / h->desc.n_kv_heads;
+    for (int b = 0; b < batch; ++b)
+        if (size[b] * G > 16) return MK_ERR_INVALID_ARG;  // two 8-wide query column tiles
+    h->pf_batch = batch;
+    for (int b = 0; b < mk::kMaxBatch; ++b) {
+        h->pf_lead[b] = b < batch ? lead[b] : -1;
+        h->pf_pages[b] = b < batch ? pages[b] : 0;
+    }
     return MK_OK;
 }
 
@@ -800,6 +839,11 @@ extern "C" mk_status mk_decode_step_noalloc(
     a.timeout_ns = 1000000000LL;
     a.temperature = 0.f;  // greedy
     a.seed_lo = a.seed_hi = 0;
+    a.pf_on = 0;  // no shared-prefix groups
+    for (int b = 0; b < mk::kMaxBatch; ++b) {
+        a.pf_lead[b] = -1;
+        a.pf_pages[b] = 0;
+    }
     void* args[] = {&a};
     const void* fn = hd == 128 ? (const void*)mk::decode_step_kernel<128>
                                : (const void*)mk::decode_step_kernel<64>;

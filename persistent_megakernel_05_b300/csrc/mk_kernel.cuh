@@ -174,6 +174,11 @@ struct StepArgs {
     int skip_publish;                   // task id whose outputs are never written, or -1
     int prefetch_slots;                 // L2 prefetch lead over the loader, in slots (0 = off)
     long long timeout_ns;
+    // shared prefixes: row b shares its logical pages [0, pf_pages[b]) with the rows of
+    // the same leader pf_lead[b] (-1: none); pf_on = 0 when no group is declared
+    int pf_on;
+    int pf_lead[kMaxBatch];
+    int pf_pages[kMaxBatch];
 };
 
 // Up to this batch size the activations between stages travel as tagged words (one
@@ -551,22 +556,77 @@ __device__ __forceinline__ SeqSpan seq_span(const Plan& p, const Smem* sm, int l
     return s;
 }
 
-// Calls f(b, g, first page of the piece within the span, page count, split, nsplit) for
-// each attention piece of this CTA. Work items are (sequence b, kv head g) with np(b)
-// pages each. When there are no more items than CTAs, every item gets CTAs of its own,
-// in proportion to its pages and at least one: with C' = C - W spare CTAs and S_i the
-// pages of the items before item i, item i takes CTAs [i + C' S_i / U, i + 1 + C' S_(i+1) / U)
-// and splits its pages evenly over min(CTAs, pages) of them. No CTA then carries the
-// fixed cost of two pieces (those CTAs would finish last and every merge would wait for
-// them). With more items than CTAs, (b, g, page) units are dealt out in contiguous ranges.
+// ---- shared prefixes (cascade attention) ----
+// Rows whose leading logical pages are the same physical pages form a group (declared by
+// the caller). In a layer where every row of a group attends its whole prefix (lo = 0)
+// and keeps its current page to itself, the group's prefix pages are read once for all
+// its rows: one item whose query columns are the rows' G heads side by side (at most 16
+// columns, two 8-wide MMA column tiles), whose partial records go to every row's merge.
+// Packed per row: lead (4 bits, leader + 1, 0 = none); rows of a leader (8 bits).
+struct Groups {
+    uint32_t lead;
+    uint64_t rows;
+    __device__ __forceinline__ int leader(int b) const { return (int)((lead >> (4 * b)) & 15u) - 1; }
+    __device__ __forceinline__ uint32_t members(int L) const { return (uint32_t)(rows >> (8 * L)) & 0xffu; }
+};
+
+__device__ __forceinline__ Groups prefix_groups(const StepArgs& a, const Smem* sm, int l) {
+    Groups gr{0u, 0ull};
+    if (!a.pf_on) return gr;
+    uint64_t rows = 0;
+    for (int b = 0; b < a.B; ++b) {
+        const int L = a.pf_lead[b];
+        if (L >= 0 && L < a.B && a.pf_pages[L] > 0) rows |= 1ull << (8 * L + b);
+    }
+    for (int L = 0; L < a.B; ++L) {
+        const uint32_t m = (uint32_t)(rows >> (8 * L)) & 0xffu;
+        if (__popc(m) < 2) continue;
+        bool ok = true;
+        for (int r = 0; r < a.B; ++r)
+            if ((m >> r) & 1u) {
+                const SeqSpan sp = seq_span(a.p, sm, l, r);
+                ok = ok && sp.lo == 0 && a.pf_pages[L] <= sp.pos / kPage;
+            }
+        if (!ok) continue;
+        gr.rows |= (uint64_t)m << (8 * L);
+        for (int r = 0; r < a.B; ++r)
+            if ((m >> r) & 1u) gr.lead |= (uint32_t)(L + 1) << (4 * r);
+    }
+    return gr;
+}
+
+// One attention piece: pages [sp.p0 + u, sp.p0 + u + n) of an item (a row's pages, a
+// row's private pages after its group's prefix, or a group's shared prefix).
+struct Piece {
+    SeqSpan sp;      // the item's pages [p0, p0 + np), keys [lo, pos]
+    int b, g;        // row whose page table the item walks (a prefix: the leader), kv head
+    uint32_t rows;   // rows whose queries the piece serves (bit mask)
+    int u, n;        // the piece within the item
+    int split, nsplit;
+    int slot0;       // partial-record slot of split 0 (after the records of the row's prefix)
+    int nrec;        // records the row's merge reads (prefix pieces + its own)
+    bool prefix;     // a shared-prefix piece: writes records for every row, merges nothing
+};
+
+// Calls f(piece) for each attention piece of this CTA. Work items are (row b, kv head g)
+// with np(b) pages each, plus one item per (active prefix group, g). When there are no
+// more items than CTAs, every item gets CTAs of its own, in proportion to its pages and
+// at least one: with C' = C - W spare CTAs and S_i the pages of the items before item i,
+// item i takes CTAs [i + C' S_i / U, i + 1 + C' S_(i+1) / U) and splits its pages evenly
+// over min(CTAs, pages) of them. No CTA then carries the fixed cost of two pieces (those
+// CTAs would finish last and every merge would wait for them). With more items than
+// CTAs (no prefix groups then), (b, g, page) units are dealt out in contiguous ranges.
+// Items of one row each (no prefix groups): (b, g) in row-major order.
 template <typename F>
-__device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta, F&& f) {
+__device__ __forceinline__ void for_each_row_piece(const StepArgs& a, const Smem* sm, int l, int cta, F&& f) {
     const Plan& p = a.p;
-    // 32-bit unsigned unit arithmetic: U * C < 2^31 (checked on the host)
     uint32_t U = 0;
     for (int b = 0; b < a.B; ++b) U += (uint32_t)(p.Hkv * seq_span(p, sm, l, b).np);
     const uint32_t C = (uint32_t)p.C;
     const uint32_t W = (uint32_t)(a.B * p.Hkv);
+    Piece pc;
+    pc.slot0 = 0;
+    pc.prefix = false;
     if (W <= C) {
         const uint32_t Cp = C - W;
         uint32_t S = 0, i = 0;
@@ -579,9 +639,12 @@ __device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta
                 if ((uint32_t)cta < c1) {
                     const int nsplit = min((int)(c1 - c0), sp.np), k = cta - (int)c0;
                     if (k < nsplit) {
-                        const int u0 = (int)((uint32_t)k * sp.np / nsplit);
-                        const int u1 = (int)((uint32_t)(k + 1) * sp.np / nsplit);
-                        f(b, g, sp, u0, u1 - u0, k, nsplit);
+                        pc.sp = sp;
+                        pc.b = b; pc.g = g; pc.rows = 1u << b;
+                        pc.u = (int)((uint32_t)k * sp.np / nsplit);
+                        pc.n = (int)((uint32_t)(k + 1) * sp.np / nsplit) - pc.u;
+                        pc.split = k; pc.nsplit = nsplit; pc.nrec = nsplit;
+                        f(pc);
                     }
                     return;
                 }
@@ -600,11 +663,101 @@ __device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta
             const uint32_t lo = max(s, u0), hi = min(e, u1);
             if (lo < hi) {
                 const int c0 = first_cta(s);
-                const int nsplit = first_cta(e - 1) - c0 + 1;
-                f(b, g, sp, (int)(lo - s), (int)(hi - lo), cta - c0, nsplit);
+                pc.sp = sp;
+                pc.b = b; pc.g = g; pc.rows = 1u << b;
+                pc.u = (int)(lo - s); pc.n = (int)(hi - lo);
+                pc.split = cta - c0; pc.nsplit = first_cta(e - 1) - c0 + 1;
+                pc.nrec = pc.nsplit;
+                f(pc);
             }
             s = e;
             if (s >= u1) return;
+        }
+    }
+}
+
+template <typename F>
+__device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta, F&& f) {
+    if (!a.pf_on) {
+        for_each_row_piece(a, sm, l, cta, f);
+        return;
+    }
+    const Plan& p = a.p;
+    // 32-bit unsigned unit arithmetic: U * C < 2^31 (checked on the host)
+    const uint32_t C = (uint32_t)p.C;
+    const Groups gr = prefix_groups(a, sm, l);
+    int ng = 0;
+    for (int L = 0; L < a.B; ++L) ng += gr.members(L) != 0u;
+    const uint32_t W = (uint32_t)((a.B + ng) * p.Hkv);
+    // no active group in this layer, or more items than CTAs: every row on its own
+    if (ng == 0 || W > C) {
+        for_each_row_piece(a, sm, l, cta, f);
+        return;
+    }
+    {
+        uint32_t U = 0;
+        for (int b = 0; b < a.B; ++b) {
+            const SeqSpan sp = seq_span(p, sm, l, b);
+            const int L = gr.leader(b);
+            if (L == b) U += (uint32_t)a.pf_pages[L];
+            U += (uint32_t)(L >= 0 ? sp.pos / kPage - a.pf_pages[L] + 1 : sp.np);
+        }
+        U *= (uint32_t)p.Hkv;
+        const uint32_t Cp = C - W;
+        uint32_t S = 0, i = 0;
+        int ncs[kMaxBatch];  // splits of each group's prefix item (this kv head)
+        for (int g = 0; g < p.Hkv; ++g) {
+            for (int b = 0; b < a.B; ++b) {
+                const SeqSpan full = seq_span(p, sm, l, b);
+                const int L = gr.leader(b);
+                if (L == b) {  // the group's shared prefix, ahead of its rows' own pages
+                    const int P = a.pf_pages[L];
+                    const uint32_t c0 = i + Cp * S / U;
+                    S += (uint32_t)P;
+                    const uint32_t c1 = i + 1 + Cp * S / U;
+                    ++i;
+                    const int ns = min((int)(c1 - c0), P);
+                    ncs[b] = ns;
+                    if ((uint32_t)cta < c1) {
+                        const int k = cta - (int)c0;
+                        if (k < ns) {
+                            Piece pc;
+                            pc.sp = SeqSpan{0, full.pos, 0, P};
+                            pc.b = b; pc.g = g; pc.rows = gr.members(L);
+                            pc.u = (int)((uint32_t)k * P / ns);
+                            pc.n = (int)((uint32_t)(k + 1) * P / ns) - pc.u;
+                            pc.split = k; pc.nsplit = ns; pc.slot0 = 0; pc.nrec = ns; pc.prefix = true;
+                            f(pc);
+                        }
+                        return;
+                    }
+                }
+                SeqSpan sp = full;
+                int slot0 = 0;
+                if (L >= 0) {  // the row's pages after its group's prefix
+                    sp.p0 = a.pf_pages[L];
+                    sp.np = full.pos / kPage - sp.p0 + 1;
+                    slot0 = ncs[L];
+                }
+                const uint32_t c0 = i + Cp * S / U;
+                S += (uint32_t)sp.np;
+                const uint32_t c1 = i + 1 + Cp * S / U;
+                ++i;
+                if ((uint32_t)cta < c1) {
+                    const int ns = min((int)(c1 - c0), sp.np), k = cta - (int)c0;
+                    if (k < ns) {
+                        Piece pc;
+                        pc.sp = sp;
+                        pc.b = b; pc.g = g; pc.rows = 1u << b;
+                        pc.u = (int)((uint32_t)k * sp.np / ns);
+                        pc.n = (int)((uint32_t)(k + 1) * sp.np / ns) - pc.u;
+                        pc.split = k; pc.nsplit = ns; pc.slot0 = slot0; pc.nrec = slot0 + ns;
+                        pc.prefix = false;
+                        f(pc);
+                    }
+                    return;
+                }
+            }
         }
     }
 }
@@ -720,9 +873,10 @@ struct Producer {
         constexpr int NB = HD / 64;     // 64-wide boxes per page row
         MK_TRACE_P(*this, TR_P_STAGE, l * 16 + ST_ATTN);
         bool ok = true;
-        for_each_piece(*a, sm, l, cta, [&](int b, int g, const SeqSpan& sp, int u, int n,
-                                           int split, int nsplit) {
+        for_each_piece(*a, sm, l, cta, [&](const Piece& pc) {
             if (!ok) return;
+            const int b = pc.b, g = pc.g, u = pc.u, n = pc.n;
+            const SeqSpan& sp = pc.sp;
             const int* pt = a->page_table + (size_t)b * a->max_pages;
             for (int st = 0; st < n; st += PPS) {
                 const int np = min(PPS, n - st);
@@ -1467,68 +1621,98 @@ __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
 
 __device__ __forceinline__ int bg_id(const Plan& p, int b, int g) { return b * p.Hkv + g; }
 
-// ---- attention: one piece (a CTA's share of one (b, kv head)) ----
-// After the key loop of a piece: merge the 8 warps' partial softmax states (left in
-// shared memory by the loop) and write this split's partial record as tagged words.
-// Non-inlined so the key loop keeps its registers to itself.
+// ---- attention: one piece (a CTA's share of one item) ----
+// Query columns of a piece: row r of the piece's rows (ascending) holds columns
+// r*G .. r*G + G-1 (its G heads of kv head g). Columns go in 8-wide MMA tiles; with two
+// tiles, warps 0-3 serve tile 0 and warps 4-7 tile 1 on the same pages.
+__device__ __forceinline__ int piece_row(uint32_t rows, int r) { return (int)__fns(rows, 0u, r + 1); }
+
+// Local columns (of a tile) whose per-warp softmax states fit the scratch at once.
 template <int HD>
-__device__ __noinline__ void attention_finish(Ctx& c_in, int l, int b, int g, int split) {
+struct FinishCols {
+    static constexpr int fit = (kScratchBytes - 512) / (kConsumerWarps * (HD + 8) * 4);
+    static constexpr int value = fit < 8 ? fit : 8;
+};
+
+// After the key loop of a piece: merge the warps' partial softmax states of local
+// columns [ch0, ch0 + FinishCols) (left in shared memory by the piece) and write them as
+// this split's partial records, one per row, as tagged words. MULTI: a shared-prefix
+// piece (several rows, one or two column tiles); otherwise one row, one tile, one pass.
+// Non-inlined so the key loop keeps its registers to itself.
+template <int HD, bool MULTI>
+__device__ __noinline__ void attention_finish(Ctx& c_in, int l, const Piece& pc, int ch0, int NC, int wpt_in) {
     Ctx c = c_in;
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
     const int G = p.G;
     const int task = l * 16 + ST_ATTN;
     constexpr int OS = HD + 8;
-    float* ws_o = c.scratch;                                  // [8][G][OS]
-    float* ws_m = c.scratch + kConsumerWarps * G * OS;        // [8][8]
+    constexpr int kFC = FinishCols<HD>::value;
+    float* ws_o = c.scratch;                                  // [8][kFC][OS]
+    float* ws_m = c.scratch + kConsumerWarps * kFC * OS;      // [8][8]
     float* ws_l = ws_m + 64;                                  // [8][8]
     consumer_sync();
-    const int bg = b * p.Hkv + g;
-    const int GHD = G * HD;
-    uint64_t* rec = p.part + ((size_t)bg * p.C + split) * (GHD + 2 * G);
+    const int GHD = G * HD, RS = GHD + 2 * G;
+    const int wpt = MULTI ? wpt_in : kConsumerWarps;
+    const int CT = MULTI ? (NC + 7) >> 3 : 1, nct = MULTI ? min(kFC, min(8, NC) - ch0) : G;
+    const int tot = CT * nct * HD;
+    const int slot = pc.slot0 + pc.split;
     const uint32_t tag = tag_of(a, l, TAG_PART);
     if (!c.sm->abort && a.skip_publish != task) {
-        for (int e = 2 * c.tid; e < GHD; e += 2 * kConsumerThreads) {
-            const int hl = e / HD, d = e % HD;
+        for (int e = 2 * c.tid; e < tot; e += 2 * kConsumerThreads) {
+            const int T = MULTI ? e / (nct * HD) : 0, rem = e - T * nct * HD;
+            const int hl = rem / HD, d = rem - hl * HD;
+            const int h = MULTI ? ch0 + hl : hl, col = T * 8 + h;
+            if (MULTI && col >= NC) continue;
+            const int w0 = T * wpt;
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ws_m[w * 8 + hl]);
+            for (int k = 0; k < kConsumerWarps; ++k)
+                if (k < wpt) M = fmaxf(M, ws_m[(w0 + k) * 8 + h]);
             float o0 = 0.f, o1 = 0.f, L = 0.f;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = ws_m[w * 8 + hl];
+            for (int k = 0; k < kConsumerWarps; ++k) {
+                if (k >= wpt) continue;
+                const int w = w0 + k;
+                const float mw = ws_m[w * 8 + h];
                 const float f = mw == -INFINITY ? 0.f : expf(mw - M);
-                const float2 ov = *reinterpret_cast<const float2*>(ws_o + (w * G + hl) * OS + d);
+                const float2 ov = *reinterpret_cast<const float2*>(ws_o + (w * kFC + hl) * OS + d);
                 o0 += f * ov.x;
                 o1 += f * ov.y;
-                L += f * ws_l[w * 8 + hl];
+                L += f * ws_l[w * 8 + h];
             }
-            ll_st2(rec + e, o0, o1, tag);
-            if (d == 0) ll_st2(rec + GHD + 2 * hl, M, L, tag);
+            const int r = MULTI ? col / G : 0, hh = col - r * G;
+            const int b = MULTI ? piece_row(pc.rows, r) : pc.b;
+            uint64_t* rec = p.part + ((size_t)(b * p.Hkv + pc.g) * p.C + slot) * RS;
+            ll_st2(rec + hh * HD + d, o0, o1, tag);
+            if (d == 0) ll_st2(rec + GHD + 2 * hh, M, L, tag);
         }
     }
     consumer_sync();  // the scratch is free for the next piece
     MK_PROF_MARK(c, PS_A_FINISH);
-    if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_PART, (uint32_t)split);
+    if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_PART, (uint32_t)pc.split);
     c_in.tn = c.tn;
     MK_PROF_BACK(c_in, c);
 }
 
-// The split-`split` CTA of a (sequence, kv head) merges output dims [j0, j1) of the
-// G heads (flattened h * HD + d) from all nsplit partial records: per head
-// M = max m_s, w_s = exp(m_s - M), L = sum w_s l_s, O = sum w_s o_s / L. Every split
-// takes an equal slice, so the merge is spread over all the item's CTAs instead of
-// one CTA merging every split.
+// The split-`split` of the nsplit CTAs of a (sequence, kv head) item merges output dims
+// [j0, j1) of the G heads (flattened h * HD + d) from all nrec partial records of that
+// row (its shared prefix's pieces, if any, then its own): per head M = max m_s,
+// w_s = exp(m_s - M), L = sum w_s l_s, O = sum w_s o_s / L. Every split takes an equal
+// slice, so the merge is spread over all the item's CTAs instead of one CTA merging
+// every split.
 template <int HD>
-__device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int split, int nsplit) {
+__device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int split, int nsplit_in,
+                                             int nrec) {
     Ctx c = c_in;
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
     const int G = p.G, GHD = G * HD, RS = GHD + 2 * G;
     const int task = l * 16 + ST_ATTN;
     const uint32_t tp = tag_of(a, l, TAG_PART);
-    const int j0 = (int)((uint32_t)split * GHD / (uint32_t)nsplit);
-    const int j1 = (int)((uint32_t)(split + 1) * GHD / (uint32_t)nsplit);
+    const int j0 = (int)((uint32_t)split * GHD / (uint32_t)nsplit_in);
+    const int j1 = (int)((uint32_t)(split + 1) * GHD / (uint32_t)nsplit_in);
+    const int nsplit = nrec;  // records merged
     if (j0 >= j1 || c.sm->abort) return;  // uniform over the CTA
     const int h0 = j0 / HD, nh = (j1 - 1) / HD - h0 + 1;
     const uint64_t* rec0 = p.part + (size_t)(b * p.Hkv + g) * p.C * RS;
@@ -1627,11 +1811,12 @@ __device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int
     MK_PROF_BACK(c_in, c);
 }
 
-template <int HD>
-__device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, const SeqSpan& sp_in, int u,
-                                             int n, int split, int nsplit) {
+template <int HD, bool MULTI>
+__device__ __noinline__ void attention_piece(Ctx& c_in, int l, const Piece& pc_in) {
     Ctx c = c_in;  // register copy (see gemv_task)
-    const SeqSpan sp = sp_in;
+    const Piece& pc = pc_in;  // fields read where needed (most are dead in the key loop)
+    const SeqSpan sp = pc.sp;
+    const int b = pc.b, g = pc.g, u = pc.u, n = pc.n;
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
     constexpr int NKS = HD / 16;   // k16 steps over the head dim
@@ -1639,31 +1824,48 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
     constexpr int PPS = 512 / HD;  // pages per slot
     const int G = p.G;
     const int gq = c.lane >> 2, t = c.lane & 3;
-    const int hq = g * G + gq;
     const int task = l * 16 + ST_ATTN;
     const int pos = sp.pos, lo = sp.lo;
-    const bool has_last = (sp.p0 + u + n - 1) == pos / kPage;
-    const float2* rope = p.rope + (size_t)pos * (HD / 2);
+    // query columns: the G heads of each row of the piece; 8-wide column tiles (1 or 2,
+    // MULTI only: a shared prefix's rows side by side)
+    const int nrows = MULTI ? __popc(pc.rows) : 1, NC = nrows * G;
+    const int CT = MULTI ? (NC + 7) >> 3 : 1, wpt = MULTI ? kConsumerWarps / CT : kConsumerWarps;
+    const int tile = MULTI ? c.cw / wpt : 0, wl = c.cw - tile * wpt;
+    const bool has_last = !MULTI && (sp.p0 + u + n - 1) == pos / kPage;
     MK_PROF_MARK(c, PS_A_ENTRY);
 
-    // Stage q of the G heads (and the new token's k, v when this piece appends), plus
-    // the RoPE row, through shared memory with coalesced loads: one L2 round trip. Rows
-    // of q are padded to HD + 8 floats so the fragment reads below are conflict-free.
+    // Stage q of the columns (and the new token's k, v when this piece appends), plus the
+    // rows' RoPE rows, through shared memory with coalesced loads: one L2 round trip.
+    // Rows of q are padded to HD + 8 floats so the fragment reads below are conflict-free.
     constexpr int QS = HD + 8;
-    float* qs = c.scratch;                         // [G][QS]
-    float* ks = qs + 8 * QS;                       // [HD]
+    float* qs = c.scratch;                         // [16][QS] (one row: [8][QS])
+    float* ks = qs + (MULTI ? 16 : 8) * QS;        // [HD]
     float* vs = ks + HD;                           // [HD]
-    float2* rs = reinterpret_cast<float2*>(vs + HD);  // [HD / 2]
+    float2* rs = reinterpret_cast<float2*>(vs + HD);  // [nrows][HD / 2]
     if (!c.sm->abort) {
-        for (int i = c.tid; i < HD / 2; i += kConsumerThreads) rs[i] = __ldg(rope + i);
-        // q of the G heads, then (appending piece) k and v: pairs of tagged words, all of
+        if (MULTI) {
+            for (int i = c.tid; i < nrows * (HD / 2); i += kConsumerThreads) {
+                const int r = i / (HD / 2);
+                const int pr = r == 0 ? pos : c.sm->pos[piece_row(pc.rows, r)];
+                rs[i] = __ldg(p.rope + (size_t)pr * (HD / 2) + (i - r * (HD / 2)));
+            }
+        } else {
+            const float2* rope = p.rope + (size_t)pos * (HD / 2);
+            for (int i = c.tid; i < HD / 2; i += kConsumerThreads) rs[i] = __ldg(rope + i);
+        }
+        // q of the columns, then (appending piece) k and v: pairs of tagged words, all of
         // a thread's pairs in flight at once, polled until they carry the QKV tag
         const uint64_t* row = p.qkv + (size_t)b * p.qkv_rows;
         const uint32_t tq = tag_of(a, l, TAG_QKV);
-        const int nq = G * HD / 2, nt = nq + (has_last ? HD : 0);
-        constexpr int kPairs = (8 * HD / 2 + HD + kConsumerThreads - 1) / kConsumerThreads;
+        const int nq = NC * HD / 2, nt = nq + (has_last ? HD : 0);
+        constexpr int kPairs = ((MULTI ? 16 : 8) * HD / 2 + HD + kConsumerThreads - 1) / kConsumerThreads;
         auto src_of = [&](int i) -> const uint64_t* {
-            if (i < nq) return row + (size_t)g * G * HD + 2 * i;
+            if (i < nq) {
+                if (!MULTI) return row + (size_t)g * G * HD + 2 * i;
+                const int col = (2 * i) / HD, r = col / G;
+                return p.qkv + (size_t)piece_row(pc.rows, r) * p.qkv_rows +
+                       (size_t)(g * G + col - r * G) * HD + (2 * i - col * HD);
+            }
             const int j = i - nq;
             return j < HD / 2 ? row + (size_t)(p.Hq + g) * HD + 2 * j
                               : row + (size_t)(p.Hq + p.Hkv + g) * HD + 2 * (j - HD / 2);
@@ -1703,20 +1905,22 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
     consumer_sync();
     MK_PROF_MARK(c, PS_A_QSYNC);
     if (l == 1) MK_TRACE_C(c, TR_Q_SYNCED, 0);
-    // q^T (after RoPE) as the B operand: column gq = query head, k = head dims; hi/lo split.
-    // b0b1 of k-step s holds dims 16s + 2t, +1; b2b3 holds 16s + 8 + 2t, +1.
+    // q^T (after RoPE) as the B operand: column gq of this warp's tile, k = head dims;
+    // hi/lo split. b0b1 of k-step s holds dims 16s + 2t, +1; b2b3 holds 16s + 8 + 2t, +1.
+    const int qcol = tile * 8 + gq;
+    const float2* rq = MULTI ? rs + (qcol < NC ? qcol / G : 0) * (HD / 2) : rs;
     uint32_t qa[NKS][2], ql[NKS][2];
 #pragma unroll
     for (int s = 0; s < NKS; ++s)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             float v0 = 0.f, v1 = 0.f;
-            if (gq < G) {
+            if (qcol < NC) {
                 const int d = 16 * s + 8 * hh + 2 * t;
                 const int dp = d < HD / 2 ? d + HD / 2 : d - HD / 2;
-                const float4 cs = *reinterpret_cast<const float4*>(rs + (d % (HD / 2)));
-                const float2 x0 = *reinterpret_cast<const float2*>(qs + gq * QS + d);
-                const float2 xp = *reinterpret_cast<const float2*>(qs + gq * QS + dp);
+                const float4 cs = *reinterpret_cast<const float4*>(rq + (d % (HD / 2)));
+                const float2 x0 = *reinterpret_cast<const float2*>(qs + qcol * QS + d);
+                const float2 xp = *reinterpret_cast<const float2*>(qs + qcol * QS + dp);
                 if (d < HD / 2) {
                     v0 = x0.x * cs.x - xp.x * cs.y;
                     v1 = x0.y * cs.z - xp.y * cs.w;
@@ -1751,13 +1955,14 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
 #pragma unroll
     for (int i = 0; i < NMT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
     float* pbuf = c.scratch + c.cw * 32 * 9;  // P[32 keys][9] for this warp (fp32)
-    // Windows of 16 pages: warp w takes pages 2w and 2w + 1 (one ring slot holds PPS
-    // pages) and processes the two together, so two independent MMA chains hide each
-    // other's latency. Every warp waits for and releases every slot of the window in
-    // order (a slot is handed back only after its data has arrived).
-    constexpr int WIN = 2 * kConsumerWarps;
+    // Windows of 2 * wpt pages (16, or 8 with two column tiles): warp w of a tile takes
+    // pages 2w and 2w + 1 (one ring slot holds PPS pages) and processes the two together,
+    // so two independent MMA chains hide each other's latency. Every warp waits for and
+    // releases every slot of the window in order (a slot is handed back only after its
+    // data has arrived).
+    const int WIN = MULTI ? 2 * wpt : 2 * kConsumerWarps;
     const int lrow8 = c.lane & 7, lmi = c.lane >> 3;
-    const int pa = 2 * c.cw, mys = pa / PPS;
+    const int pa = 2 * wl, mys = pa / PPS;
 
     for (int w0 = 0; w0 < n; w0 += WIN) {
         const int nw = min(WIN, n - w0), nsl = (nw + PPS - 1) / PPS;
@@ -1887,10 +2092,12 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
 
     MK_PROF_MARK(c, PS_A_LOOP);
     if (l == 0) MK_TRACE_C(c, TR_A_LOOP, (uint32_t)n);
-    // this warp's softmax state for heads 2t, 2t+1 -> shared memory (rows padded to HD + 8)
+    // this warp's softmax state for local columns 2t, 2t+1 -> shared memory (rows padded
+    // to HD + 8), as many columns at a time as the scratch holds
     constexpr int OS = HD + 8;
-    float* ws_o = c.scratch;                                  // [8][G][OS]
-    float* ws_m = c.scratch + kConsumerWarps * G * OS;        // [8][8]
+    constexpr int kFC = FinishCols<HD>::value;
+    float* ws_o = c.scratch;                                  // [8][kFC][OS]
+    float* ws_m = c.scratch + kConsumerWarps * kFC * OS;      // [8][8]
     float* ws_l = ws_m + 64;                                  // [8][8]
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -1898,40 +2105,46 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, int b, int g, con
         l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 8);
         l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 16);
     }
-    consumer_sync();
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        const int h = 2 * t + hh;
-        if (h < G) {
-            if (gq == 0) { ws_m[c.cw * 8 + h] = m_run[hh]; ws_l[c.cw * 8 + h] = l_run[hh]; }
-#pragma unroll
-            for (int mt = 0; mt < NMT; ++mt) {
-                ws_o[(c.cw * G + h) * OS + 16 * mt + gq] = oacc[mt][hh];
-                ws_o[(c.cw * G + h) * OS + 16 * mt + gq + 8] = oacc[mt][2 + hh];
-            }
-        }
-    }
-    MK_PROF_MARK(c, PS_A_POST);
     c_in.seq = c.seq;
     c_in.tn = c.tn;
-    MK_PROF_BACK(c_in, c);
-    attention_finish<HD>(c_in, l, b, g, split);
+    const int ncl = MULTI ? min(8, NC) : 1;  // one pass for one row (G columns <= kFC)
+    for (int ch0 = 0; ch0 < ncl; ch0 += kFC) {
+        consumer_sync();  // the key loop's P buffers / the previous pass are done with it
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int h = 2 * t + hh;
+            if (MULTI ? (h >= ch0 && h < ch0 + kFC && tile * 8 + h < NC) : h < G) {
+                if (gq == 0) { ws_m[c.cw * 8 + h] = m_run[hh]; ws_l[c.cw * 8 + h] = l_run[hh]; }
+#pragma unroll
+                for (int mt = 0; mt < NMT; ++mt) {
+                    ws_o[(c.cw * kFC + h - ch0) * OS + 16 * mt + gq] = oacc[mt][hh];
+                    ws_o[(c.cw * kFC + h - ch0) * OS + 16 * mt + gq + 8] = oacc[mt][2 + hh];
+                }
+            }
+        }
+        MK_PROF_MARK(c, PS_A_POST);
+        MK_PROF_BACK(c_in, c);
+        attention_finish<HD, MULTI>(c_in, l, pc, ch0, NC, wpt);
+#ifdef MK_PROF
+        c.pt = c_in.pt;
+#endif
+    }
 }
 
 template <int HD>
-__device__ void attention_stage(Ctx& c, int l, int cta) {
+__device__ __noinline__ void attention_stage(Ctx& c, int l, int cta) {
     MK_PROF_MARK(c, PS_OTHER);
     MK_TRACE_C(c, TR_WAIT, l * 16 + ST_ATTN);
     // every piece first writes its partial record; then each split merges its slice
-    for_each_piece(*c.a, c.sm, l, cta, [&](int b, int g, const SeqSpan& sp, int u, int n,
-                                          int split, int nsplit) {
-        MK_TRACE_C(c, TR_PIECE, (uint32_t)(b * 256 + g));
-        attention_piece<HD>(c, l, b, g, sp, u, n, split, nsplit);
+    for_each_piece(*c.a, c.sm, l, cta, [&](const Piece& pc) {
+        MK_TRACE_C(c, TR_PIECE, (uint32_t)(pc.b * 256 + pc.g));
+        if (pc.prefix) attention_piece<HD, true>(c, l, pc);
+        else attention_piece<HD, false>(c, l, pc);
     });
-    for_each_piece(*c.a, c.sm, l, cta, [&](int b, int g, const SeqSpan&, int, int, int split,
-                                          int nsplit) {
-        attention_merge<HD>(c, l, b, g, split, nsplit);
-        MK_TRACE_C(c, TR_MERGE, (uint32_t)(b * 256 + g));
+    for_each_piece(*c.a, c.sm, l, cta, [&](const Piece& pc) {
+        if (pc.prefix) return;  // a shared prefix's records are merged by each row's own CTAs
+        attention_merge<HD>(c, l, pc.b, pc.g, pc.split, pc.nsplit, pc.nrec);
+        MK_TRACE_C(c, TR_MERGE, (uint32_t)(pc.b * 256 + pc.g));
     });
     // larger batches: every CTA counts its (possibly empty) share of the merges
     if (!tagged(*c.a)) publish(c, cnt_stage(l, ST_ATTN), l * 16 + ST_ATTN);
