@@ -287,6 +287,37 @@ def run_device_loop(S, steps, warmup, cfg, batch8=False):
     return one, starts, ends
 
 
+def multi_step_loop(S, launches, warmup, n):
+    """The same decode loop, n steps per launch (mk_decode_steps): each launch starts at
+    the next position of the cycle and takes the previous launch's last token. Returns
+    the mean milliseconds per step of the timed launches (CUDA events)."""
+    import torch
+    model = S["model"]
+    dev = S["pos"].device
+    total = warmup + launches
+    starts = torch.tensor([[CTX + (n * i) % CYCLE] for i in range(total)], dtype=torch.int32, device=dev)
+    sls = starts + 1
+    bufs = [torch.zeros((n, 1), dtype=torch.int32, device=dev) for _ in range(2)]
+    bufs[1][n - 1, 0] = S["tok0"]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def one(i):
+        model.steps(n, bufs[(i + 1) % 2][n - 1], starts[i], S["pt"], sls[i], bufs[i % 2])
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    ev[0].record()
+    for i in range(warmup, total):
+        one(i)
+    ev[1].record()
+    torch.cuda.synchronize()
+    code, task = model.status()
+    if code != 0:
+        raise RuntimeError(f"multi-step launches failed: status {code} task {task}")
+    return ev[0].elapsed_time(ev[1]) / (launches * n)
+
+
 def timed_region(one, warmup, steps, dist):
     import torch
     if dist:
@@ -591,6 +622,13 @@ def main():
         "hbm_gbs": round(achieved, 1), "pct_of_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2),
         "roofline": roof, "clocks": clk.summary(), "gpu_launches": args.steps,
     }
+    # the same loop with 16 steps per launch (tokens fed back inside the launch)
+    ms16 = multi_step_loop(S, max(1, args.steps // 16), 1, 16)
+    ach16 = algo / (ms16 / 1000.0) / 1e9
+    out["multi_step"] = {"steps_per_launch": 16, "ms_per_step": round(ms16, 4),
+                         "tokens_per_s": round(world * 1000.0 / ms16, 2), "hbm_gbs": round(ach16, 1),
+                         "frac_of_measured_peak": round(ach16 / peak, 4),
+                         "workload": "the headline workload through mk_decode_steps"}
     # batch 8 (secondary workload)
     if not args.no_batch8:
         cfg8 = synth.DENSE_2B_SWA.with_(n_layers=cfg.n_layers)

@@ -162,6 +162,26 @@ MK_API mk_status mk_decode_step(mk_handle *h, const int32_t *tokens, const int32
                          const int32_t *seq_lens, int32_t batch, int32_t *next_tokens,
                          float *logits, void *stream);
 
+/* n_steps consecutive decode steps of the same rows as ONE launch (the token of each
+ * step is fed back on the device). Source: "Kog AI: standart GPU'larda 3,000 token/s",
+ * on kernel boundaries and on sampling kept on the GPU.
+ *   tokens, positions, page_table, seq_lens, batch: as for mk_decode_step, for step 0.
+ *   Step s (0 <= s < n_steps) decodes at positions[b] + s; its input token is
+ *   tokens[b] for s = 0, else the token step s-1 chose. Every row's page table must
+ *   already map the pages of positions[b] + n_steps - 1.
+ *   next_tokens[n_steps][batch]  out: the token each step chose (greedy, or sampled as
+ *                       set by mk_set_sampling, with the step's own position)
+ *   logits              out: the LAST step's [batch][vocab] fp32, or NULL
+ * 1 <= n_steps <= 65536. The result equals n_steps calls of mk_decode_step that feed
+ * each step's next_tokens back as the next tokens. Inside the launch, each CTA's loader
+ * streams the next step's weights while the step's argmax is still being reduced.
+ * Errors as for mk_decode_step; the device check of positions covers the last step. */
+MK_API mk_status mk_decode_steps(mk_handle *h, int32_t n_steps, const int32_t *tokens,
+                                 const int32_t *positions, const int32_t *page_table,
+                                 int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                 int32_t batch, int32_t *next_tokens, float *logits,
+                                 void *stream);
+
 /* Waits for `stream`, then reads the device status word. Returns MK_OK or the
  * latched device error; *failing_task (may be NULL) receives the id of the task
  * that latched it (layer*16 + stage, or -1). */

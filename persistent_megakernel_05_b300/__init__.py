@@ -34,7 +34,7 @@ MK_OPT_PREFETCH_SLOTS = 3
 ABI_SYMBOLS = ("mk_create", "mk_kv_alloc", "mk_kv_free", "mk_decode_step", "mk_status_sync",
                "mk_status_reset", "mk_set_option", "mk_get_info", "mk_debug_buffer",
                "mk_status_string", "mk_destroy", "mk_decode_step_noalloc", "mk_set_sampling",
-               "mk_set_shared_prefix")
+               "mk_set_shared_prefix", "mk_decode_steps")
 MK_NOALLOC_SCRATCH_BYTES = 8 << 20
 MK_BUF_X, MK_BUF_QKV, MK_BUF_ATTN, MK_BUF_H, MK_BUF_ROUTE, MK_BUF_MOE_UNION = 1, 2, 3, 4, 5, 6
 
@@ -108,6 +108,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mk_kv_free.argtypes = [_vp, _P(mk_kv_pool)]
     L.mk_decode_step.restype = ctypes.c_int
     L.mk_decode_step.argtypes = [_vp, _vp, _vp, _vp, i32, _vp, i32, _vp, _vp, _vp]
+    L.mk_decode_steps.restype = ctypes.c_int
+    L.mk_decode_steps.argtypes = [_vp, i32, _vp, _vp, _vp, i32, _vp, i32, _vp, _vp, _vp]
     L.mk_status_sync.restype = ctypes.c_int
     L.mk_status_sync.argtypes = [_vp, _vp, _P(i32)]
     L.mk_status_reset.restype = ctypes.c_int
@@ -170,6 +172,15 @@ def mk_decode_step(handle: int, tokens: int, positions: int, page_table: int,
     """Raw call with device addresses (ints). Returns the mk_status code."""
     return load().mk_decode_step(handle, tokens, positions, page_table, max_pages_per_seq,
                                  seq_lens, batch, next_tokens, logits, stream)
+
+
+def mk_decode_steps(handle: int, n_steps: int, tokens: int, positions: int, page_table: int,
+                    max_pages_per_seq: int, seq_lens: int, batch: int, next_tokens: int,
+                    logits: Optional[int], stream: Optional[int] = None) -> int:
+    """Raw call with device addresses (ints): n_steps steps in one launch. Returns the
+    mk_status code."""
+    return load().mk_decode_steps(handle, n_steps, tokens, positions, page_table,
+                                  max_pages_per_seq, seq_lens, batch, next_tokens, logits, stream)
 
 
 def mk_status_sync(handle: int, stream: Optional[int] = None):
@@ -342,6 +353,25 @@ class DecodeModel:
                               next_tokens.data_ptr(),
                               logits.data_ptr() if logits is not None else None, s.cuda_stream)
         _check(code, "mk_decode_step")
+
+    def steps(self, n_steps, tokens, positions, page_table, seq_lens, next_tokens, logits=None,
+              stream=None):
+        """Enqueues n_steps decode steps as one launch: step s > 0 takes step s-1's tokens
+        at positions + s. next_tokens is [n_steps][B] int32; logits (optional) receives the
+        last step's [B][vocab] fp32."""
+        import torch
+        for t in (tokens, positions, page_table, seq_lens, next_tokens):
+            assert t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()
+        B = tokens.shape[0]
+        assert next_tokens.numel() >= n_steps * B
+        if logits is not None:
+            assert logits.is_cuda and logits.dtype == torch.float32 and logits.is_contiguous()
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        code = mk_decode_steps(self.handle, int(n_steps), tokens.data_ptr(), positions.data_ptr(),
+                               page_table.data_ptr(), page_table.shape[1], seq_lens.data_ptr(), B,
+                               next_tokens.data_ptr(),
+                               logits.data_ptr() if logits is not None else None, s.cuda_stream)
+        _check(code, "mk_decode_steps")
 
     def status(self, stream=None):
         import torch

@@ -226,7 +226,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     const size_t o_xf = take(sizeof(float) * (size_t)maxB * d);
     const size_t o_attnf = take(sizeof(float) * (size_t)maxB * Hq * hd);
     const size_t o_hf = take(sizeof(float) * (size_t)maxB * hrow);
-    const size_t o_am = take(sizeof(float2) * (size_t)C * maxB);
+    const size_t o_am = take(16 * (size_t)C * maxB);  // tagged (value, index) pairs
     h->counters_words = (size_t)(1 + L * mk::kStagesPerLayer) * mk::kCounterStride;
     h->arrivals_words = (size_t)mk::kCounterStride;
     const size_t o_cnt = take(sizeof(uint32_t) * h->counters_words);
@@ -321,7 +321,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     p.attnf = (float*)(base + o_attnf);
     p.hf = (float*)(base + o_hf);
     p.counters = (uint32_t*)(base + o_cnt);
-    p.amax_part = (float2*)(base + o_am);
+    p.amax = (uint64_t*)(base + o_am);
     p.arrivals = (uint32_t*)(base + o_arr);
     p.status = (int*)(base + o_status);
     p.kv = nullptr;
@@ -397,13 +397,21 @@ mk_status mk_kv_free(mk_handle* h, mk_kv_pool* pool) {
     return MK_OK;
 }
 
-mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* positions,
-                         const int32_t* page_table, int32_t max_pages_per_seq,
-                         const int32_t* seq_lens, int32_t batch, int32_t* next_tokens,
-                         float* logits, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// decode steps one launch may run (the loader's MoE readiness words encode step * 128)
+constexpr int32_t kMaxStepsPerLaunch = 1 << 16;
+
+// One launch of the decode kernel for n_steps consecutive steps (see mk_decode_steps).
+mk_status launch_steps(mk_handle* h, int32_t n_steps, const int32_t* tokens, const int32_t* positions,
+                       const int32_t* page_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                       int32_t batch, int32_t* next_tokens, float* logits, void* stream) {
     if (!h || !tokens || !positions || !page_table || !seq_lens || !next_tokens)
         return MK_ERR_INVALID_ARG;
     if (batch < 1 || batch > h->desc.max_batch || max_pages_per_seq < 1) return MK_ERR_INVALID_ARG;
+    if (n_steps < 1 || n_steps > kMaxStepsPerLaunch) return MK_ERR_INVALID_ARG;
     // the kernel partitions attention units in 32-bit arithmetic
     if ((uint64_t)batch * h->desc.n_kv_heads * max_pages_per_seq * h->num_ctas >= (1ull << 31))
         return MK_ERR_INVALID_ARG;
@@ -419,14 +427,18 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
     a.page_table = page_table;
     a.seq_lens = seq_lens;
     a.next_tokens = next_tokens;
-    a.logits = logits;
+    a.n_steps = n_steps;
+    a.logits_last = logits;
+    a.logits = n_steps == 1 ? logits : nullptr;  // the kernel sets it for the last step
     a.max_pages = max_pages_per_seq;
     a.B = batch;
-    // 20-bit epochs, never 0 (zeroed memory never carries a valid tag)
+    // 20-bit epochs, never 0 (zeroed memory never carries a valid tag); step s of the
+    // launch uses the s-th epoch after the first
     const uint32_t epoch = h->epoch % 0xFFFFFu + 1u;
     a.epoch = epoch;
     // the stage counters only advance in steps whose batch exceeds the tagged-word limit
-    const uint32_t cnt_epoch = h->cnt_epoch + (batch > mk::kMaxTaggedBatch ? 1u : 0u);
+    const bool counted = batch > mk::kMaxTaggedBatch;
+    const uint32_t cnt_epoch = h->cnt_epoch + (counted ? 1u : 0u);
     a.stage_target = cnt_epoch * (uint32_t)h->num_ctas;
     a.skip_publish = h->skip_publish;
     a.prefetch_slots = h->prefetch_slots;
@@ -448,11 +460,32 @@ mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* pos
         cudaGetLastError();
         return MK_ERR_LAUNCH;
     }
-    h->epoch = epoch;
-    h->cnt_epoch = cnt_epoch;
+    h->epoch = (uint32_t)((epoch - 1u + (uint32_t)(n_steps - 1)) % 0xFFFFFu) + 1u;
+    h->cnt_epoch = cnt_epoch + (counted ? (uint32_t)(n_steps - 1) : 0u);
     h->last_batch = batch;
     return MK_OK;
 }
+
+}  // namespace
+
+extern "C" {
+
+mk_status mk_decode_step(mk_handle* h, const int32_t* tokens, const int32_t* positions,
+                         const int32_t* page_table, int32_t max_pages_per_seq,
+                         const int32_t* seq_lens, int32_t batch, int32_t* next_tokens,
+                         float* logits, void* stream) {
+    return launch_steps(h, 1, tokens, positions, page_table, max_pages_per_seq, seq_lens, batch,
+                        next_tokens, logits, stream);
+}
+
+mk_status mk_decode_steps(mk_handle* h, int32_t n_steps, const int32_t* tokens,
+                          const int32_t* positions, const int32_t* page_table,
+                          int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                          int32_t* next_tokens, float* logits, void* stream) {
+    return launch_steps(h, n_steps, tokens, positions, page_table, max_pages_per_seq, seq_lens,
+                        batch, next_tokens, logits, stream);
+}
+
 
 mk_status mk_status_sync(mk_handle* h, void* stream, int32_t* failing_task) {
     if (!h) return MK_ERR_INVALID_ARG;
@@ -726,13 +759,13 @@ extern "C" mk_status mk_decode_step_noalloc(
     const size_t o_layers = take(sizeof(mk::LayerPlan) * L);
     const size_t o_gains = take(sizeof(float) * (size_t)(2 * L + 1) * d);
     const size_t o_rope = take(sizeof(float2) * (size_t)desc->max_positions * (hd / 2));
-    const size_t o_am = take(sizeof(float2) * (size_t)C * maxB);
     const size_t o_xf = take(sizeof(float) * (size_t)maxB * d);
     const size_t o_attnf = take(sizeof(float) * (size_t)maxB * Hq * hd);
     const size_t o_hf = take(sizeof(float) * (size_t)maxB * hrow);
     const size_t o_union = take(sizeof(int) * (size_t)L);
     // cleared every call (every call runs with tag epoch 1 and counter epoch 1): the
-    // tagged activations and attention partials, the counters and the status word
+    // tagged activations, attention partials and argmax pairs, the counters and the
+    // status word
     const size_t o_zero = off;
     const size_t o_x = take(8 * (size_t)maxB * d);
     const size_t o_qkv = take(8 * (size_t)maxB * qkv_rows);
@@ -740,6 +773,7 @@ extern "C" mk_status mk_decode_step_noalloc(
     const size_t o_h = take(8 * (size_t)maxB * hrow);
     const size_t o_part = take(8 * (size_t)maxB * Hkv * C * (G * hd + 2 * G));
     const size_t o_route = take(8 * (size_t)maxB * (E > 0 ? E : 1));
+    const size_t o_am = take(16 * (size_t)C * maxB);  // tagged (value, index) pairs
     const size_t o_cnt = take(sizeof(uint32_t) * (size_t)(1 + L * mk::kStagesPerLayer) * mk::kCounterStride);
     const size_t o_arr = take(sizeof(uint32_t) * mk::kCounterStride);
     const size_t o_status = take(sizeof(int) * 4);
@@ -819,7 +853,7 @@ extern "C" mk_status mk_decode_step_noalloc(
     p.attnf = (float*)(base + o_attnf);
     p.hf = (float*)(base + o_hf);
     p.counters = (uint32_t*)(base + o_cnt);
-    p.amax_part = (float2*)(base + o_am);
+    p.amax = (uint64_t*)(base + o_am);
     p.arrivals = (uint32_t*)(base + o_arr);
     p.status = (int*)(base + o_status);
     p.kv = (bf16*)kv_pool;
@@ -839,6 +873,8 @@ extern "C" mk_status mk_decode_step_noalloc(
     a.timeout_ns = 1000000000LL;
     a.temperature = 0.f;  // greedy
     a.seed_lo = a.seed_hi = 0;
+    a.n_steps = 1;
+    a.logits_last = logits;
     a.pf_on = 0;  // no shared-prefix groups
     for (int b = 0; b < mk::kMaxBatch; ++b) {
         a.pf_lead[b] = -1;

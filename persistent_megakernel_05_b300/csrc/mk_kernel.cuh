@@ -147,8 +147,8 @@ struct Plan {
     float* attnf;
     float* hf;
     uint32_t* counters;                 // stage counters, kCounterStride apart
-    float2* amax_part;                  // [C][maxB] (value, index as float bits)
-    uint32_t* arrivals;                 // argmax arrival counter
+    uint64_t* amax;                     // [C][maxB][2] tagged (value, index as float bits)
+    uint32_t* arrivals;                 // (unused by the kernel; zeroed with the counters)
     int* status;                        // [0] code, [1] task
     bf16* kv;                           // paged pool base
 };
@@ -179,6 +179,10 @@ struct StepArgs {
     int pf_on;
     int pf_lead[kMaxBatch];
     int pf_pages[kMaxBatch];
+    // decode steps in this launch: step s > 0 takes step s-1's tokens as input, at
+    // positions + s; next_tokens is [n_steps][B]; logits (if any) are the last step's
+    int n_steps;
+    float* logits_last;
 };
 
 // Up to this batch size the activations between stages travel as tagged words (one
@@ -209,7 +213,11 @@ struct Smem {
     float rstd[kMaxBatch];
     float amax_v[kMaxBatch];
     int amax_i[kMaxBatch];
-    int pos[kMaxBatch];
+    int pos[kMaxBatch];                    // consumers' positions of their current step
+    int ppos[kMaxBatch];                   // the loader's positions of its current step
+    int tok[kMaxBatch];                    // the next step's input tokens
+    volatile int step_ready;               // steps whose K/V appends the loader may read
+    int cstep;                             // the consumers' step of this launch
     float ssq[kConsumerWarps][kMaxBatch];  // per-warp sums of squares (fused RMSNorm)
     float xown[kMaxBatch][kMaxOwnRows];    // this CTA's rows of the residual stream
     volatile int abort;
@@ -223,7 +231,7 @@ struct Smem {
     StepArgs args;
     __align__(16) LayerPlan lp[2];  // consumers' copies of the plans of layers l (l & 1) and l + 1
     // MoE routing of the current layer, written by the consumers, read by the loader too
-    volatile int moe_ready;            // layer + 1 whose routing is below
+    volatile int moe_ready;            // step * kMaxLayers + layer + 1 whose routing is below
     int moe_nu;                        // experts in the union of the batch rows' routes
     int moe_uni[kMaxExperts];          // that union, ascending expert id
     float moe_w[kMaxBatch][kMaxExperts];  // routing weight of union slot j for row b (0: not routed)
@@ -547,9 +555,9 @@ __device__ __forceinline__ SlotGeom slot_geom(const GemvStage& s, int k0) {
 // ---- attention work partition (identical in producer and consumers) ----
 struct SeqSpan { int lo, pos, p0, np; };  // attended keys [lo, pos], logical pages [p0, p0+np)
 
-__device__ __forceinline__ SeqSpan seq_span(const Plan& p, const Smem* sm, int l, int b) {
+__device__ __forceinline__ SeqSpan seq_span(const Plan& p, const int* posv, int l, int b) {
     SeqSpan s;
-    s.pos = sm->pos[b];
+    s.pos = posv[b];
     s.lo = (p.window > 0 && p.layers[l].sliding) ? max(0, s.pos - p.window + 1) : 0;
     s.p0 = s.lo / kPage;
     s.np = s.pos / kPage - s.p0 + 1;
@@ -570,7 +578,7 @@ struct Groups {
     __device__ __forceinline__ uint32_t members(int L) const { return (uint32_t)(rows >> (8 * L)) & 0xffu; }
 };
 
-__device__ __forceinline__ Groups prefix_groups(const StepArgs& a, const Smem* sm, int l) {
+__device__ __forceinline__ Groups prefix_groups(const StepArgs& a, const int* posv, int l) {
     Groups gr{0u, 0ull};
     if (!a.pf_on) return gr;
     uint64_t rows = 0;
@@ -584,7 +592,7 @@ __device__ __forceinline__ Groups prefix_groups(const StepArgs& a, const Smem* s
         bool ok = true;
         for (int r = 0; r < a.B; ++r)
             if ((m >> r) & 1u) {
-                const SeqSpan sp = seq_span(a.p, sm, l, r);
+                const SeqSpan sp = seq_span(a.p, posv, l, r);
                 ok = ok && sp.lo == 0 && a.pf_pages[L] <= sp.pos / kPage;
             }
         if (!ok) continue;
@@ -618,10 +626,10 @@ struct Piece {
 // CTAs (no prefix groups then), (b, g, page) units are dealt out in contiguous ranges.
 // Items of one row each (no prefix groups): (b, g) in row-major order.
 template <typename F>
-__device__ __forceinline__ void for_each_row_piece(const StepArgs& a, const Smem* sm, int l, int cta, F&& f) {
+__device__ __forceinline__ void for_each_row_piece(const StepArgs& a, const int* posv, int l, int cta, F&& f) {
     const Plan& p = a.p;
     uint32_t U = 0;
-    for (int b = 0; b < a.B; ++b) U += (uint32_t)(p.Hkv * seq_span(p, sm, l, b).np);
+    for (int b = 0; b < a.B; ++b) U += (uint32_t)(p.Hkv * seq_span(p, posv, l, b).np);
     const uint32_t C = (uint32_t)p.C;
     const uint32_t W = (uint32_t)(a.B * p.Hkv);
     Piece pc;
@@ -631,7 +639,7 @@ __device__ __forceinline__ void for_each_row_piece(const StepArgs& a, const Smem
         const uint32_t Cp = C - W;
         uint32_t S = 0, i = 0;
         for (int b = 0; b < a.B; ++b) {
-            const SeqSpan sp = seq_span(p, sm, l, b);
+            const SeqSpan sp = seq_span(p, posv, l, b);
             for (int g = 0; g < p.Hkv; ++g, ++i) {
                 const uint32_t c0 = i + Cp * S / U;
                 S += (uint32_t)sp.np;
@@ -657,7 +665,7 @@ __device__ __forceinline__ void for_each_row_piece(const StepArgs& a, const Smem
     auto first_cta = [&](uint32_t s) -> int { return (int)(((s + 1) * C - 1) / U); };
     uint32_t s = 0;
     for (int b = 0; b < a.B; ++b) {
-        const SeqSpan sp = seq_span(p, sm, l, b);
+        const SeqSpan sp = seq_span(p, posv, l, b);
         for (int g = 0; g < p.Hkv; ++g) {
             const uint32_t e = s + (uint32_t)sp.np;
             const uint32_t lo = max(s, u0), hi = min(e, u1);
@@ -677,27 +685,33 @@ __device__ __forceinline__ void for_each_row_piece(const StepArgs& a, const Smem
 }
 
 template <typename F>
-__device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta, F&& f) {
-    if (!a.pf_on) {
-        for_each_row_piece(a, sm, l, cta, f);
-        return;
-    }
+__device__ __noinline__ void for_each_group_piece(const StepArgs& a, const int* posv, int l, int cta, F& f);
+
+template <typename F>
+__device__ __forceinline__ void for_each_piece(const StepArgs& a, const int* posv, int l, int cta, F&& f) {
+    if (!a.pf_on) for_each_row_piece(a, posv, l, cta, f);
+    else for_each_group_piece(a, posv, l, cta, f);
+}
+
+// for_each_piece with shared-prefix groups declared (out of line: rarely taken)
+template <typename F>
+__device__ __noinline__ void for_each_group_piece(const StepArgs& a, const int* posv, int l, int cta, F& f) {
     const Plan& p = a.p;
     // 32-bit unsigned unit arithmetic: U * C < 2^31 (checked on the host)
     const uint32_t C = (uint32_t)p.C;
-    const Groups gr = prefix_groups(a, sm, l);
+    const Groups gr = prefix_groups(a, posv, l);
     int ng = 0;
     for (int L = 0; L < a.B; ++L) ng += gr.members(L) != 0u;
     const uint32_t W = (uint32_t)((a.B + ng) * p.Hkv);
     // no active group in this layer, or more items than CTAs: every row on its own
     if (ng == 0 || W > C) {
-        for_each_row_piece(a, sm, l, cta, f);
+        for_each_row_piece(a, posv, l, cta, f);
         return;
     }
     {
         uint32_t U = 0;
         for (int b = 0; b < a.B; ++b) {
-            const SeqSpan sp = seq_span(p, sm, l, b);
+            const SeqSpan sp = seq_span(p, posv, l, b);
             const int L = gr.leader(b);
             if (L == b) U += (uint32_t)a.pf_pages[L];
             U += (uint32_t)(L >= 0 ? sp.pos / kPage - a.pf_pages[L] + 1 : sp.np);
@@ -708,7 +722,7 @@ __device__ void for_each_piece(const StepArgs& a, const Smem* sm, int l, int cta
         int ncs[kMaxBatch];  // splits of each group's prefix item (this kv head)
         for (int g = 0; g < p.Hkv; ++g) {
             for (int b = 0; b < a.B; ++b) {
-                const SeqSpan full = seq_span(p, sm, l, b);
+                const SeqSpan full = seq_span(p, posv, l, b);
                 const int L = gr.leader(b);
                 if (L == b) {  // the group's shared prefix, ahead of its rows' own pages
                     const int P = a.pf_pages[L];
@@ -873,7 +887,7 @@ struct Producer {
         constexpr int NB = HD / 64;     // 64-wide boxes per page row
         MK_TRACE_P(*this, TR_P_STAGE, l * 16 + ST_ATTN);
         bool ok = true;
-        for_each_piece(*a, sm, l, cta, [&](const Piece& pc) {
+        for_each_piece(*a, sm->ppos, l, cta, [&](const Piece& pc) {
             if (!ok) return;
             const int b = pc.b, g = pc.g, u = pc.u, n = pc.n;
             const SeqSpan& sp = pc.sp;
@@ -919,11 +933,11 @@ struct Producer {
     // A MoE layer's expert rows depend on its routing, which this CTA's consumers compute
     // from the router logits: wait until they publish it (bounded; on abort or time-out
     // the loader stops, and the consumers report the cause).
-    __device__ bool wait_route(int l) {
+    __device__ bool wait_route(int step, int l) {
         int ok = 1;
         if (lane == 0) {
             uint64_t t0 = 0;
-            for (int it = 0; sm->moe_ready != l + 1; ++it) {
+            for (int it = 0; sm->moe_ready != step * kMaxLayers + l + 1; ++it) {
                 if (sm->abort) { ok = 0; break; }
                 __nanosleep(64);
                 if ((it & 63) == 63) {
@@ -942,24 +956,53 @@ struct Producer {
         return __shfl_sync(0xffffffffu, ok, 0) != 0;
     }
 
+    // Step `step` of a multi-step launch reads pages that the previous step appended to
+    // (in other CTAs, by generic stores): wait until this CTA's consumers have seen every
+    // CTA finish that step (each released its stores before its argmax record), then
+    // order the coming TMA reads after that (bounded; on abort or time-out: stop).
+    __device__ bool wait_step(int step) {
+        int ok = 1;
+        if (lane == 0) {
+            uint64_t t0 = 0;
+            for (int it = 0; sm->step_ready < step; ++it) {
+                if (sm->abort) { ok = 0; break; }
+                __nanosleep(64);
+                if ((it & 63) == 63) {
+                    const uint64_t now = globaltimer();
+                    if (t0 == 0) t0 = now;
+                    else if ((long long)(now - t0) > 4 * a->timeout_ns) { ok = 0; break; }
+                }
+            }
+            __threadfence_block();
+        }
+        __syncwarp();
+        fence_proxy_async_global();
+        return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    }
+
     template <int HD>
     __device__ __noinline__ void run(int cta) {
         policy = policy_evict_first();
         if (lane == 0) prefetch_tmap(tmap);
         const Plan& p = a->p;
         bool ok = !sm->abort;
-        for (int l = 0; l < p.L && ok; ++l) {
-            ok = ok && gemv(make_gemv(*a, G_QKV, l, sm), cta);
-            ok = ok && attention<HD>(l, cta);
-            ok = ok && gemv(make_gemv(*a, G_O, l, sm), cta);
-            if (p.E > 0) {
-                ok = ok && gemv(make_gemv(*a, G_ROUTE, l, sm), cta);
-                ok = ok && wait_route(l);
+        for (int step = 0; step < a->n_steps && ok; ++step) {
+            if (step > 0 && lane < a->B) sm->ppos[lane] += 1;
+            __syncwarp();
+            for (int l = 0; l < p.L && ok; ++l) {
+                ok = ok && gemv(make_gemv(*a, G_QKV, l, sm), cta);
+                if (step > 0 && l == 0) ok = ok && wait_step(step);
+                ok = ok && attention<HD>(l, cta);
+                ok = ok && gemv(make_gemv(*a, G_O, l, sm), cta);
+                if (p.E > 0) {
+                    ok = ok && gemv(make_gemv(*a, G_ROUTE, l, sm), cta);
+                    ok = ok && wait_route(step, l);
+                }
+                ok = ok && gemv(make_gemv(*a, G_GU, l, sm), cta);
+                ok = ok && gemv(make_gemv(*a, G_DOWN, l, sm), cta);
             }
-            ok = ok && gemv(make_gemv(*a, G_GU, l, sm), cta);
-            ok = ok && gemv(make_gemv(*a, G_DOWN, l, sm), cta);
+            if (ok) ok = gemv(make_gemv(*a, G_LM, 0, sm), cta);
         }
-        if (ok) gemv(make_gemv(*a, G_LM, 0, sm), cta);
         // drain: never leave a copy in flight into shared memory
         if (lane == 0 && !pf) {
             const uint32_t first = seq > (uint32_t)kStages ? seq - kStages : 0;
@@ -2136,12 +2179,12 @@ __device__ __noinline__ void attention_stage(Ctx& c, int l, int cta) {
     MK_PROF_MARK(c, PS_OTHER);
     MK_TRACE_C(c, TR_WAIT, l * 16 + ST_ATTN);
     // every piece first writes its partial record; then each split merges its slice
-    for_each_piece(*c.a, c.sm, l, cta, [&](const Piece& pc) {
+    for_each_piece(*c.a, c.sm->pos, l, cta, [&](const Piece& pc) {
         MK_TRACE_C(c, TR_PIECE, (uint32_t)(pc.b * 256 + pc.g));
         if (pc.prefix) attention_piece<HD, true>(c, l, pc);
         else attention_piece<HD, false>(c, l, pc);
     });
-    for_each_piece(*c.a, c.sm, l, cta, [&](const Piece& pc) {
+    for_each_piece(*c.a, c.sm->pos, l, cta, [&](const Piece& pc) {
         if (pc.prefix) return;  // a shared prefix's records are merged by each row's own CTAs
         attention_merge<HD>(c, l, pc.b, pc.g, pc.split, pc.nsplit, pc.nrec);
         MK_TRACE_C(c, TR_MERGE, (uint32_t)(pc.b * 256 + pc.g));
@@ -2162,7 +2205,7 @@ __device__ void embed_stage(Ctx& c, int cta) {
     if (!c.sm->abort)
         for (int e = c.tid; e < a.B * nr; e += kConsumerThreads) {
             const int b = e / nr, k = a0 + e % nr;
-            const int tok = __ldg(a.tokens + b);
+            const int tok = c.sm->cstep == 0 ? __ldg(a.tokens + b) : c.sm->tok[b];
             const float v = __bfloat162float(p.embed[(size_t)tok * p.d + k]);
             const size_t o = (size_t)b * p.d + perm_col(k);
             if (!tagged(a)) p.xf[o] = v;
@@ -2172,32 +2215,60 @@ __device__ void embed_stage(Ctx& c, int cta) {
     if (!tagged(a)) publish(c, cnt_embed(), -2);
 }
 
+// After the LM head: every CTA writes its running argmax of each row as a tagged pair
+// (value, index); CTA 0 reads every CTA's pairs and reduces them (largest value, lowest
+// index on ties) into next_tokens. When another step of the launch follows, every CTA
+// reduces them itself (its next embedding needs the tokens), and each first releases the
+// step's K/V appends, which the next step's TMA page loads in other CTAs will read.
 __device__ void argmax_finish(Ctx& c, int cta) {
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
+    const int step = c.sm->cstep;
+    const bool more = step + 1 < a.n_steps;
+    const int task = p.L * 16;
+    const uint32_t tag = tag_of(a, p.L, TAG_EMBED);  // layer index L: no other write uses it
     consumer_sync();  // every warp's LM-head epilogue has updated amax_v / amax_i
-    if (c.tid < a.B)
-        p.amax_part[(size_t)cta * p.maxB + c.tid] =
-            make_float2(c.sm->amax_v[c.tid], __int_as_float(c.sm->amax_i[c.tid]));
-    consumer_sync();
-    if (c.tid == 0) {
-        int last = 0;
-        if (!c.sm->abort && a.skip_publish != p.L * 16) {
-            uint32_t* ctr = p.arrivals + ((size_t)p.L * p.maxB * p.Hkv) * kCounterStride;
-            const uint32_t old = atom_acq_rel_add(ctr, 1u);
-            if (old == (uint32_t)(p.C - 1)) { last = 1; st_relaxed(ctr, 0u); }
+    if (c.tid == 0 && !c.sm->abort && a.skip_publish != task) {
+        if (more) {
+            fence_proxy_async_global();
+            __threadfence();
         }
-        c.sm->bcast = last;
+        for (int b = 0; b < a.B; ++b)
+            ll_st2(p.amax + ((size_t)cta * p.maxB + b) * 2, c.sm->amax_v[b],
+                   __int_as_float(c.sm->amax_i[b]), tag);
     }
-    consumer_sync();
-    if (c.sm->bcast && c.cw < a.B) {
+    if (!more && cta != 0) return;
+    if (c.cw < a.B) {
         const int b = c.cw;
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-        for (int k = c.lane; k < p.C; k += 32) {
-            const float2 v = __ldcg(&p.amax_part[(size_t)k * p.maxB + b]);
-            const int vi = __float_as_int(v.y);
-            if (v.x > bv || (v.x == bv && vi < bi)) { bv = v.x; bi = vi; }
+        // up to 8 CTAs' pairs per lane in flight at once; a missing pair is then awaited
+        // alone and the batch re-read
+        for (int k0 = c.lane; k0 < p.C; k0 += 8 * 32) {
+            uint64_t w[8][2];
+            Spin sp;
+            for (;;) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int k = k0 + 32 * j;
+                    w[j][0] = w[j][1] = (uint64_t)tag << 32;
+                    if (k < p.C) ll_ld2(p.amax + ((size_t)k * p.maxB + b) * 2, w[j][0], w[j][1]);
+                }
+                int miss = -1;
+#pragma unroll
+                for (int j = 7; j >= 0; --j)
+                    if (ll_tag(w[j][0]) != tag || ll_tag(w[j][1]) != tag) miss = j;
+                if (miss < 0 || !ll_wait_pair(p.amax + ((size_t)(k0 + 32 * miss) * p.maxB + b) * 2, tag,
+                                              sp, a, c.sm, task))
+                    break;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (k0 + 32 * j >= p.C) continue;
+                const float v = ll_val(w[j][0]);
+                const int vi = __float_as_int(ll_val(w[j][1]));
+                if (v > bv || (v == bv && vi < bi)) { bv = v; bi = vi; }
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -2205,8 +2276,31 @@ __device__ void argmax_finish(Ctx& c, int cta) {
             const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
             if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
         }
-        if (c.lane == 0) a.next_tokens[b] = bi == 0x7fffffff ? 0 : bi;
+        const int tok = bi == 0x7fffffff ? 0 : bi;
+        if (c.lane == 0) {
+            c.sm->tok[b] = tok;
+            if (cta == 0) a.next_tokens[(size_t)step * a.B + b] = tok;
+        }
     }
+    if (!more) return;
+    consumer_sync();  // the tokens are in shared memory; every warp is past this step's reads
+    if (c.tid == 0) {
+        __threadfence();  // the pairs read above: acquire the step's K/V appends they released
+        fence_proxy_async_global();
+        c.sm->step_ready = step + 1;
+        c.sm->cstep = step + 1;
+        // the consumers' step arguments for the next step (the loader reads none of these)
+        StepArgs& m = *const_cast<StepArgs*>(c.a);
+        m.epoch = m.epoch % 0xFFFFFu + 1u;
+        if (!tagged(m)) m.stage_target += (uint32_t)p.C;
+        if (step + 2 == m.n_steps) m.logits = m.logits_last;
+        for (int b = 0; b < m.B; ++b) {
+            c.sm->pos[b] += 1;
+            c.sm->amax_v[b] = -INFINITY;
+            c.sm->amax_i[b] = 0x7fffffff;
+        }
+    }
+    consumer_sync();
 }
 
 // MoE routing of layer l (every CTA, identically): warp b polls row b's E router logits,
@@ -2304,7 +2398,7 @@ __device__ __noinline__ void moe_route(Ctx& c_in, int l) {
     if (l == 1) MK_TRACE_C(c, TR_R_DONE, 0);
     if (c.tid == 0) {
         __threadfence_block();  // the routing above before the flag the loader waits on
-        c.sm->moe_ready = l + 1;
+        c.sm->moe_ready = c.sm->cstep * kMaxLayers + l + 1;
     }
     c_in.tn = c.tn;
     MK_PROF_BACK(c_in, c);
@@ -2329,27 +2423,30 @@ __device__ void consumer_run(Ctx& c, int cta) {
     const long long t_start = clock64();
     c.pt = t_start;
 #endif
-    fetch_plan(0);
-    embed_stage(c, cta);
-    MK_PROF_MARK(c, PS_EMBED);
-    for (int l = 0; l < p.L; ++l) {
-        if (c.tid < kPlanChunks) cp_async_wait_all();
-        consumer_sync();  // layer l's plan is in place; slot (l + 1) & 1 is free
-        const LayerPlan& lp = c.sm->lp[l & 1];
-        gemv_stage(c, make_gemv(*c.a, G_QKV, l, lp, c.sm), cta);
-        if (l + 1 < p.L) fetch_plan(l + 1);  // read at the next layer, after a barrier
-        attention_stage<HD>(c, l, cta);
-        gemv_stage(c, make_gemv(*c.a, G_O, l, lp, c.sm), cta);
-        if (p.E > 0) {
-            gemv_stage(c, make_gemv(*c.a, G_ROUTE, l, lp, c.sm), cta);
-            moe_route(c, l);
+    for (int step = 0; step < c.a->n_steps; ++step) {  // (sm->cstep advances in argmax_finish)
+        fetch_plan(0);
+        embed_stage(c, cta);
+        MK_PROF_MARK(c, PS_EMBED);
+        for (int l = 0; l < p.L; ++l) {
+            if (c.tid < kPlanChunks) cp_async_wait_all();
+            consumer_sync();  // layer l's plan is in place; slot (l + 1) & 1 is free
+            const LayerPlan& lp = c.sm->lp[l & 1];
+            gemv_stage(c, make_gemv(*c.a, G_QKV, l, lp, c.sm), cta);
+            if (l + 1 < p.L) fetch_plan(l + 1);  // read at the next layer, after a barrier
+            attention_stage<HD>(c, l, cta);
+            gemv_stage(c, make_gemv(*c.a, G_O, l, lp, c.sm), cta);
+            if (p.E > 0) {
+                gemv_stage(c, make_gemv(*c.a, G_ROUTE, l, lp, c.sm), cta);
+                moe_route(c, l);
+            }
+            gemv_stage(c, make_gemv(*c.a, G_GU, l, lp, c.sm), cta);
+            gemv_stage(c, make_gemv(*c.a, G_DOWN, l, lp, c.sm), cta);
         }
-        gemv_stage(c, make_gemv(*c.a, G_GU, l, lp, c.sm), cta);
-        gemv_stage(c, make_gemv(*c.a, G_DOWN, l, lp, c.sm), cta);
+        gemv_stage(c, make_gemv(*c.a, G_LM, 0, c.sm->lp[0], c.sm), cta);
+        argmax_finish(c, cta);
+        MK_PROF_MARK(c, PS_ARGMAX);
+        if (c.sm->abort) break;
     }
-    gemv_stage(c, make_gemv(*c.a, G_LM, 0, c.sm->lp[0], c.sm), cta);
-    argmax_finish(c, cta);
-    MK_PROF_MARK(c, PS_ARGMAX);
 #ifdef MK_PROF
     if (c.tid == 0) c.sm->prof[PS_TOTAL] += clock64() - t_start;
     consumer_sync();
@@ -2381,6 +2478,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         sm->abort = 0;
         sm->lseq = 0;
         sm->moe_ready = 0;
+        sm->step_ready = 0;
+        sm->cstep = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm->full[s]), 1);
             mbar_init(smem_u32(&sm->empty[s]), kConsumerWarps);
@@ -2388,13 +2487,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         fence_barrier_init();
         // step-input checks (every CTA reads the same values)
         bool bad = a.B < 1 || a.B > a.p.maxB;
-        for (int b = 0; b < kMaxBatch; ++b) sm->pos[b] = 0;
+        for (int b = 0; b < kMaxBatch; ++b) sm->pos[b] = sm->ppos[b] = 0;
+        bad = bad || a.n_steps < 1;
         for (int b = 0; b < a.B && !bad; ++b) {
             const int tok = __ldg(a.tokens + b), pos = __ldg(a.positions + b);
             const int sl = __ldg(a.seq_lens + b);
-            bad = tok < 0 || tok >= a.p.V || pos < 0 || pos >= a.p.max_pos || sl != pos + 1 ||
-                  pos / kPage >= a.max_pages;
-            sm->pos[b] = pos;
+            const int last = pos + a.n_steps - 1;  // position of the launch's last step
+            bad = tok < 0 || tok >= a.p.V || pos < 0 || last >= a.p.max_pos || last < pos ||
+                  sl != pos + 1 || last / kPage >= a.max_pages;
+            sm->pos[b] = sm->ppos[b] = pos;
         }
         if (bad) set_error(a.p, sm, kErrInvalid, -1);
         if (status_bad(a.p)) sm->abort = 1;
@@ -2414,7 +2515,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         pr.ring_s = smem_u32(ring);
         pr.lane = lane;
         pr.pf = warp != 0;
-        if (!pr.pf || a.prefetch_slots > 0) pr.run<HD>(cta);
+        // (the prefetching walker shares the loader's positions: single-step launches only)
+        if (!pr.pf || (a.prefetch_slots > 0 && a.n_steps == 1)) pr.run<HD>(cta);
         return;
     }
     Ctx c;

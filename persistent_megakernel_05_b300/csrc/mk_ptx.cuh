@@ -95,6 +95,10 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// generic-proxy global writes / reads against async-proxy (TMA) accesses of global memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- gpu-scope counters
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
