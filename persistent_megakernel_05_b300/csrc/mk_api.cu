@@ -110,14 +110,24 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 template <int HD>
 cudaError_t set_kernel_attrs() {
-    return cudaFuncSetAttribute(mk::decode_step_kernel<HD>,
+    cudaError_t e = cudaFuncSetAttribute(mk::decode_step_kernel<HD, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, mk::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mk::decode_step_kernel<HD, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, mk::kSmemBytes);
 }
 
+// resident CTAs per SM of both instances (single- and multi-step launches)
 template <int HD>
 cudaError_t occupancy(int* blocks) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mk::decode_step_kernel<HD>,
-                                                         mk::kThreads, mk::kSmemBytes);
+    int b1 = 0, b2 = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, mk::decode_step_kernel<HD, false>,
+                                                                  mk::kThreads, mk::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, mk::decode_step_kernel<HD, true>,
+                                                          mk::kThreads, mk::kSmemBytes);
+    *blocks = b1 < b2 ? b1 : b2;
+    return e;
 }
 
 void free_handle(mk_handle* h) {
@@ -452,8 +462,10 @@ mk_status launch_steps(mk_handle* h, int32_t n_steps, const int32_t* tokens, con
         a.pf_pages[b] = h->pf_batch ? h->pf_pages[b] : 0;
     }
     void* args[] = {&a};
-    const void* fn = h->hd == 128 ? (const void*)mk::decode_step_kernel<128>
-                                  : (const void*)mk::decode_step_kernel<64>;
+    const bool multi = n_steps > 1;
+    const void* fn = h->hd == 128
+        ? (multi ? (const void*)mk::decode_step_kernel<128, true> : (const void*)mk::decode_step_kernel<128, false>)
+        : (multi ? (const void*)mk::decode_step_kernel<64, true> : (const void*)mk::decode_step_kernel<64, false>);
     cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(h->num_ctas), dim3(mk::kThreads), args,
                                                 mk::kSmemBytes, (cudaStream_t)stream);
     if (e != cudaSuccess) {
@@ -881,8 +893,8 @@ extern "C" mk_status mk_decode_step_noalloc(
         a.pf_pages[b] = 0;
     }
     void* args[] = {&a};
-    const void* fn = hd == 128 ? (const void*)mk::decode_step_kernel<128>
-                               : (const void*)mk::decode_step_kernel<64>;
+    const void* fn = hd == 128 ? (const void*)mk::decode_step_kernel<128, false>
+                               : (const void*)mk::decode_step_kernel<64, false>;
     if (cudaLaunchCooperativeKernel(fn, dim3(C), dim3(mk::kThreads), args, mk::kSmemBytes, s) !=
         cudaSuccess) {
         cudaGetLastError();

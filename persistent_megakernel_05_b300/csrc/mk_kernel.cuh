@@ -980,18 +980,19 @@ struct Producer {
         return __shfl_sync(0xffffffffu, ok, 0) != 0;
     }
 
-    template <int HD>
+    template <int HD, bool MULTI>
     __device__ __noinline__ void run(int cta) {
         policy = policy_evict_first();
         if (lane == 0) prefetch_tmap(tmap);
         const Plan& p = a->p;
         bool ok = !sm->abort;
-        for (int step = 0; step < a->n_steps && ok; ++step) {
-            if (step > 0 && lane < a->B) sm->ppos[lane] += 1;
+        const int nsteps = MULTI ? a->n_steps : 1;
+        for (int step = 0; step < nsteps && ok; ++step) {
+            if (MULTI && step > 0 && lane < a->B) sm->ppos[lane] += 1;
             __syncwarp();
             for (int l = 0; l < p.L && ok; ++l) {
                 ok = ok && gemv(make_gemv(*a, G_QKV, l, sm), cta);
-                if (step > 0 && l == 0) ok = ok && wait_step(step);
+                if (MULTI && step > 0 && l == 0) ok = ok && wait_step(step);
                 ok = ok && attention<HD>(l, cta);
                 ok = ok && gemv(make_gemv(*a, G_O, l, sm), cta);
                 if (p.E > 0) {
@@ -2220,11 +2221,12 @@ __device__ void embed_stage(Ctx& c, int cta) {
 // index on ties) into next_tokens. When another step of the launch follows, every CTA
 // reduces them itself (its next embedding needs the tokens), and each first releases the
 // step's K/V appends, which the next step's TMA page loads in other CTAs will read.
+template <bool MULTI>
 __device__ void argmax_finish(Ctx& c, int cta) {
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
-    const int step = c.sm->cstep;
-    const bool more = step + 1 < a.n_steps;
+    const int step = MULTI ? c.sm->cstep : 0;
+    const bool more = MULTI && step + 1 < a.n_steps;
     const int task = p.L * 16;
     const uint32_t tag = tag_of(a, p.L, TAG_EMBED);  // layer index L: no other write uses it
     consumer_sync();  // every warp's LM-head epilogue has updated amax_v / amax_i
@@ -2404,7 +2406,7 @@ __device__ __noinline__ void moe_route(Ctx& c_in, int l) {
     MK_PROF_BACK(c_in, c);
 }
 
-template <int HD>
+template <int HD, bool MULTI>
 __device__ void consumer_run(Ctx& c, int cta) {
     const Plan& p = c.a->p;
     if (c.sm->abort) return;  // step inputs rejected (uniform: set before the first barrier)
@@ -2423,7 +2425,8 @@ __device__ void consumer_run(Ctx& c, int cta) {
     const long long t_start = clock64();
     c.pt = t_start;
 #endif
-    for (int step = 0; step < c.a->n_steps; ++step) {  // (sm->cstep advances in argmax_finish)
+    const int nsteps = MULTI ? c.a->n_steps : 1;
+    for (int step = 0; step < nsteps; ++step) {  // (sm->cstep advances in argmax_finish)
         fetch_plan(0);
         embed_stage(c, cta);
         MK_PROF_MARK(c, PS_EMBED);
@@ -2443,7 +2446,7 @@ __device__ void consumer_run(Ctx& c, int cta) {
             gemv_stage(c, make_gemv(*c.a, G_DOWN, l, lp, c.sm), cta);
         }
         gemv_stage(c, make_gemv(*c.a, G_LM, 0, c.sm->lp[0], c.sm), cta);
-        argmax_finish(c, cta);
+        argmax_finish<MULTI>(c, cta);
         MK_PROF_MARK(c, PS_ARGMAX);
         if (c.sm->abort) break;
     }
@@ -2455,7 +2458,9 @@ __device__ void consumer_run(Ctx& c, int cta) {
     MK_TRACE_C(c, TR_END, 0);
 }
 
-template <int HD>
+// MULTI: a launch of several steps (mk_decode_steps); single-step launches run the
+// instance without the step loop and its cross-step hand-off.
+template <int HD, bool MULTI = false>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ StepArgs a_param) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -2516,7 +2521,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         pr.lane = lane;
         pr.pf = warp != 0;
         // (the prefetching walker shares the loader's positions: single-step launches only)
-        if (!pr.pf || (a.prefetch_slots > 0 && a.n_steps == 1)) pr.run<HD>(cta);
+        if (!pr.pf || (!MULTI && a.prefetch_slots > 0)) pr.run<HD, MULTI>(cta);
         return;
     }
     Ctx c;
@@ -2530,7 +2535,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     c.lane = lane;
     c.tid = c.cw * 32 + lane;
     c.tn = 0;
-    consumer_run<HD>(c, cta);
+    consumer_run<HD, MULTI>(c, cta);
 }
 
 }  // namespace mk
