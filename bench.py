@@ -605,7 +605,7 @@ def main():
             "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
             else "fallback 6400 GB/s", "algorithmic_bytes_per_launch": int(algo),
-            "kernel": "mk::decode_step_kernel<128>", "kernel_ms_mean": round(kern_ms, 4)}
+            "kernel": "mk::decode_step_kernel<128, false>", "kernel_ms_mean": round(kern_ms, 4)}
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
