@@ -187,7 +187,7 @@ MK_API mk_status mk_decode_steps(mk_handle *h, int32_t n_steps, const int32_t *t
  * that latched it (layer*16 + stage, or -1). */
 MK_API mk_status mk_status_sync(mk_handle *h, void *stream, int32_t *failing_task);
 
-/* Clears a latched device error and re-zeroes the argmax arrival counter (synchronous). */
+/* Clears a latched device error and re-zeroes the stage counters (synchronous). */
 MK_API mk_status mk_status_reset(mk_handle *h);
 
 /* Options (host-side; take effect from the next step):
