@@ -315,6 +315,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     p.scale = (float)(1.0 / std::sqrt((double)hd));
     p.C = C;
     p.qkv_rows = qkv_rows;
+    for (int l = 0; l < L; ++l)
+        if (h->sliding[l]) p.sliding_mask[l >> 5] |= 1u << (l & 31);
     p.layers = h->d_layers;
     p.embed = (const bf16*)weights->embed;
     p.lm_head = (const bf16*)weights->lm_head;
@@ -849,6 +851,9 @@ extern "C" mk_status mk_decode_step_noalloc(
     p.scale = (float)(1.0 / std::sqrt((double)hd));
     p.C = C;
     p.qkv_rows = qkv_rows;
+    std::memset(p.sliding_mask, 0, sizeof(p.sliding_mask));
+    for (int l = 0; l < L; ++l)
+        if (desc->layer_is_sliding && desc->layer_is_sliding[l]) p.sliding_mask[l >> 5] |= 1u << (l & 31);
     p.layers = su.layers_dst;
     p.embed = (const bf16*)weights->embed;
     p.lm_head = (const bf16*)weights->lm_head;

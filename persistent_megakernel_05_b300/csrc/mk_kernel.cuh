@@ -128,6 +128,8 @@ struct Plan {
     float eps, scale;                   // scale = 1/sqrt(hd)
     int C;                              // CTAs in the launch
     int qkv_rows;                       // (Hq + 2 Hkv) * hd
+    uint32_t sliding_mask[kMaxLayers / 32];  // bit l: layer l slides (kept with the step
+                                        // arguments in shared memory: no global read per use)
     const LayerPlan* layers;            // [L]
     const bf16* embed;
     const bf16* lm_head;
@@ -558,7 +560,8 @@ struct SeqSpan { int lo, pos, p0, np; };  // attended keys [lo, pos], logical pa
 __device__ __forceinline__ SeqSpan seq_span(const Plan& p, const int* posv, int l, int b) {
     SeqSpan s;
     s.pos = posv[b];
-    s.lo = (p.window > 0 && p.layers[l].sliding) ? max(0, s.pos - p.window + 1) : 0;
+    const bool slides = (p.sliding_mask[l >> 5] >> (l & 31)) & 1u;
+    s.lo = (p.window > 0 && slides) ? max(0, s.pos - p.window + 1) : 0;
     s.p0 = s.lo / kPage;
     s.np = s.pos / kPage - s.p0 + 1;
     return s;
@@ -1166,14 +1169,18 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[8 * BP], int l
 
 // Small batches (B <= 4): exact fp32 CUDA-core dot products. Each lane owns one 8-column
 // piece of the k-chunk (a 16 B read of every row), with the piece's activations in
-// registers. The 8 x BP partial sums of 32 / (8 BP) consecutive slots are reduced across
-// the warp together (32 values, one per lane at the end), then summed over warps in a
-// fixed order. When the whole input row is one chunk the RMSNorm statistics come from
-// the same loads. Writes yout[vrow][8].
+// registers. Each slot's 8 x BP partial sums are reduced across the warp at once (one
+// value per lane, or per group of lanes, at the end) and added to this warp's partials
+// in shared memory, which the epilogue sums over warps in a fixed order. The slot loop
+// is not unrolled: at small batch most stages run only a few slots per CTA, so the code
+// is executed once per layer, and a compact loop keeps the step's instruction working
+// set small. When the whole input row is one chunk the RMSNorm statistics come from
+// the same loads. Writes yout[vrow][8] when yout is given.
 template <int BP>
 __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int r1, float* yout,
                                          bool fused_norm) {
-    constexpr int SB = 4 / BP;  // slots per reduction batch (8 * BP * SB = 32 values)
+    constexpr int V = 8 * BP;   // values one slot leaves per lane before the reduction
+    constexpr int LPV = 32 / V;  // lanes holding each reduced value
     const StepArgs& a = *c.a;
     const int B = a.B;
     const int n = r1 - r0, ng = num_groups(s, n), ngate = s.kind == G_GU ? ng / 2 : ng;
@@ -1207,16 +1214,24 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
     constexpr bool kAhead = BP == 1;
     uint64_t wn[BP][8];
     issue(0, wn);
+#pragma unroll 1
     for (int k0 = 0; k0 < s.K; k0 += s.kcw) {
         const SlotGeom geo = slot_geom(s, k0);
         const bool has_p = piece < (geo.kc >> 3);
         float xv[BP][8];
         if (!kAhead && k0 > 0) issue(k0, wn);
+        const int col = k0 + 8 * piece;
+        const int base = (col & ~63) + 2 * ((col >> 3) & 7);  // permuted pair (t = 0)
+        // the norm gains do not depend on the step: request them before the activations
+        // are awaited, so the two reads overlap
+        float2 gg[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            gg[t] = (s.gain && has_p) ? __ldg(reinterpret_cast<const float2*>(s.gain + base + 16 * t))
+                                      : make_float2(0.f, 0.f);
         if (!c.sm->abort) {  // poll until every word carries the awaited tag
             Spin sp;
             while (!tags_ok(wn)) {
-                const int col = k0 + 8 * piece;
-                const int base = (col & ~63) + 2 * ((col >> 3) & 7);
                 int miss = 0;  // first pair (b * 4 + t) that is not there yet
 #pragma unroll
                 for (int q = 4 * BP - 1; q >= 0; --q)
@@ -1233,8 +1248,6 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
 #pragma unroll
             for (int i = 0; i < 8; ++i) xv[b][i] = (b < B && has_p) ? ll_val(wn[b][i]) : 0.f;
         if (kAhead && k0 + s.kcw < s.K) issue(k0 + s.kcw, wn);
-        const int col = k0 + 8 * piece;
-        const int base = (col & ~63) + 2 * ((col >> 3) & 7);  // permuted pair (t = 0)
         if (s.gain) {
             if (fused_norm) {  // this chunk is the whole row: sum of squares from registers
 #pragma unroll
@@ -1263,11 +1276,10 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
             if (has_p) {
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const float2 gg = __ldg(reinterpret_cast<const float2*>(s.gain + base + 16 * t));
 #pragma unroll
                     for (int b = 0; b < BP; ++b) {
-                        xv[b][2 * t] *= rs[b] * gg.x;
-                        xv[b][2 * t + 1] *= rs[b] * gg.y;
+                        xv[b][2 * t] *= rs[b] * gg[t].x;
+                        xv[b][2 * t + 1] *= rs[b] * gg[t].y;
                     }
                 }
             }
@@ -1277,55 +1289,47 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
         uint32_t roff[8];  // byte offset of row r (this lane's piece) inside a slot
 #pragma unroll
         for (int r = 0; r < 8; ++r) roff[r] = (uint32_t)(geo.row_off(r) + 16 * piece);
-        for (int gb = 0; gb < ng; gb += SB) {
-            float acc[32];
+#pragma unroll 1
+        for (int gi = 0; gi < ng; ++gi) {
+            const int nr = group_rows(s, n, gi, ngate);
+            if (trace_slots(s)) MK_TRACE_C(c, TR_S_WAIT, c.seq);
+            MK_PROF_MARK(c, PS_G_SLOTS + 4 * s.kind);
+            const bool ok = wait_full_at(c, c.seq, s.task_id);
+            MK_PROF_MARK(c, PS_G_SWAIT);
+            if (trace_slots(s)) MK_TRACE_C(c, TR_S_FULL, c.seq);
+            uint4 wr[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            for (int r = 0; r < 8; ++r) wr[r] = make_uint4(0u, 0u, 0u, 0u);
+            if (ok && has_p) {
+                const uint32_t slot = c.ring_s + (c.seq % kStages) * kSlotBytes;
 #pragma unroll
-            for (int j = 0; j < SB; ++j) {
-                const int gi = gb + j;
-                if (gi < ng) {
-                    const int nr = group_rows(s, n, gi, ngate);
-                    if (trace_slots(s)) MK_TRACE_C(c, TR_S_WAIT, c.seq);
-                    MK_PROF_MARK(c, PS_G_SLOTS + 4 * s.kind);
-                    const bool ok = wait_full_at(c, c.seq, s.task_id);
-                    MK_PROF_MARK(c, PS_G_SWAIT);
-                    if (trace_slots(s)) MK_TRACE_C(c, TR_S_FULL, c.seq);
-                    uint4 wr[8];
+                for (int r = 0; r < 8; ++r)
+                    if (r < nr)
+                        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                     : "=r"(wr[r].x), "=r"(wr[r].y), "=r"(wr[r].z), "=r"(wr[r].w)
+                                     : "r"(slot + roff[r]));
+            }
+            release_at(c, c.seq);  // the rows are in registers: hand the slot back
+            if (trace_slots(s)) MK_TRACE_C(c, TR_S_REL, c.seq);
+            c.seq++;
+            float acc[V];
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) wr[r] = make_uint4(0u, 0u, 0u, 0u);
-                    if (ok && has_p) {
-                        const uint32_t slot = c.ring_s + (c.seq % kStages) * kSlotBytes;
+            for (int r = 0; r < 8; ++r) {
+                const uint32_t w[4] = {wr[r].x, wr[r].y, wr[r].z, wr[r].w};
 #pragma unroll
-                        for (int r = 0; r < 8; ++r)
-                            if (r < nr)
-                                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                                             : "=r"(wr[r].x), "=r"(wr[r].y), "=r"(wr[r].z), "=r"(wr[r].w)
-                                             : "r"(slot + roff[r]));
+                for (int b = 0; b < BP; ++b) {
+                    float sacc = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        sacc = fmaf(__uint_as_float(w[q] << 16), xv[b][2 * q], sacc);
+                        sacc = fmaf(__uint_as_float(w[q] & 0xffff0000u), xv[b][2 * q + 1], sacc);
                     }
-                    release_at(c, c.seq);  // the rows are in registers: hand the slot back
-                    if (trace_slots(s)) MK_TRACE_C(c, TR_S_REL, c.seq);
-                    c.seq++;
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const uint32_t w[4] = {wr[r].x, wr[r].y, wr[r].z, wr[r].w};
-#pragma unroll
-                        for (int b = 0; b < BP; ++b) {
-                            float sacc = 0.f;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                sacc = fmaf(__uint_as_float(w[q] << 16), xv[b][2 * q], sacc);
-                                sacc = fmaf(__uint_as_float(w[q] & 0xffff0000u), xv[b][2 * q + 1], sacc);
-                            }
-                            acc[(j * 8 + r) * BP + b] = sacc;
-                        }
-                    }
+                    acc[r * BP + b] = sacc;
                 }
             }
-            int idx;  // = lane: (slot j, row r, batch b) = idx / (8 BP), (idx / BP) % 8, idx % BP
-            const float v = warp_transpose_reduce<4>(acc, c.lane, idx);
-            const int j = idx / (8 * BP), r = (idx / BP) & 7, b = idx % BP;
-            if (gb + j < ng) red[(c.cw * kTaskRows + (gb + j) * kGroupRows + r) * BP + b] += v;
+            int idx;  // (row r, batch b) = (idx / BP, idx % BP); LPV lanes hold each total
+            const float v = warp_transpose_reduce<BP>(acc, c.lane, idx);
+            if ((c.lane & (LPV - 1)) == 0) red[(c.cw * kTaskRows + gi * kGroupRows + idx / BP) * BP + idx % BP] += v;
         }
     }
     MK_PROF_MARK(c, PS_G_SLOTS + 4 * s.kind);
@@ -1349,7 +1353,8 @@ template <int BP>
 __device__ __forceinline__ void fma_epilogue(Ctx& c, const GemvStage& s, int r0, int r1, int cta) {
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
-    const int B = a.B, n = r1 - r0;
+    // BP 1 and 2 serve exactly that batch; BP 4 serves batches 3 and 4
+    const int B = BP < 4 ? BP : a.B, n = r1 - r0;
     const float* red = c.scratch;
     auto ysum = [&](int vr, int b) {
         float y = 0.f;
@@ -1357,43 +1362,35 @@ __device__ __forceinline__ void fma_epilogue(Ctx& c, const GemvStage& s, int r0,
         for (int w = 0; w < kConsumerWarps; ++w) y += red[(w * kTaskRows + vr) * BP + b];
         return y;
     };
-    const bool pub = a.skip_publish != s.task_id;
-    switch (s.kind) {
-        case G_QKV:
-            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
-                const int r = e / B, b = e % B;
-                const float y = ysum(r, b);
-                if (pub) ll_st(p.qkv + (size_t)b * p.qkv_rows + r0 + r, y, s.out_tag);
+    if (a.skip_publish == s.task_id) return;
+    int a0 = 0, a1;
+    if (s.kind == G_O || s.kind == G_DOWN) cta_rows(p.d, cta, p.C, a0, a1);
+    const int up0 = s.kind == G_GU ? kGroupRows * (num_groups(s, n) >> 1) : 0;
+    // one loop for every stage kind (a uniform switch per element): at small batch each
+    // thread stores at most a couple of outputs, so compact code matters more here
+#pragma unroll 1
+    for (int e = c.tid; e < n * B; e += kConsumerThreads) {
+        const int r = BP == 1 ? e : e / B, b = BP == 1 ? 0 : e - r * B;
+        const float y = ysum(r, b);
+        switch (s.kind) {
+            case G_QKV:
+                ll_st(p.qkv + (size_t)b * p.qkv_rows + r0 + r, y, s.out_tag);
+                break;
+            case G_ROUTE:
+                ll_st(p.route + (size_t)b * p.E + r0 + r, y, s.out_tag);
+                break;
+            case G_GU: {  // MoE: scaled by the row's routing weight of the union slot
+                float h = silu(y) * ysum(up0 + r, b);
+                if (s.moe) h *= c.sm->moe_w[b][(r0 + r) / s.Fe];
+                ll_st(p.h + (size_t)b * p.hrow + perm_col(r0 + r), h, s.out_tag);
+                break;
             }
-            break;
-        case G_O:
-        case G_DOWN: {
-            int a0, a1;
-            cta_rows(p.d, cta, p.C, a0, a1);
-            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
-                const int r = e / B, b = e % B;
-                const float xn = c.sm->xown[b][r0 + r - a0] + ysum(r, b);
+            default: {  // G_O, G_DOWN: residual add into the owned rows
+                const float xn = c.sm->xown[b][r0 + r - a0] + y;
                 c.sm->xown[b][r0 + r - a0] = xn;
-                if (pub) ll_st(p.x + (size_t)b * p.d + perm_col(r0 + r), xn, s.out_tag);
+                ll_st(p.x + (size_t)b * p.d + perm_col(r0 + r), xn, s.out_tag);
+                break;
             }
-            break;
-        }
-        case G_ROUTE:
-            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
-                const int r = e / B, b = e % B;
-                const float y = ysum(r, b);
-                if (pub) ll_st(p.route + (size_t)b * p.E + r0 + r, y, s.out_tag);
-            }
-            break;
-        default: {  // G_GU (MoE: scaled by the row's routing weight of the union slot)
-            const int up0 = kGroupRows * (num_groups(s, n) >> 1);
-            for (int e = c.tid; e < n * B; e += kConsumerThreads) {
-                const int r = e / B, b = e % B;
-                float y = silu(ysum(r, b)) * ysum(up0 + r, b);
-                if (s.moe) y *= c.sm->moe_w[b][(r0 + r) / s.Fe];
-                if (pub) ll_st(p.h + (size_t)b * p.hrow + perm_col(r0 + r), y, s.out_tag);
-            }
-            break;
         }
     }
 }
@@ -1601,16 +1598,24 @@ __device__ __noinline__ void gemv_task_fma(Ctx& c_in, int kind, int layer, int r
     Ctx c = c_in;
     const StepArgs& a = *c.a;
     const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[layer & 1], c.sm);
-    const bool fused = fused_norm_stage(a, s);
-    if (s.kind != G_LM) {
-        gemv_fma<BP>(c, s, r0, r1, nullptr, fused);
-        if (!c.sm->abort) fma_epilogue<BP>(c, s, r0, r1, cta_of(c));
-    } else {
-        float* yout = c.scratch + kConsumerWarps * kTaskRows * 4;  // [128 vrows][8]
-        gemv_fma<BP>(c, s, r0, r1, yout, fused);
-        consumer_sync();
-        if (!c.sm->abort) yout_epilogue(c, s, r0, r1, yout);
-    }
+    gemv_fma<BP>(c, s, r0, r1, nullptr, fused_norm_stage(a, s));
+    if (!c.sm->abort) fma_epilogue<BP>(c, s, r0, r1, cta_of(c));
+    MK_PROF_MARK(c, PS_G_EPI + 4 * s.kind);
+    if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
+    c_in.seq = c.seq;
+    c_in.tn = c.tn;
+    MK_PROF_BACK(c_in, c);
+}
+// The LM head (once per step): outputs staged for the logits and argmax epilogue.
+template <int BP>
+__device__ __noinline__ void gemv_task_fma_lm(Ctx& c_in, int r0, int r1) {
+    Ctx c = c_in;
+    const StepArgs& a = *c.a;
+    const GemvStage s = make_gemv(a, G_LM, 0, c.sm->lp[0], c.sm);
+    float* yout = c.scratch + kConsumerWarps * kTaskRows * 4;  // [128 vrows][8]
+    gemv_fma<BP>(c, s, r0, r1, yout, fused_norm_stage(a, s));
+    consumer_sync();
+    if (!c.sm->abort) yout_epilogue(c, s, r0, r1, yout);
     MK_PROF_MARK(c, PS_G_EPI + 4 * s.kind);
     if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
     c_in.seq = c.seq;
@@ -1633,10 +1638,14 @@ __device__ __noinline__ void gemv_task_mma(Ctx& c_in, int kind, int layer, int r
 }
 __device__ __forceinline__ void gemv_task(Ctx& c, int kind, int layer, int r0, int r1) {
     const int B = c.a->B;
-    if (B == 1) gemv_task_fma<1>(c, kind, layer, r0, r1);
+    if (B > 4) gemv_task_mma(c, kind, layer, r0, r1);
+    else if (kind == G_LM) {
+        if (B == 1) gemv_task_fma_lm<1>(c, r0, r1);
+        else if (B == 2) gemv_task_fma_lm<2>(c, r0, r1);
+        else gemv_task_fma_lm<4>(c, r0, r1);
+    } else if (B == 1) gemv_task_fma<1>(c, kind, layer, r0, r1);
     else if (B == 2) gemv_task_fma<2>(c, kind, layer, r0, r1);
-    else if (B <= 4) gemv_task_fma<4>(c, kind, layer, r0, r1);
-    else gemv_task_mma(c, kind, layer, r0, r1);
+    else gemv_task_fma<4>(c, kind, layer, r0, r1);
 }
 
 __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
@@ -1876,6 +1885,8 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, const Piece& pc_i
     const int CT = MULTI ? (NC + 7) >> 3 : 1, wpt = MULTI ? kConsumerWarps / CT : kConsumerWarps;
     const int tile = MULTI ? c.cw / wpt : 0, wl = c.cw - tile * wpt;
     const bool has_last = !MULTI && (sp.p0 + u + n - 1) == pos / kPage;
+    // page of the new token's K/V (appending piece): read now, used in the key loop
+    const int last_page = has_last ? __ldg(a.page_table + (size_t)b * a.max_pages + pos / kPage) : -1;
     MK_PROF_MARK(c, PS_A_ENTRY);
 
     // Stage q of the columns (and the new token's k, v when this piece appends), plus the
@@ -2023,7 +2034,7 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, const Piece& pc_i
                     // splice the new row into the last page and append it to the pool
                     const uint32_t kb = w0 + pa == n - 1 ? kbA : kbB;
                     const int row = pos % kPage;
-                    const int page = __ldg(a.page_table + (size_t)b * a.max_pages + pos / kPage);
+                    const int page = MULTI ? 0 : last_page;  // (MULTI pieces never append)
                     if (page >= 0 && page < p.num_pages) {
                         if (c.lane < 2 * NCH) {
                             const int kv = c.lane / NCH, ch = c.lane % NCH;
