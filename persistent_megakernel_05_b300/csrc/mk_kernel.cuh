@@ -69,7 +69,7 @@ __device__ __forceinline__ void trace_event(int cta, int& n, int base, uint32_t 
     if (cta < kTraceCtas && n < kTraceEvents / 2)
         g_mk_trace[cta][base + n++] = make_ulonglong2(globaltimer(), ((unsigned long long)code << 32) | arg);
 }
-#define MK_TRACE_C(c, code, arg) do { if ((c).tid == 0) trace_event(blockIdx.x, (c).tn, 0, code, arg); } while (0)
+#define MK_TRACE_C(c, code, arg) do { if ((c).tid == 0) trace_event(blockIdx.x, (c).sm->trace_n, 0, code, arg); } while (0)
 #define MK_TRACE_P(pr, code, arg) do { if ((pr).lane == 0 && !(pr).pf) trace_event(blockIdx.x, (pr).tn, kTraceEvents / 2, code, arg); } while (0)
 #else
 #define MK_TRACE_C(c, code, arg) do { } while (0)
@@ -85,11 +85,9 @@ __device__ unsigned long long g_mk_prof[kProfCtas][kProfSections];
 // sums accumulate in shared memory (no global round trip inside a section) and are
 // flushed to g_mk_prof once at the end of the step
 #define MK_PROF_MARK(c, sec) do { if ((c).tid == 0) { \
-    const long long t_ = clock64(); (c).sm->prof[sec] += t_ - (c).pt; (c).pt = t_; } } while (0)
-#define MK_PROF_BACK(dst, src) ((dst).pt = (src).pt)
+    const long long t_ = clock64(); (c).sm->prof[sec] += t_ - (c).sm->prof_pt; (c).sm->prof_pt = t_; } } while (0)
 #else
 #define MK_PROF_MARK(c, sec) do { } while (0)
-#define MK_PROF_BACK(dst, src) do { } while (0)
 #endif
 // profile sections: GEMV kind k (QKV, O, GU, DOWN, LM, ROUTE) uses 1 + 4k .. 4 + 4k
 enum ProfSection { PS_OTHER = 0, PS_G_DATA = 1, PS_G_SLOTS = 2, PS_G_EPI = 3, PS_G_END = 4,
@@ -239,6 +237,10 @@ struct Smem {
     float moe_w[kMaxBatch][kMaxExperts];  // routing weight of union slot j for row b (0: not routed)
 #ifdef MK_PROF
     unsigned long long prof[64];
+    long long prof_pt;                 // cycle count at the last profile mark
+#endif
+#ifdef MK_TRACE
+    int trace_n;                       // consumer trace events recorded
 #endif
     uint64_t full[kStages];
     uint64_t empty[kStages];
@@ -256,11 +258,32 @@ struct Ctx {
     uint32_t ring_s;     // shared address of the ring
     uint32_t seq;        // ring sequence number (slot = seq % kStages)
     int cw, lane, tid;   // consumer warp (0..7), lane, consumer thread id (0..255)
-    int tn;              // trace events recorded (MK_TRACE builds)
-#ifdef MK_PROF
-    long long pt;        // cycle count at the last profile mark (MK_PROF builds)
-#endif
 };
+
+// The dynamic shared memory of the kernel: [pad to 1024][ring][scratch][Smem].
+extern __shared__ __align__(1024) uint8_t mk_smem[];
+
+// A consumer thread's context, rebuilt from the thread index and the shared-memory base
+// wherever it is needed. Functions that are not inlined take the ring sequence number
+// and return the advanced one instead of taking the context by reference: a context
+// whose address is taken lives in local memory, and its reloads after every call missed
+// L1 and waited on L2 in the middle of the step.
+__device__ __forceinline__ Ctx make_ctx(uint32_t seq) {
+    Ctx c;
+    const uint32_t raw_s = smem_u32(mk_smem);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    c.ring = mk_smem + pad;
+    c.ring_s = raw_s + pad;
+    c.scratch = reinterpret_cast<float*>(c.ring + kStages * kSlotBytes);
+    c.sm = reinterpret_cast<Smem*>(c.ring + kStages * kSlotBytes + kScratchBytes);
+    c.a = &c.sm->args;
+    c.seq = seq;
+    const int warp = (int)(threadIdx.x >> 5);
+    c.cw = consumer_index(warp);
+    c.lane = (int)(threadIdx.x & 31);
+    c.tid = c.cw * 32 + c.lane;
+    return c;
+}
 
 // ------------------------------------------------------------------ errors / waits
 __device__ __forceinline__ void set_error(const Plan& p, Smem* sm, int code, int task) {
@@ -688,7 +711,7 @@ __device__ __forceinline__ void for_each_row_piece(const StepArgs& a, const int*
 }
 
 template <typename F>
-__device__ __noinline__ void for_each_group_piece(const StepArgs& a, const int* posv, int l, int cta, F& f);
+__device__ __forceinline__ void for_each_group_piece(const StepArgs& a, const int* posv, int l, int cta, F& f);
 
 template <typename F>
 __device__ __forceinline__ void for_each_piece(const StepArgs& a, const int* posv, int l, int cta, F&& f) {
@@ -696,9 +719,10 @@ __device__ __forceinline__ void for_each_piece(const StepArgs& a, const int* pos
     else for_each_group_piece(a, posv, l, cta, f);
 }
 
-// for_each_piece with shared-prefix groups declared (out of line: rarely taken)
+// for_each_piece with shared-prefix groups declared (inlined like the rest: a call would
+// put the callers' captured state in local memory)
 template <typename F>
-__device__ __noinline__ void for_each_group_piece(const StepArgs& a, const int* posv, int l, int cta, F& f) {
+__device__ __forceinline__ void for_each_group_piece(const StepArgs& a, const int* posv, int l, int cta, F& f) {
     const Plan& p = a.p;
     // 32-bit unsigned unit arithmetic: U * C < 2^31 (checked on the host)
     const uint32_t C = (uint32_t)p.C;
@@ -799,7 +823,7 @@ struct Producer {
     // page-table batch cache: ids of logical pages [pt_lp0, pt_lp0 + 32) of sequence pt_b
     int pt_b = -1, pt_lp0 = 0, pt_ids = -1;
 
-    __device__ bool acquire_slot(int task) {
+    __device__ __forceinline__ bool acquire_slot(int task) {
         if (pf) {
             int ok = 1;
             if (lane == 0) {
@@ -839,10 +863,10 @@ struct Producer {
         if (pf) l2_prefetch_1d(src, bytes);
         else tma_load_1d(dst, src, bytes, bar, policy);
     }
-    __device__ uint32_t slot_addr() const { return ring_s + (seq % kStages) * kSlotBytes; }
-    __device__ uint32_t full_bar() const { return smem_u32(&sm->full[seq % kStages]); }
+    __device__ __forceinline__ uint32_t slot_addr() const { return ring_s + (seq % kStages) * kSlotBytes; }
+    __device__ __forceinline__ uint32_t full_bar() const { return smem_u32(&sm->full[seq % kStages]); }
 
-    __device__ bool gemv(const GemvStage& s, int cta) {
+    __device__ __forceinline__ bool gemv(const GemvStage& s, int cta) {
         MK_TRACE_P(*this, TR_P_STAGE, s.task_id);
         int a0, a1;
         cta_rows(s.R, cta, a->p.C, a0, a1);
@@ -884,7 +908,7 @@ struct Producer {
     }
 
     template <int HD>
-    __device__ bool attention(int l, int cta) {
+    __device__ __forceinline__ bool attention(int l, int cta) {
         const Plan& p = a->p;
         constexpr int PPS = 512 / HD;   // pages per ring slot (K + V of one kv head)
         constexpr int NB = HD / 64;     // 64-wide boxes per page row
@@ -936,7 +960,7 @@ struct Producer {
     // A MoE layer's expert rows depend on its routing, which this CTA's consumers compute
     // from the router logits: wait until they publish it (bounded; on abort or time-out
     // the loader stops, and the consumers report the cause).
-    __device__ bool wait_route(int step, int l) {
+    __device__ __forceinline__ bool wait_route(int step, int l) {
         int ok = 1;
         if (lane == 0) {
             uint64_t t0 = 0;
@@ -963,7 +987,7 @@ struct Producer {
     // (in other CTAs, by generic stores): wait until this CTA's consumers have seen every
     // CTA finish that step (each released its stores before its argmax record), then
     // order the coming TMA reads after that (bounded; on abort or time-out: stop).
-    __device__ bool wait_step(int step) {
+    __device__ __forceinline__ bool wait_step(int step) {
         int ok = 1;
         if (lane == 0) {
             uint64_t t0 = 0;
@@ -984,7 +1008,7 @@ struct Producer {
     }
 
     template <int HD, bool MULTI>
-    __device__ __noinline__ void run(int cta) {
+    __device__ __forceinline__ void run(int cta) {
         policy = policy_evict_first();
         if (lane == 0) prefetch_tmap(tmap);
         const Plan& p = a->p;
@@ -1029,9 +1053,10 @@ struct Producer {
 // rstd[b] = 1 / sqrt(mean(src[b]^2) + eps); fixed summation order. Every k-step reads
 // all the batch rows at once, so the whole pass costs K / 1024 read latencies, not one
 // per row and k-step. Small batches read the tagged rows, larger ones the fp32 rows.
-__device__ __noinline__ void rms_scale(Ctx& c_in, const GemvStage& s) {
-    Ctx c = c_in;
+__device__ __noinline__ void rms_scale(int kind, int layer) {
+    Ctx c = make_ctx(0);
     const StepArgs& a = *c.a;
+    const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[kind == G_LM ? 0 : (layer & 1)], c.sm);
     const int K = s.K, B = a.B;
     float* red = c.scratch;
     float ss[kMaxBatch];
@@ -1086,8 +1111,6 @@ __device__ __noinline__ void rms_scale(Ctx& c_in, const GemvStage& s) {
         c.sm->rstd[c.tid] = rsqrtf(t / (float)K + a.p.eps);
     }
     consumer_sync();
-    c_in.tn = c.tn;
-    MK_PROF_BACK(c_in, c);
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
@@ -1594,22 +1617,20 @@ __device__ __forceinline__ void yout_epilogue(Ctx& c, const GemvStage& s, int r0
 // budget. They work on register copies of the context and of the stage description;
 // only the ring sequence number (and the trace count) go back to the caller.
 template <int BP>
-__device__ __noinline__ void gemv_task_fma(Ctx& c_in, int kind, int layer, int r0, int r1) {
-    Ctx c = c_in;
+__device__ __noinline__ uint32_t gemv_task_fma(uint32_t seq, int kind, int layer, int r0, int r1) {
+    Ctx c = make_ctx(seq);
     const StepArgs& a = *c.a;
     const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[layer & 1], c.sm);
     gemv_fma<BP>(c, s, r0, r1, nullptr, fused_norm_stage(a, s));
     if (!c.sm->abort) fma_epilogue<BP>(c, s, r0, r1, cta_of(c));
     MK_PROF_MARK(c, PS_G_EPI + 4 * s.kind);
     if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
-    c_in.seq = c.seq;
-    c_in.tn = c.tn;
-    MK_PROF_BACK(c_in, c);
+    return c.seq;
 }
 // The LM head (once per step): outputs staged for the logits and argmax epilogue.
 template <int BP>
-__device__ __noinline__ void gemv_task_fma_lm(Ctx& c_in, int r0, int r1) {
-    Ctx c = c_in;
+__device__ __noinline__ uint32_t gemv_task_fma_lm(uint32_t seq, int r0, int r1) {
+    Ctx c = make_ctx(seq);
     const StepArgs& a = *c.a;
     const GemvStage s = make_gemv(a, G_LM, 0, c.sm->lp[0], c.sm);
     float* yout = c.scratch + kConsumerWarps * kTaskRows * 4;  // [128 vrows][8]
@@ -1618,12 +1639,10 @@ __device__ __noinline__ void gemv_task_fma_lm(Ctx& c_in, int r0, int r1) {
     if (!c.sm->abort) yout_epilogue(c, s, r0, r1, yout);
     MK_PROF_MARK(c, PS_G_EPI + 4 * s.kind);
     if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
-    c_in.seq = c.seq;
-    c_in.tn = c.tn;
-    MK_PROF_BACK(c_in, c);
+    return c.seq;
 }
-__device__ __noinline__ void gemv_task_mma(Ctx& c_in, int kind, int layer, int r0, int r1) {
-    Ctx c = c_in;
+__device__ __noinline__ uint32_t gemv_task_mma(uint32_t seq, int kind, int layer, int r0, int r1) {
+    Ctx c = make_ctx(seq);
     const StepArgs& a = *c.a;
     const GemvStage s = make_gemv(a, kind, layer, c.sm->lp[layer & 1], c.sm);
     float* yout = c.scratch + kConsumerWarps * kTaskRows * 4;  // [128 vrows][8]
@@ -1632,23 +1651,21 @@ __device__ __noinline__ void gemv_task_mma(Ctx& c_in, int kind, int layer, int r
     if (!c.sm->abort) yout_epilogue(c, s, r0, r1, yout);
     MK_PROF_MARK(c, PS_G_EPI + 4 * s.kind);
     if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
-    c_in.seq = c.seq;
-    c_in.tn = c.tn;
-    MK_PROF_BACK(c_in, c);
+    return c.seq;
 }
 __device__ __forceinline__ void gemv_task(Ctx& c, int kind, int layer, int r0, int r1) {
     const int B = c.a->B;
-    if (B > 4) gemv_task_mma(c, kind, layer, r0, r1);
+    if (B > 4) c.seq = gemv_task_mma(c.seq, kind, layer, r0, r1);
     else if (kind == G_LM) {
-        if (B == 1) gemv_task_fma_lm<1>(c, r0, r1);
-        else if (B == 2) gemv_task_fma_lm<2>(c, r0, r1);
-        else gemv_task_fma_lm<4>(c, r0, r1);
-    } else if (B == 1) gemv_task_fma<1>(c, kind, layer, r0, r1);
-    else if (B == 2) gemv_task_fma<2>(c, kind, layer, r0, r1);
-    else gemv_task_fma<4>(c, kind, layer, r0, r1);
+        if (B == 1) c.seq = gemv_task_fma_lm<1>(c.seq, r0, r1);
+        else if (B == 2) c.seq = gemv_task_fma_lm<2>(c.seq, r0, r1);
+        else c.seq = gemv_task_fma_lm<4>(c.seq, r0, r1);
+    } else if (B == 1) c.seq = gemv_task_fma<1>(c.seq, kind, layer, r0, r1);
+    else if (B == 2) c.seq = gemv_task_fma<2>(c.seq, kind, layer, r0, r1);
+    else c.seq = gemv_task_fma<4>(c.seq, kind, layer, r0, r1);
 }
 
-__device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
+__device__ __forceinline__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
     const Plan& p = c.a->p;
     int a0, a1;
     cta_rows(s.R, cta, p.C, a0, a1);
@@ -1657,7 +1674,7 @@ __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
     if (a0 < a1) {
         MK_TRACE_C(c, TR_WAIT, s.task_id);
         if (!tg) consumer_wait(c, s.cnt_wait, s.task_id);
-        if (s.gain && !fused_norm_stage(*c.a, s)) rms_scale(c, s);
+        if (s.gain && !fused_norm_stage(*c.a, s)) rms_scale(s.kind, s.layer);
         if (trace_slots(s)) MK_TRACE_C(c, TR_G_NORM, 0);
         const int tr = task_rows(s.kind);
         for (int r0 = a0; r0 < a1; r0 += tr) {
@@ -1670,6 +1687,14 @@ __device__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
     else consumer_sync();  // every warp is done with the shared scratch of this stage
     MK_PROF_MARK(c, PS_G_END + 4 * s.kind);
     MK_TRACE_C(c, TR_DONE, s.task_id);
+}
+
+// One GEMV stage of layer `layer` (kind G_*), out of line with its own registers; takes
+// and returns the ring sequence number.
+__device__ __noinline__ uint32_t gemv_stage_call(uint32_t seq, int kind, int layer, int cta) {
+    Ctx c = make_ctx(seq);
+    gemv_stage(c, make_gemv(*c.a, kind, layer, c.sm->lp[kind == G_LM ? 0 : (layer & 1)], c.sm), cta);
+    return c.seq;
 }
 
 __device__ __forceinline__ int bg_id(const Plan& p, int b, int g) { return b * p.Hkv + g; }
@@ -1693,8 +1718,8 @@ struct FinishCols {
 // piece (several rows, one or two column tiles); otherwise one row, one tile, one pass.
 // Non-inlined so the key loop keeps its registers to itself.
 template <int HD, bool MULTI>
-__device__ __noinline__ void attention_finish(Ctx& c_in, int l, const Piece& pc, int ch0, int NC, int wpt_in) {
-    Ctx c = c_in;
+__device__ __noinline__ void attention_finish(int l, Piece pc, int ch0, int NC, int wpt_in) {
+    Ctx c = make_ctx(0);
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
     const int G = p.G;
@@ -1744,8 +1769,6 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, const Piece& pc,
     consumer_sync();  // the scratch is free for the next piece
     MK_PROF_MARK(c, PS_A_FINISH);
     if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_PART, (uint32_t)pc.split);
-    c_in.tn = c.tn;
-    MK_PROF_BACK(c_in, c);
 }
 
 // The split-`split` of the nsplit CTAs of a (sequence, kv head) item merges output dims
@@ -1755,9 +1778,8 @@ __device__ __noinline__ void attention_finish(Ctx& c_in, int l, const Piece& pc,
 // slice, so the merge is spread over all the item's CTAs instead of one CTA merging
 // every split.
 template <int HD>
-__device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int split, int nsplit_in,
-                                             int nrec) {
-    Ctx c = c_in;
+__device__ __noinline__ void attention_merge(int l, int b, int g, int split, int nsplit_in, int nrec) {
+    Ctx c = make_ctx(0);
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
     const int G = p.G, GHD = G * HD, RS = GHD + 2 * G;
@@ -1860,14 +1882,11 @@ __device__ __noinline__ void attention_merge(Ctx& c_in, int l, int b, int g, int
     consumer_sync();  // the scratch is free again
     MK_PROF_MARK(c, PS_M_O);
     if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_MERGED, 0);
-    c_in.tn = c.tn;
-    MK_PROF_BACK(c_in, c);
 }
 
 template <int HD, bool MULTI>
-__device__ __noinline__ void attention_piece(Ctx& c_in, int l, const Piece& pc_in) {
-    Ctx c = c_in;  // register copy (see gemv_task)
-    const Piece& pc = pc_in;  // fields read where needed (most are dead in the key loop)
+__device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) {
+    Ctx c = make_ctx(seq);
     const SeqSpan sp = pc.sp;
     const int b = pc.b, g = pc.g, u = pc.u, n = pc.n;
     const StepArgs& a = *c.a;
@@ -2160,8 +2179,6 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, const Piece& pc_i
         l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 8);
         l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 16);
     }
-    c_in.seq = c.seq;
-    c_in.tn = c.tn;
     const int ncl = MULTI ? min(8, NC) : 1;  // one pass for one row (G columns <= kFC)
     for (int ch0 = 0; ch0 < ncl; ch0 += kFC) {
         consumer_sync();  // the key loop's P buffers / the previous pass are done with it
@@ -2178,37 +2195,36 @@ __device__ __noinline__ void attention_piece(Ctx& c_in, int l, const Piece& pc_i
             }
         }
         MK_PROF_MARK(c, PS_A_POST);
-        MK_PROF_BACK(c_in, c);
-        attention_finish<HD, MULTI>(c_in, l, pc, ch0, NC, wpt);
-#ifdef MK_PROF
-        c.pt = c_in.pt;
-#endif
+        attention_finish<HD, MULTI>(l, pc, ch0, NC, wpt);
     }
+    return c.seq;
 }
 
 template <int HD>
-__device__ __noinline__ void attention_stage(Ctx& c, int l, int cta) {
+__device__ __noinline__ uint32_t attention_stage(uint32_t seq, int l, int cta) {
+    Ctx c = make_ctx(seq);
     MK_PROF_MARK(c, PS_OTHER);
     MK_TRACE_C(c, TR_WAIT, l * 16 + ST_ATTN);
     // every piece first writes its partial record; then each split merges its slice
     for_each_piece(*c.a, c.sm->pos, l, cta, [&](const Piece& pc) {
         MK_TRACE_C(c, TR_PIECE, (uint32_t)(pc.b * 256 + pc.g));
-        if (pc.prefix) attention_piece<HD, true>(c, l, pc);
-        else attention_piece<HD, false>(c, l, pc);
+        if (pc.prefix) c.seq = attention_piece<HD, true>(c.seq, l, pc);
+        else c.seq = attention_piece<HD, false>(c.seq, l, pc);
     });
     for_each_piece(*c.a, c.sm->pos, l, cta, [&](const Piece& pc) {
         if (pc.prefix) return;  // a shared prefix's records are merged by each row's own CTAs
-        attention_merge<HD>(c, l, pc.b, pc.g, pc.split, pc.nsplit, pc.nrec);
+        attention_merge<HD>(l, pc.b, pc.g, pc.split, pc.nsplit, pc.nrec);
         MK_TRACE_C(c, TR_MERGE, (uint32_t)(pc.b * 256 + pc.g));
     });
     // larger batches: every CTA counts its (possibly empty) share of the merges
     if (!tagged(*c.a)) publish(c, cnt_stage(l, ST_ATTN), l * 16 + ST_ATTN);
     MK_PROF_MARK(c, PS_A_END);
+    return c.seq;
 }
 
 // x[b] = E[token b]. Each CTA writes the residual rows it owns (the same rows its O and
 // down tiles update) and keeps them in shared memory for those residual adds.
-__device__ void embed_stage(Ctx& c, int cta) {
+__device__ __forceinline__ void embed_stage(Ctx& c, int cta) {
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
     int a0, a1;
@@ -2233,7 +2249,7 @@ __device__ void embed_stage(Ctx& c, int cta) {
 // reduces them itself (its next embedding needs the tokens), and each first releases the
 // step's K/V appends, which the next step's TMA page loads in other CTAs will read.
 template <bool MULTI>
-__device__ void argmax_finish(Ctx& c, int cta) {
+__device__ __forceinline__ void argmax_finish(Ctx& c, int cta) {
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
     const int step = MULTI ? c.sm->cstep : 0;
@@ -2321,8 +2337,8 @@ __device__ void argmax_finish(Ctx& c, int cta) {
 // on ties) with weights p / sum of the picked p; then the union over the batch rows, in
 // ascending expert id, goes to shared memory for the consumers' and the loader's stages.
 // ("Kog Inference Engine", MoE paragraphs; the softmax-top-k reading of the router.)
-__device__ __noinline__ void moe_route(Ctx& c_in, int l) {
-    Ctx c = c_in;
+__device__ __noinline__ void moe_route(int l) {
+    Ctx c = make_ctx(0);
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
     const int E = p.E, task = l * 16 + ST_ROUTE;
@@ -2413,12 +2429,10 @@ __device__ __noinline__ void moe_route(Ctx& c_in, int l) {
         __threadfence_block();  // the routing above before the flag the loader waits on
         c.sm->moe_ready = c.sm->cstep * kMaxLayers + l + 1;
     }
-    c_in.tn = c.tn;
-    MK_PROF_BACK(c_in, c);
 }
 
 template <int HD, bool MULTI>
-__device__ void consumer_run(Ctx& c, int cta) {
+__device__ __forceinline__ void consumer_run(Ctx& c, int cta) {
     const Plan& p = c.a->p;
     if (c.sm->abort) return;  // step inputs rejected (uniform: set before the first barrier)
     static_assert(sizeof(LayerPlan) % 16 == 0, "layer plans copy in 16-byte pieces");
@@ -2434,7 +2448,7 @@ __device__ void consumer_run(Ctx& c, int cta) {
     if (c.tid < 64) c.sm->prof[c.tid] = 0;
     consumer_sync();
     const long long t_start = clock64();
-    c.pt = t_start;
+    if (c.tid == 0) c.sm->prof_pt = t_start;
 #endif
     const int nsteps = MULTI ? c.a->n_steps : 1;
     for (int step = 0; step < nsteps; ++step) {  // (sm->cstep advances in argmax_finish)
@@ -2444,19 +2458,18 @@ __device__ void consumer_run(Ctx& c, int cta) {
         for (int l = 0; l < p.L; ++l) {
             if (c.tid < kPlanChunks) cp_async_wait_all();
             consumer_sync();  // layer l's plan is in place; slot (l + 1) & 1 is free
-            const LayerPlan& lp = c.sm->lp[l & 1];
-            gemv_stage(c, make_gemv(*c.a, G_QKV, l, lp, c.sm), cta);
+            c.seq = gemv_stage_call(c.seq, G_QKV, l, cta);
             if (l + 1 < p.L) fetch_plan(l + 1);  // read at the next layer, after a barrier
-            attention_stage<HD>(c, l, cta);
-            gemv_stage(c, make_gemv(*c.a, G_O, l, lp, c.sm), cta);
+            c.seq = attention_stage<HD>(c.seq, l, cta);
+            c.seq = gemv_stage_call(c.seq, G_O, l, cta);
             if (p.E > 0) {
-                gemv_stage(c, make_gemv(*c.a, G_ROUTE, l, lp, c.sm), cta);
-                moe_route(c, l);
+                c.seq = gemv_stage_call(c.seq, G_ROUTE, l, cta);
+                moe_route(l);
             }
-            gemv_stage(c, make_gemv(*c.a, G_GU, l, lp, c.sm), cta);
-            gemv_stage(c, make_gemv(*c.a, G_DOWN, l, lp, c.sm), cta);
+            c.seq = gemv_stage_call(c.seq, G_GU, l, cta);
+            c.seq = gemv_stage_call(c.seq, G_DOWN, l, cta);
         }
-        gemv_stage(c, make_gemv(*c.a, G_LM, 0, c.sm->lp[0], c.sm), cta);
+        c.seq = gemv_stage_call(c.seq, G_LM, 0, cta);
         argmax_finish<MULTI>(c, cta);
         MK_PROF_MARK(c, PS_ARGMAX);
         if (c.sm->abort) break;
@@ -2469,15 +2482,33 @@ __device__ void consumer_run(Ctx& c, int cta) {
     MK_TRACE_C(c, TR_END, 0);
 }
 
+// The two roles as functions of their own (each with its own register allocation, and
+// no state whose address escapes: every member the loader walks with stays in registers).
+template <int HD, bool MULTI>
+__device__ __noinline__ void loader_main(int cta, bool prefetch, const CUtensorMap* tmap) {
+    const Ctx c = make_ctx(0);
+    Producer pr;
+    pr.a = c.a;
+    pr.tmap = tmap;
+    pr.sm = c.sm;
+    pr.ring_s = c.ring_s;
+    pr.lane = c.lane;
+    pr.pf = prefetch;
+    pr.run<HD, MULTI>(cta);
+}
+template <int HD, bool MULTI>
+__device__ __noinline__ void consumer_main(int cta) {
+    Ctx c = make_ctx(0);
+    consumer_run<HD, MULTI>(c, cta);
+}
+
 // MULTI: a launch of several steps (mk_decode_steps); single-step launches run the
 // instance without the step loop and its cross-step hand-off.
 template <int HD, bool MULTI = false>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ StepArgs a_param) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t raw_s = smem_u32(mk_smem);
     const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
-    uint8_t* ring = smem_raw + pad;
-    float* scratch = reinterpret_cast<float*>(ring + kStages * kSlotBytes);
+    uint8_t* ring = mk_smem + pad;
     Smem* sm = reinterpret_cast<Smem*>(ring + kStages * kSlotBytes + kScratchBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
@@ -2491,6 +2522,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     const StepArgs& a = sm->args;
 
     if (threadIdx.x == 0) {
+#ifdef MK_TRACE
+        sm->trace_n = 0;
+#endif
         sm->abort = 0;
         sm->lseq = 0;
         sm->moe_ready = 0;
@@ -2524,29 +2558,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 
     if (idle_warp(warp)) return;
     if (warp == 0 || warp == kPrefetchWarp) {
-        Producer pr;
-        pr.a = &a;
-        pr.tmap = &a_param.kv_tmap;
-        pr.sm = sm;
-        pr.ring_s = smem_u32(ring);
-        pr.lane = lane;
-        pr.pf = warp != 0;
         // (the prefetching walker shares the loader's positions: single-step launches only)
-        if (!pr.pf || (!MULTI && a.prefetch_slots > 0)) pr.run<HD, MULTI>(cta);
+        if (warp == 0 || (!MULTI && a.prefetch_slots > 0)) loader_main<HD, MULTI>(cta, warp != 0, &a_param.kv_tmap);
         return;
     }
-    Ctx c;
-    c.a = &a;
-    c.sm = sm;
-    c.ring = ring;
-    c.scratch = scratch;
-    c.ring_s = smem_u32(ring);
-    c.seq = 0;
-    c.cw = consumer_index(warp);
-    c.lane = lane;
-    c.tid = c.cw * 32 + lane;
-    c.tn = 0;
-    consumer_run<HD, MULTI>(c, cta);
+    consumer_main<HD, MULTI>(cta);
 }
 
 }  // namespace mk
