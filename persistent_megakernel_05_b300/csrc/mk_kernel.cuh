@@ -45,7 +45,15 @@ constexpr int kPrefetchWarp = 11;
 __device__ __forceinline__ bool idle_warp(int w) { return w == 4 || w == 8; }
 __device__ __forceinline__ int consumer_index(int w) { return w - 1 - (w > 4) - (w > 8); }
 constexpr int kDefaultPrefetchSlots = 0;          // L2 prefetch lead (slots); 0 = off
-constexpr int kStages = 6;                         // shared-memory ring depth
+#ifndef MK_PF_MODE
+#define MK_PF_MODE 0  // prefetch walker: 0 TMA bulk prefetch, 1 lane line prefetch, 2 same, evict_last
+#endif
+// Shared-memory ring depth. Four 33 KB slots keep HBM streaming (132 KB in flight per
+// SM) and leave ~90 KB of the SM's unified L1/shared array to L1: the consumers' saved
+// registers at calls and the norm-gain reads then hit L1 instead of waiting on L2.
+// Measured at 2B batch 1: 6 slots 1.107, 5 slots 1.106, 4 slots 1.070, 3 slots 1.135
+// ms/step (alternating runs on one box).
+constexpr int kStages = 4;
 constexpr int KCW = 2048;                          // GEMV k-chunk: columns of a weight slot
 constexpr int kGroupRows = 8;                      // weight rows per ring slot
 constexpr int kSlotBytes = 33 * 1024;              // >= 8 * (2 * KCW + 16), multiple of 1024
@@ -94,7 +102,19 @@ enum ProfSection { PS_OTHER = 0, PS_G_DATA = 1, PS_G_SLOTS = 2, PS_G_EPI = 3, PS
                    PS_A_ENTRY = 25, PS_A_QPOLL = 26, PS_A_QSYNC = 27, PS_A_FRAG = 28, PS_A_LOOP = 29,
                    PS_A_POST = 30, PS_A_FINISH = 31, PS_M_ML = 32, PS_M_W = 33, PS_M_O = 34,
                    PS_A_END = 35, PS_EMBED = 36, PS_ARGMAX = 37, PS_A_LWAIT = 38, PS_G_SWAIT = 39,
-                   PS_MOE_ROUTE = 40, PS_TOTAL = 63 };
+                   PS_MOE_ROUTE = 40, PS_L_ISSUE = 41, PS_L_BLOCK = 42, PS_L_DEP = 43,
+                   PS_L_SLOTS = 44, PS_L_NBLOCK = 45, PS_T_RET = 46, PS_T_CALL = 47, PS_TOTAL = 63 };
+// loader sections (lane 0 of the loader; MK_PROF builds): cycles issuing, cycles waiting
+// for a free ring slot, cycles waiting on a routing / step dependency, slots issued,
+// slots that found the ring full
+#ifdef MK_PROF
+#define MK_PROF_L(pr, sec) do { if ((pr).lane == 0 && !(pr).pf) { \
+    const long long t_ = clock64(); (pr).sm->prof[sec] += t_ - (pr).ppt; (pr).ppt = t_; } } while (0)
+#define MK_PROF_LCOUNT(pr, sec) do { if ((pr).lane == 0 && !(pr).pf) (pr).sm->prof[sec] += 1; } while (0)
+#else
+#define MK_PROF_L(pr, sec) do { } while (0)
+#define MK_PROF_LCOUNT(pr, sec) do { } while (0)
+#endif
 
 enum TraceCode { TR_WAIT = 1, TR_READY = 2, TR_DONE = 3, TR_PIECE = 4, TR_MERGE = 5, TR_END = 6,
                  TR_P_STAGE = 11, TR_P_BLOCK = 12, TR_P_GO = 13,
@@ -230,6 +250,7 @@ struct Smem {
     // evicting, and cost a global round trip each (a routing pass of ~2 us took ~12 us).
     StepArgs args;
     __align__(16) LayerPlan lp[2];  // consumers' copies of the plans of layers l (l & 1) and l + 1
+    __align__(16) LayerPlan lpl[2]; // the loader's copies (it runs ahead of the consumers)
     // MoE routing of the current layer, written by the consumers, read by the loader too
     volatile int moe_ready;            // step * kMaxLayers + layer + 1 whose routing is below
     int moe_nu;                        // experts in the union of the batch rows' routes
@@ -526,7 +547,7 @@ __device__ __forceinline__ int num_groups(const GemvStage& s, int n) {
     return s.kind == G_GU ? 2 * g : g;
 }
 __device__ __forceinline__ int group_rows(const GemvStage& s, int n, int gi, int ngate) {
-    const int base = kGroupRows * (s.kind == G_GU ? (gi % ngate) : gi);
+    const int base = kGroupRows * (s.kind == G_GU && gi >= ngate ? gi - ngate : gi);
     return min(kGroupRows, n - base);
 }
 // weight row i of row group gi, as a pointer to its first column (of k-chunk 0)
@@ -822,6 +843,9 @@ struct Producer {
     bool pf = false;
     // page-table batch cache: ids of logical pages [pt_lp0, pt_lp0 + 32) of sequence pt_b
     int pt_b = -1, pt_lp0 = 0, pt_ids = -1;
+#ifdef MK_PROF
+    long long ppt = 0;  // cycle count at the loader's last profile mark
+#endif
 
     __device__ __forceinline__ bool acquire_slot(int task) {
         if (pf) {
@@ -843,12 +867,15 @@ struct Producer {
         }
         if (lane == 0) sm->lseq = seq;
         int ok = 1;
+        MK_PROF_L(*this, PS_L_ISSUE);
+        MK_PROF_LCOUNT(*this, PS_L_SLOTS);
         if (lane == 0) {
             if (sm->abort) ok = 0;
             else if (seq >= (uint32_t)kStages) {
                 const uint32_t bar = smem_u32(&sm->empty[seq % kStages]);
                 const uint32_t parity = ((seq / kStages) - 1) & 1;
                 if (!mbar_try_wait(bar, parity)) {
+                    MK_PROF_LCOUNT(*this, PS_L_NBLOCK);
                     MK_TRACE_P(*this, TR_P_BLOCK, task);
                     // a full ring only stalls when a consumer stalls; let the consumer's
                     // own (shorter) wait report the cause first
@@ -857,6 +884,7 @@ struct Producer {
                 }
             }
         }
+        MK_PROF_L(*this, PS_L_BLOCK);
         return __shfl_sync(0xffffffffu, ok, 0) != 0;
     }
     __device__ __forceinline__ void copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -881,11 +909,19 @@ struct Producer {
                 for (int gi = 0; gi < ng; ++gi) {
                     if (!acquire_slot(s.task_id)) return false;
                     const int nr = group_rows(s, n, gi, ngate);
-                    const int ncop = (nr + geo.rpc - 1) / geo.rpc;
+                    const int ncop = (nr + geo.rpc - 1) >> geo.rpc_log2;
                     const uint32_t dst = slot_addr(), bar = full_bar();
                     if (lane == 0 && !pf) mbar_arrive_expect_tx(bar, (uint32_t)(nr * geo.kc * 2));
                     __syncwarp();
-                    if (lane < ncop) {
+                    if (MK_PF_MODE != 0 && pf) {  // every lane prefetches lines of the rows
+                        for (int i = 0; i < nr; ++i) {
+                            const char* row = reinterpret_cast<const char*>(gemv_row(s, r0, gi, ngate, i) + cb);
+                            for (int o = lane * 128; o < geo.kc * 2; o += 32 * 128) {
+                                if (MK_PF_MODE == 2) l2_prefetch_line_keep(row + o);
+                                else l2_prefetch_line(row + o);
+                            }
+                        }
+                    } else if (lane < ncop) {
                         const int i0 = lane * geo.rpc;
                         const int cnt = min(geo.rpc, nr - i0);
                         const bf16* p0 = gemv_row(s, r0, gi, ngate, i0) + cb;
@@ -907,14 +943,21 @@ struct Producer {
         return true;
     }
 
+    bool last_ok = true;  // result of the out-of-line shared-prefix walk
+
+    // The attention stage: without shared-prefix groups inline; with them out of line
+    // (a rare path whose code would otherwise sit in the loader's hot loop).
     template <int HD>
-    __device__ __forceinline__ bool attention(int l, int cta) {
+    __device__ __forceinline__ bool attention(int l, int cta);
+
+    template <int HD, bool GROUPS>
+    __device__ __forceinline__ bool attention_walk(int l, int cta) {
         const Plan& p = a->p;
         constexpr int PPS = 512 / HD;   // pages per ring slot (K + V of one kv head)
         constexpr int NB = HD / 64;     // 64-wide boxes per page row
         MK_TRACE_P(*this, TR_P_STAGE, l * 16 + ST_ATTN);
         bool ok = true;
-        for_each_piece(*a, sm->ppos, l, cta, [&](const Piece& pc) {
+        auto walk = [&](const Piece& pc) {
             if (!ok) return;
             const int b = pc.b, g = pc.g, u = pc.u, n = pc.n;
             const SeqSpan& sp = pc.sp;
@@ -944,7 +987,17 @@ struct Producer {
                 const uint32_t dst = slot_addr(), bar = full_bar();
                 if (lane == 0 && !pf) mbar_arrive_expect_tx(bar, (uint32_t)(np * 2 * 2 * kPage * HD));
                 __syncwarp();
-                if (lane < nbox) {
+                if (MK_PF_MODE != 0 && pf) {  // every lane prefetches lines of the pages
+                    for (int q = 0; q < np * 2; ++q) {
+                        const int pg = __shfl_sync(0xffffffffu, pt_ids, (want - pt_lp0 + (q >> 1)) & 31);
+                        const char* blk = reinterpret_cast<const char*>(
+                            p.kv + (size_t)((((l * p.num_pages + pg) * 2 + (q & 1)) * p.Hkv + g) * kPage) * HD);
+                        for (int o = lane * 128; o < kPage * HD * 2; o += 32 * 128) {
+                            if (MK_PF_MODE == 2) l2_prefetch_line_keep(blk + o);
+                            else l2_prefetch_line(blk + o);
+                        }
+                    }
+                } else if (lane < nbox) {
                     const int row = (((l * p.num_pages + page) * 2 + kv) * p.Hkv + g) * kPage;
                     if (pf) l2_prefetch_2d(tmap, bx * 64, row);
                     else tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, tmap, bx * 64, row,
@@ -953,7 +1006,9 @@ struct Producer {
                 if (l == 1 && !pf) MK_TRACE_P(*this, TR_S_ISSUE, seq);
                 ++seq;
             }
-        });
+        };
+        if (GROUPS) for_each_group_piece(*a, sm->ppos, l, cta, walk);
+        else for_each_row_piece(*a, sm->ppos, l, cta, walk);
         return ok;
     }
 
@@ -1011,26 +1066,61 @@ struct Producer {
     __device__ __forceinline__ void run(int cta) {
         policy = policy_evict_first();
         if (lane == 0) prefetch_tmap(tmap);
+#ifdef MK_PROF
+        ppt = clock64();
+#endif
         const Plan& p = a->p;
         bool ok = !sm->abort;
         const int nsteps = MULTI ? a->n_steps : 1;
+        // The loader keeps its own double-buffered copy of the layer plans in shared
+        // memory: layer l + 1's plan is fetched while layer l streams, so a stage start
+        // never waits on a global read. (The L2 prefetch walker reads them from global
+        // memory: it must not touch the loader's buffers.)
+        static_assert(sizeof(LayerPlan) / 16 <= 32, "a layer plan copies in one warp pass");
+        auto fetch_plan = [&](int l) {
+            if (!pf && lane < (int)(sizeof(LayerPlan) / 16))
+                cp_async_16(smem_u32(&sm->lpl[l & 1]) + 16 * lane,
+                            reinterpret_cast<const uint8_t*>(p.layers + l) + 16 * lane);
+        };
+        auto plan = [&](int l) -> const LayerPlan& { return pf ? p.layers[l] : sm->lpl[l & 1]; };
         for (int step = 0; step < nsteps && ok; ++step) {
             if (MULTI && step > 0 && lane < a->B) sm->ppos[lane] += 1;
+            fetch_plan(0);
             __syncwarp();
-            for (int l = 0; l < p.L && ok; ++l) {
-                ok = ok && gemv(make_gemv(*a, G_QKV, l, sm), cta);
-                if (MULTI && step > 0 && l == 0) ok = ok && wait_step(step);
-                ok = ok && attention<HD>(l, cta);
-                ok = ok && gemv(make_gemv(*a, G_O, l, sm), cta);
-                if (p.E > 0) {
-                    ok = ok && gemv(make_gemv(*a, G_ROUTE, l, sm), cta);
-                    ok = ok && wait_route(step, l);
+            // the stages in order, as one loop with a single copy of the GEMV walker (a
+            // compact loader keeps the step's instruction working set small): (layer l,
+            // stage st) = QKV, attention, O, [router], gate/up, down; then the LM head
+            for (int l = 0, st = 0; ok;) {
+                if (st == 0 && l < p.L) {
+                    cp_async_wait_all();  // layer l's plan is in place
+                    __syncwarp();
+                    if (l + 1 < p.L) fetch_plan(l + 1);  // slot (l + 1) & 1 held layer l - 1
                 }
-                ok = ok && gemv(make_gemv(*a, G_GU, l, sm), cta);
-                ok = ok && gemv(make_gemv(*a, G_DOWN, l, sm), cta);
+                int kind;
+                if (l == p.L) kind = G_LM;
+                else if (st == 0) kind = G_QKV;
+                else if (st == 1) kind = -1;  // attention
+                else if (st == 2) kind = G_O;
+                else if (st == 3) kind = G_ROUTE;
+                else kind = st == 4 ? G_GU : G_DOWN;
+                if (kind == -1) {
+                    if (MULTI && step > 0 && l == 0) ok = wait_step(step);
+                    ok = ok && attention<HD>(l, cta);
+                } else {
+                    if (kind == G_GU && p.E > 0) {
+                        MK_PROF_L(*this, PS_L_ISSUE);
+                        ok = wait_route(step, l);
+                        MK_PROF_L(*this, PS_L_DEP);
+                    }
+                    const LayerPlan& lp = kind == G_LM ? p.layers[0] : plan(l);
+                    ok = ok && gemv(make_gemv(*a, kind, kind == G_LM ? 0 : l, lp, sm), cta);
+                }
+                if (kind == G_LM) break;
+                st += (st == 2 && p.E == 0) ? 2 : 1;  // dense layers have no router stage
+                if (st == 6) { st = 0; ++l; }
             }
-            if (ok) ok = gemv(make_gemv(*a, G_LM, 0, sm), cta);
         }
+        MK_PROF_L(*this, PS_L_ISSUE);
         // drain: never leave a copy in flight into shared memory
         if (lane == 0 && !pf) {
             const uint32_t first = seq > (uint32_t)kStages ? seq - kStages : 0;
@@ -1048,6 +1138,29 @@ struct Producer {
         __syncwarp();
     }
 };
+
+// The loader's attention walk with shared-prefix groups, out of line: it works on a copy
+// of the loader state (passed and returned by value), so the inline hot path keeps its
+// state in registers.
+template <int HD>
+__device__ __noinline__ Producer producer_attention_groups(Producer pr, int l, int cta) {
+    pr.last_ok = pr.attention_walk<HD, true>(l, cta);
+    return pr;
+}
+template <int HD>
+__device__ __forceinline__ bool Producer::attention(int l, int cta) {
+    if (!a->pf_on) return attention_walk<HD, false>(l, cta);
+    const Producer t = producer_attention_groups<HD>(*this, l, cta);
+    seq = t.seq;
+    pt_b = t.pt_b;
+    pt_lp0 = t.pt_lp0;
+    pt_ids = t.pt_ids;
+    tn = t.tn;
+#ifdef MK_PROF
+    ppt = t.ppt;
+#endif
+    return t.last_ok;
+}
 
 // ------------------------------------------------------------------ consumer pieces
 // rstd[b] = 1 / sqrt(mean(src[b]^2) + eps); fixed summation order. Every k-step reads
@@ -1653,47 +1766,58 @@ __device__ __noinline__ uint32_t gemv_task_mma(uint32_t seq, int kind, int layer
     if (trace_slots(s)) MK_TRACE_C(c, TR_G_EPI, 0);
     return c.seq;
 }
-__device__ __forceinline__ void gemv_task(Ctx& c, int kind, int layer, int r0, int r1) {
-    const int B = c.a->B;
-    if (B > 4) c.seq = gemv_task_mma(c.seq, kind, layer, r0, r1);
-    else if (kind == G_LM) {
-        if (B == 1) c.seq = gemv_task_fma_lm<1>(c.seq, r0, r1);
-        else if (B == 2) c.seq = gemv_task_fma_lm<2>(c.seq, r0, r1);
-        else c.seq = gemv_task_fma_lm<4>(c.seq, r0, r1);
-    } else if (B == 1) c.seq = gemv_task_fma<1>(c.seq, kind, layer, r0, r1);
-    else if (B == 2) c.seq = gemv_task_fma<2>(c.seq, kind, layer, r0, r1);
-    else c.seq = gemv_task_fma<4>(c.seq, kind, layer, r0, r1);
+__device__ __forceinline__ uint32_t gemv_task_call(uint32_t seq, int kind, int layer, int r0, int r1) {
+    const int B = make_ctx(seq).a->B;
+    if (B > 4) return gemv_task_mma(seq, kind, layer, r0, r1);
+    if (kind == G_LM) {
+        if (B == 1) return gemv_task_fma_lm<1>(seq, r0, r1);
+        if (B == 2) return gemv_task_fma_lm<2>(seq, r0, r1);
+        return gemv_task_fma_lm<4>(seq, r0, r1);
+    }
+    if (B == 1) return gemv_task_fma<1>(seq, kind, layer, r0, r1);
+    if (B == 2) return gemv_task_fma<2>(seq, kind, layer, r0, r1);
+    return gemv_task_fma<4>(seq, kind, layer, r0, r1);
 }
 
-__device__ __forceinline__ void gemv_stage(Ctx& c, const GemvStage& s, int cta) {
-    const Plan& p = c.a->p;
-    int a0, a1;
-    cta_rows(s.R, cta, p.C, a0, a1);
-    const bool tg = tagged(*c.a);
-    MK_PROF_MARK(c, PS_OTHER);
-    if (a0 < a1) {
-        MK_TRACE_C(c, TR_WAIT, s.task_id);
-        if (!tg) consumer_wait(c, s.cnt_wait, s.task_id);
-        if (s.gain && !fused_norm_stage(*c.a, s)) rms_scale(s.kind, s.layer);
-        if (trace_slots(s)) MK_TRACE_C(c, TR_G_NORM, 0);
-        const int tr = task_rows(s.kind);
-        for (int r0 = a0; r0 < a1; r0 += tr) {
-            // a task's epilogue reads every warp's partials; the next task clears them
-            if (r0 > a0) consumer_sync();
-            gemv_task(c, s.kind, s.layer, r0, min(a1, r0 + tr));
-        }
-    }
-    if (!tg && s.cnt_pub >= 0) publish(c, s.cnt_pub, s.task_id);
-    else consumer_sync();  // every warp is done with the shared scratch of this stage
-    MK_PROF_MARK(c, PS_G_END + 4 * s.kind);
-    MK_TRACE_C(c, TR_DONE, s.task_id);
-}
 
 // One GEMV stage of layer `layer` (kind G_*), out of line with its own registers; takes
 // and returns the ring sequence number.
+// Only a few scalars stay live across the calls it makes (the context and the stage
+// description are rebuilt where needed), so it saves and restores nothing around them.
 __device__ __noinline__ uint32_t gemv_stage_call(uint32_t seq, int kind, int layer, int cta) {
+    int a0, a1, task, cnt_wait, cnt_pub;
+    bool norm, tg;
+    {
+        const Ctx c = make_ctx(seq);
+        MK_PROF_MARK(c, PS_T_CALL);
+        const GemvStage s = make_gemv(*c.a, kind, layer, c.sm->lp[kind == G_LM ? 0 : (layer & 1)], c.sm);
+        cta_rows(s.R, cta, c.a->p.C, a0, a1);
+        task = s.task_id;
+        cnt_wait = s.cnt_wait;
+        cnt_pub = s.cnt_pub;
+        norm = s.gain && !fused_norm_stage(*c.a, s);
+        tg = tagged(*c.a);
+        MK_PROF_MARK(c, PS_OTHER);
+        MK_TRACE_C(c, TR_WAIT, task);
+    }
+    if (a0 < a1) {
+        if (!tg) {
+            Ctx c = make_ctx(seq);
+            consumer_wait(c, cnt_wait, task);
+        }
+        if (norm) rms_scale(kind, layer);
+        const int tr = task_rows(kind);
+        for (int r0 = a0; r0 < a1; r0 += tr) {
+            // a task's epilogue reads every warp's partials; the next task clears them
+            if (r0 > a0) consumer_sync();
+            seq = gemv_task_call(seq, kind, layer, r0, min(a1, r0 + tr));
+        }
+    }
     Ctx c = make_ctx(seq);
-    gemv_stage(c, make_gemv(*c.a, kind, layer, c.sm->lp[kind == G_LM ? 0 : (layer & 1)], c.sm), cta);
+    if (!tg && cnt_pub >= 0) publish(c, cnt_pub, task);
+    else consumer_sync();  // every warp is done with the shared scratch of this stage
+    MK_PROF_MARK(c, PS_G_END + 4 * kind);
+    MK_TRACE_C(c, TR_DONE, task);
     return c.seq;
 }
 
@@ -2200,22 +2324,31 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
     return c.seq;
 }
 
-template <int HD>
+// The attention stage of layer l; GROUPS: with shared-prefix groups declared (a separate
+// function, so the common path carries none of the group partition's code).
+template <int HD, bool GROUPS>
 __device__ __noinline__ uint32_t attention_stage(uint32_t seq, int l, int cta) {
     Ctx c = make_ctx(seq);
     MK_PROF_MARK(c, PS_OTHER);
     MK_TRACE_C(c, TR_WAIT, l * 16 + ST_ATTN);
     // every piece first writes its partial record; then each split merges its slice
-    for_each_piece(*c.a, c.sm->pos, l, cta, [&](const Piece& pc) {
+    auto piece = [&](const Piece& pc) {
         MK_TRACE_C(c, TR_PIECE, (uint32_t)(pc.b * 256 + pc.g));
         if (pc.prefix) c.seq = attention_piece<HD, true>(c.seq, l, pc);
         else c.seq = attention_piece<HD, false>(c.seq, l, pc);
-    });
-    for_each_piece(*c.a, c.sm->pos, l, cta, [&](const Piece& pc) {
+    };
+    auto merge = [&](const Piece& pc) {
         if (pc.prefix) return;  // a shared prefix's records are merged by each row's own CTAs
         attention_merge<HD>(l, pc.b, pc.g, pc.split, pc.nsplit, pc.nrec);
         MK_TRACE_C(c, TR_MERGE, (uint32_t)(pc.b * 256 + pc.g));
-    });
+    };
+    if (GROUPS) {
+        for_each_group_piece(*c.a, c.sm->pos, l, cta, piece);
+        for_each_group_piece(*c.a, c.sm->pos, l, cta, merge);
+    } else {
+        for_each_row_piece(*c.a, c.sm->pos, l, cta, piece);
+        for_each_row_piece(*c.a, c.sm->pos, l, cta, merge);
+    }
     // larger batches: every CTA counts its (possibly empty) share of the merges
     if (!tagged(*c.a)) publish(c, cnt_stage(l, ST_ATTN), l * 16 + ST_ATTN);
     MK_PROF_MARK(c, PS_A_END);
@@ -2459,15 +2592,20 @@ __device__ __forceinline__ void consumer_run(Ctx& c, int cta) {
             if (c.tid < kPlanChunks) cp_async_wait_all();
             consumer_sync();  // layer l's plan is in place; slot (l + 1) & 1 is free
             c.seq = gemv_stage_call(c.seq, G_QKV, l, cta);
+            MK_PROF_MARK(c, PS_T_RET);
             if (l + 1 < p.L) fetch_plan(l + 1);  // read at the next layer, after a barrier
-            c.seq = attention_stage<HD>(c.seq, l, cta);
+            c.seq = c.a->pf_on ? attention_stage<HD, true>(c.seq, l, cta) : attention_stage<HD, false>(c.seq, l, cta);
+            MK_PROF_MARK(c, PS_T_RET);
             c.seq = gemv_stage_call(c.seq, G_O, l, cta);
+            MK_PROF_MARK(c, PS_T_RET);
             if (p.E > 0) {
                 c.seq = gemv_stage_call(c.seq, G_ROUTE, l, cta);
                 moe_route(l);
             }
             c.seq = gemv_stage_call(c.seq, G_GU, l, cta);
+            MK_PROF_MARK(c, PS_T_RET);
             c.seq = gemv_stage_call(c.seq, G_DOWN, l, cta);
+            MK_PROF_MARK(c, PS_T_RET);
         }
         c.seq = gemv_stage_call(c.seq, G_LM, 0, cta);
         argmax_finish<MULTI>(c, cta);
