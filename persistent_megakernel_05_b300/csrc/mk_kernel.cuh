@@ -45,9 +45,7 @@ constexpr int kPrefetchWarp = 11;
 __device__ __forceinline__ bool idle_warp(int w) { return w == 4 || w == 8; }
 __device__ __forceinline__ int consumer_index(int w) { return w - 1 - (w > 4) - (w > 8); }
 constexpr int kDefaultPrefetchSlots = 0;          // L2 prefetch lead (slots); 0 = off
-#ifndef MK_PF_MODE
-#define MK_PF_MODE 0  // prefetch walker: 0 TMA bulk prefetch, 1 lane line prefetch, 2 same, evict_last
-#endif
+
 // Shared-memory ring depth. Four 33 KB slots keep HBM streaming (132 KB in flight per
 // SM) and leave ~90 KB of the SM's unified L1/shared array to L1: the consumers' saved
 // registers at calls and the norm-gain reads then hit L1 instead of waiting on L2.
@@ -913,15 +911,7 @@ struct Producer {
                     const uint32_t dst = slot_addr(), bar = full_bar();
                     if (lane == 0 && !pf) mbar_arrive_expect_tx(bar, (uint32_t)(nr * geo.kc * 2));
                     __syncwarp();
-                    if (MK_PF_MODE != 0 && pf) {  // every lane prefetches lines of the rows
-                        for (int i = 0; i < nr; ++i) {
-                            const char* row = reinterpret_cast<const char*>(gemv_row(s, r0, gi, ngate, i) + cb);
-                            for (int o = lane * 128; o < geo.kc * 2; o += 32 * 128) {
-                                if (MK_PF_MODE == 2) l2_prefetch_line_keep(row + o);
-                                else l2_prefetch_line(row + o);
-                            }
-                        }
-                    } else if (lane < ncop) {
+                    if (lane < ncop) {
                         const int i0 = lane * geo.rpc;
                         const int cnt = min(geo.rpc, nr - i0);
                         const bf16* p0 = gemv_row(s, r0, gi, ngate, i0) + cb;
@@ -987,17 +977,7 @@ struct Producer {
                 const uint32_t dst = slot_addr(), bar = full_bar();
                 if (lane == 0 && !pf) mbar_arrive_expect_tx(bar, (uint32_t)(np * 2 * 2 * kPage * HD));
                 __syncwarp();
-                if (MK_PF_MODE != 0 && pf) {  // every lane prefetches lines of the pages
-                    for (int q = 0; q < np * 2; ++q) {
-                        const int pg = __shfl_sync(0xffffffffu, pt_ids, (want - pt_lp0 + (q >> 1)) & 31);
-                        const char* blk = reinterpret_cast<const char*>(
-                            p.kv + (size_t)((((l * p.num_pages + pg) * 2 + (q & 1)) * p.Hkv + g) * kPage) * HD);
-                        for (int o = lane * 128; o < kPage * HD * 2; o += 32 * 128) {
-                            if (MK_PF_MODE == 2) l2_prefetch_line_keep(blk + o);
-                            else l2_prefetch_line(blk + o);
-                        }
-                    }
-                } else if (lane < nbox) {
+                if (lane < nbox) {
                     const int row = (((l * p.num_pages + page) * 2 + kv) * p.Hkv + g) * kPage;
                     if (pf) l2_prefetch_2d(tmap, bx * 64, row);
                     else tma_load_2d(dst + i * 64 * HD + kv * 32 * HD + bx * 2048, tmap, bx * 64, row,
@@ -1363,7 +1343,7 @@ __device__ __forceinline__ void gemv_fma(Ctx& c, const GemvStage& s, int r0, int
         float2 gg[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-            gg[t] = (s.gain && has_p) ? __ldg(reinterpret_cast<const float2*>(s.gain + base + 16 * t))
+            gg[t] = (s.gain && has_p) ? ldg_na_f2(reinterpret_cast<const float2*>(s.gain + base + 16 * t))
                                       : make_float2(0.f, 0.f);
         if (!c.sm->abort) {  // poll until every word carries the awaited tag
             Spin sp;
@@ -2045,11 +2025,11 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
             for (int i = c.tid; i < nrows * (HD / 2); i += kConsumerThreads) {
                 const int r = i / (HD / 2);
                 const int pr = r == 0 ? pos : c.sm->pos[piece_row(pc.rows, r)];
-                rs[i] = __ldg(p.rope + (size_t)pr * (HD / 2) + (i - r * (HD / 2)));
+                rs[i] = ldg_na_f2(p.rope + (size_t)pr * (HD / 2) + (i - r * (HD / 2)));
             }
         } else {
             const float2* rope = p.rope + (size_t)pos * (HD / 2);
-            for (int i = c.tid; i < HD / 2; i += kConsumerThreads) rs[i] = __ldg(rope + i);
+            for (int i = c.tid; i < HD / 2; i += kConsumerThreads) rs[i] = ldg_na_f2(rope + i);
         }
         // q of the columns, then (appending piece) k and v: pairs of tagged words, all of
         // a thread's pairs in flight at once, polled until they carry the QKV tag

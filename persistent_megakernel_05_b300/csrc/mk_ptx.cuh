@@ -79,17 +79,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
 __device__ __forceinline__ void l2_prefetch_1d(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
-// L2 prefetch of the 128-byte line holding `p` (one per lane; no TMA involvement)
-__device__ __forceinline__ void l2_prefetch_line(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-__device__ __forceinline__ void l2_prefetch_line_keep(const void* p) {
-    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
-}
 // L2 prefetch of one tensor-map box
 __device__ __forceinline__ void l2_prefetch_2d(const void* tmap, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
                  ::"l"(tmap), "r"(x), "r"(y) : "memory");
+}
+// read-only 8-byte load that does not allocate in L1 (L1 is kept for the threads' saved
+// registers; these values are read once per stage)
+__device__ __forceinline__ float2 ldg_na_f2(const float2* p) {
+    float2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
 }
 // 16-byte asynchronous global -> shared copy (no register, no wait at issue)
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
