@@ -481,9 +481,22 @@ def other_config(mk, local, name, B, ctx, steps, warmup, prefix_pages=0, private
 
 
 # ------------------------------------------------------------------ CPU baseline (oracle)
-def oracle_sample(cfg, W_cpu, kv_host, pt, budget_s=20.0, max_steps=16, B=1):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), or '' if unavailable."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return ""
+
+
+def oracle_sample(cfg, W_cpu, kv_host, pt, budget_s=12.0, max_steps=16, B=1):
     """Times the CPU oracle, as it stands, on a bounded sample of the same workload:
-    consecutive decode steps at positions 8192, 8193, ... until the budget is spent."""
+    consecutive decode steps at positions 8192, 8193, ... until the budget is spent, on
+    every core the process may use; then one step on a single thread."""
     import oracle
     om = oracle.OracleModel(cfg, W_cpu)
     threads = oracle.default_threads()
@@ -497,10 +510,15 @@ def oracle_sample(cfg, W_cpu, kv_host, pt, budget_s=20.0, max_steps=16, B=1):
         t_sum += time.perf_counter() - t0
         tok = int(nx[0])
         done += 1
+    pos = CTX + done
+    t0 = time.perf_counter()
+    om.decode_step(kv_host, [tok] * B, [pos] * B, np.repeat(pt[:1], B, 0), [pos + 1] * B, nthreads=1)
+    t1 = time.perf_counter() - t0
     return {"value": B * done / t_sum, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "single_thread_value": B / t1, "cpu_model": cpu_model(),
             "sample": f"{done} consecutive decode steps of the dense-2b batch-{B} workload "
-                      f"(context {CTX}..{CTX + done - 1}), {t_sum:.1f} s of CPU time, "
-                      f"plain C fp32, OpenMP over output rows"}
+                      f"(context {CTX}..{CTX + done - 1}), {t_sum:.1f} s on {threads} threads, then "
+                      f"step {CTX + done} on 1 thread ({t1:.1f} s); plain C fp32, OpenMP over output rows"}
 
 
 def reference_arm(args, rank, world):
@@ -520,9 +538,9 @@ def reference_arm(args, rank, world):
     import oracle
     om = oracle.OracleModel(cfg, W)
     threads = oracle.default_threads()
-    # warm-up: min(W, 1) steps; timed: up to K steps within a 90 s budget
+    # warm-up: W steps, as the repo arm; timed: up to K steps within a 90 s budget
     tok = 1
-    for w in range(min(args.warmup, 1)):
+    for w in range(args.warmup):
         _, nx = om.decode_step(kv_host, [tok], [CTX + w], pt[:1], [CTX + w + 1], nthreads=threads)
         tok = int(nx[0])
     done, t0 = 0, time.perf_counter()
@@ -537,13 +555,13 @@ def reference_arm(args, rank, world):
               f"(90 s budget), plain C fp32 oracle, OpenMP over output rows")
     emit({
         "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
-        "n_gpus": world, "steps": done, "warmup": min(args.warmup, 1),
+        "n_gpus": world, "steps": done, "warmup": args.warmup,
         "ms_per_step": 1000.0 * el / max(done, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "dense-2b decoder, batch 1, 8192-token seeded paged KV, greedy decode",
                    "batch": 1, "context": CTX},
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }, rank)
 
@@ -596,8 +614,9 @@ def main():
     ms = elapsed_ms / args.steps
     value = whole_job_value(world, 1, args.steps, elapsed_ms)
     lo = [[0] for _ in range(cfg.n_layers)]
-    pos_mean = CTX + (CYCLE - 1) / 2.0
-    algo = algorithmic_bytes(cfg, 1, lo, [pos_mean])
+    # positions of the timed steps (the decode loop's step t runs at CTX + t mod CYCLE)
+    timed_pos = [CTX + (t % CYCLE) for t in range(args.warmup, args.warmup + args.steps)]
+    algo = algorithmic_bytes(cfg, 1, lo, [float(np.mean(timed_pos))])
     kern_ms = statistics.mean(per)
     peak, peak_src = measured_peak()
     achieved = algo / (kern_ms / 1000.0) / 1e9
@@ -632,7 +651,9 @@ def main():
     # batch 8 (secondary workload)
     if not args.no_batch8:
         cfg8 = synth.DENSE_2B_SWA.with_(n_layers=cfg.n_layers)
-        steps8 = min(args.steps, 512)
+        # the configuration's 256 decode steps (at least), so that the replacement events
+        # (every 64 steps) fall inside the timed window whatever --steps is
+        steps8 = min(max(args.steps, 256), 512)
         S8 = setup_b8(cfg8, W, local, args.warmup + steps8, mk)
         one8, st8, en8 = run_device_loop(S8, steps8, args.warmup, cfg8, batch8=True)
         el8, _ = timed_region(one8, args.warmup, steps8, dist)
@@ -649,8 +670,10 @@ def main():
                    for l in range(cfg8.n_layers)]
             bytes8 += algorithmic_bytes(cfg8, 8, los, [int(x) for x in p])
         ach8 = bytes8 / (sum(per8) / 1000.0) / 1e9
+        events = sum(1 for t in range(args.warmup, args.warmup + steps8) if t > 0 and t % 64 == 0)
         out["batch8"] = {"value": round(whole_job_value(world, 8, steps8, el8), 2), "unit": "tokens/s",
                          "steps": steps8, "ms_per_step": round(el8 / steps8, 4),
+                         "replacement_events_timed": events,
                          "hbm_gbs": round(ach8, 1), "pct_of_8tbs": round(100 * ach8 / NOMINAL_HBM_GBS, 2),
                          "frac_of_measured_peak": round(ach8 / peak, 4),
                          "workload": "dense-2b, batch 8, lengths U[512, 8192], SWA 4096 on odd layers, "

@@ -661,6 +661,13 @@ struct NoAllocDevice {
     bool ready;
     int num_sms;
     unsigned char* base;  // device address of g_noalloc_scratch on this device
+    // the RoPE table the array holds (written by the last call on this device): it is
+    // rewritten only when the next call needs another one (theta, head dim, positions
+    // or its place in the array differ)
+    bool rope_valid;
+    float rope_theta;
+    int rope_hd, rope_max_pos;
+    size_t rope_off;
 };
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 std::mutex g_noalloc_mutex;
@@ -838,8 +845,24 @@ extern "C" mk_status mk_decode_step_noalloc(
     su.zero_dst = reinterpret_cast<uint32_t*>(base + o_zero);
     su.zero_words = (long long)((o_status + sizeof(int) * 4 - o_zero) / sizeof(uint32_t));
     su.L = L; su.d = d; su.hd = hd; su.max_pos = desc->max_positions; su.theta = desc->rope_theta;
-    noalloc_setup_kernel<<<C, 256, 0, s>>>(su);
-    if (cudaGetLastError() != cudaSuccess) return MK_ERR_LAUNCH;
+    {
+        // The RoPE table (max_positions x head_dim / 2 angles in double) is the costly
+        // part of the set-up: skip it when the array already holds this very table.
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        const bool same = D->rope_valid && D->rope_theta == desc->rope_theta && D->rope_hd == hd &&
+                          D->rope_max_pos == desc->max_positions && D->rope_off == o_rope;
+        if (same) su.max_pos = 0;
+        // from here on the array holds this call's table (the set-up kernel writes it
+        // before anything else on the stream reads it)
+        D->rope_valid = false;
+        noalloc_setup_kernel<<<C, 256, 0, s>>>(su);
+        if (cudaGetLastError() != cudaSuccess) return MK_ERR_LAUNCH;
+        D->rope_valid = true;
+        D->rope_theta = desc->rope_theta;
+        D->rope_hd = hd;
+        D->rope_max_pos = desc->max_positions;
+        D->rope_off = o_rope;
+    }
 
     mk::StepArgs a;
     mk::Plan& p = a.p;

@@ -3,8 +3,10 @@ the CPU oracle on the same seeded inputs and compare them.
 
 Parity bar (stated by the task's target): logits max-abs error <= 3e-2 (fp32
 accumulation), greedy tokens equal wherever the oracle's top-2 margin exceeds 0.1,
-KV slot writes at exactly the oracle's addresses (values within 1 BF16 ulp, since
-the two sides round K/V computed with different fp32 summation orders).
+KV slot writes at exactly the oracle's addresses, and every written value within 1
+BF16 ulp of the oracle's (the two sides round K/V computed with different fp32
+summation orders; elements much smaller than their row's scale are held to 1/4096 of
+the row RMS instead, see check_kv).
 """
 from __future__ import annotations
 
@@ -83,7 +85,16 @@ def bf16_ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return np.abs(key(a) - key(b))
 
 
-KV_REL = 2e-2
+# Every written K/V element must be within 1 BF16 ulp of the oracle's element, or within
+# 1/4096 of its row's RMS (a sixteenth of one ulp at the row's scale). The two sides
+# compute the same fp32 projection in different summation orders (and, past the first
+# layer, from fp32 inputs that differ in the last bits) and round it to BF16 once; that
+# fp32 difference is far below a BF16 ulp of any element of ordinary size, so those
+# round to the same or the neighbouring BF16 value. Only elements much smaller than
+# their row's scale have an ulp finer than the fp32 difference; they are held to the
+# absolute bound instead. KV_STATS collects the histogram of every check for the report.
+SMALL = 2.0 ** -12
+KV_STATS = {"elements": 0, "ulp0": 0, "ulp1": 0, "small": 0}
 
 
 def _f32(bits):
@@ -92,9 +103,8 @@ def _f32(bits):
 
 def check_kv(pair: Pair):
     """The GPU wrote exactly the slots the oracle wrote (bit-exact addresses: every other
-    byte of the pool is unchanged), and each written row agrees with the oracle's row
-    to KV_REL of the row's largest magnitude (the rows are fp32 projections computed in
-    a different summation order, then rounded to BF16)."""
+    byte of the pool is unchanged), and every written element is within 1 BF16 ulp of the
+    oracle's, or within 1/4096 of its row's RMS. Returns the number of written rows."""
     g = pair.gpu_kv_bits()
     o = pair.kv_host
     s = pair.kv_start
@@ -103,8 +113,36 @@ def check_kv(pair: Pair):
     # a slot may be written with an identical value by chance only with vanishing odds
     assert np.array_equal(g_changed, o_changed), "KV slot writes differ from the oracle's"
     assert np.array_equal(g[~g_changed], s[~g_changed])
-    gv, ov = _f32(g[g_changed]), _f32(o[g_changed])
-    scale = np.abs(ov).max(axis=-1, keepdims=True)
-    err = (np.abs(gv - ov) / np.maximum(scale, 1e-6)).max() if gv.size else 0.0
-    assert err <= KV_REL, f"KV rows differ by {err:.3g} of their scale"
+    gb, ob = g[g_changed], o[g_changed]
+    if gb.size:
+        ulp = bf16_ulp_diff(gb, ob)
+        gv, ov = _f32(gb).astype(np.float64), _f32(ob).astype(np.float64)
+        rms = np.sqrt(np.mean(ov ** 2, axis=-1, keepdims=True))
+        small = np.abs(gv - ov) <= SMALL * rms
+        bad = (ulp > 1) & ~small
+        assert not bad.any(), (f"{int(bad.sum())} K/V elements differ by more than 1 BF16 ulp and more "
+                               f"than 1/4096 of their row's RMS (max {int(ulp[bad].max())} ulp)")
+        KV_STATS["elements"] += int(ulp.size)
+        KV_STATS["ulp0"] += int((ulp == 0).sum())
+        KV_STATS["ulp1"] += int((ulp == 1).sum())
+        KV_STATS["small"] += int((ulp > 1).sum())
     return int(g_changed.sum())
+
+
+def check_kv_and_share(pair) -> int:
+    """check_kv, then hand the GPU's pool to the oracle as the new common history (and as
+    the new starting state): the next step is compared from identical K/V on both sides.
+    Long runs use it, since each side otherwise attends over its own rounding of every
+    earlier append and the two histories drift apart step by step."""
+    n = check_kv(pair)
+    g = pair.gpu_kv_bits()
+    pair.kv_host[...] = g
+    pair.kv_start[...] = g
+    return n
+
+
+def kv_stats_line() -> str:
+    n = max(KV_STATS["elements"], 1)
+    return (f"K/V elements checked {KV_STATS['elements']}: identical {KV_STATS['ulp0'] / n:.4%}, "
+            f"1 ulp apart {KV_STATS['ulp1'] / n:.4%}, more than 1 ulp apart but within 1/4096 of "
+            f"the row RMS {KV_STATS['small'] / n:.4%}")

@@ -450,3 +450,47 @@ def test_gumbel_max_at_tiny_temperature_is_the_argmax():
     for _ in range(20):
         z = rng.normal(size=300).astype(np.float32)
         assert oracle.sample_gumbel(z, 1e-4, 3, 17, 0) == int(np.argmax(z))
+
+
+def _gumbel_from_philox(seed: int, token: int, pos: int, row: int) -> float:
+    """The noise as the sampling rule defines it, from the known-answer-pinned generator:
+    counter (token, position, row, 0), key = seed (low word first), u from the top 24 bits
+    of word 0 plus one half, g = -log(-log u), evaluated here in float64."""
+    w0 = oracle.philox4x32_10([token, pos, row, 0], [seed & 0xFFFFFFFF, seed >> 32])[0]
+    u = ((w0 >> 8) + 0.5) / 16777216.0
+    return -np.log(-np.log(u))
+
+
+def test_gumbel_scores_use_the_documented_counter_layout():
+    """gumbel_scores(z)[i] = z_i / T + the noise of counter (i, pos, row, 0) under key =
+    seed: a swapped position / row, a wrong token index or a wrong key word fails."""
+    rng = np.random.default_rng(21)
+    for seed, pos, row in ((0, 0, 0), (3, 17, 2), ((5 << 32) | 9, 8193, 7), (123456789, 40000, 1)):
+        z = rng.normal(size=64).astype(np.float32)
+        T = 0.8
+        sc = oracle.gumbel_scores(z, T, seed, pos, row)
+        ref = np.array([z[i] / T + _gumbel_from_philox(seed, i, pos, row) for i in range(len(z))])
+        np.testing.assert_allclose(sc, ref, rtol=2e-6, atol=2e-5)
+        if pos != row:  # the counter is not symmetric in (position, row)
+            sw = oracle.gumbel_scores(z, T, seed, row, pos)
+            assert np.abs(sw - sc).max() > 1e-3
+
+
+def test_gumbel_scores_are_affine_in_the_logits_with_slope_one_over_t():
+    """The scores of z minus those of zero logits are exactly z / T (the noise does not
+    depend on the logits): a T * z or a dropped 1/T fails for T != 1."""
+    rng = np.random.default_rng(22)
+    z = rng.normal(size=500).astype(np.float32)
+    for T in (0.25, 0.5, 2.0, 3.0):
+        d = oracle.gumbel_scores(z, T, 7, 100, 3) - oracle.gumbel_scores(np.zeros_like(z), T, 7, 100, 3)
+        np.testing.assert_allclose(d, z.astype(np.float64) / T, rtol=1e-5, atol=2e-6)
+
+
+def test_sampled_token_is_the_argmax_of_the_scores():
+    """sample_gumbel picks the largest score (lowest index on ties) over many counters."""
+    rng = np.random.default_rng(23)
+    for k in range(200):
+        z = rng.normal(size=257).astype(np.float32)
+        pos, row, seed = int(rng.integers(0, 1 << 20)), int(rng.integers(0, 8)), int(rng.integers(0, 1 << 62))
+        sc = oracle.gumbel_scores(z, 0.9, seed, pos, row)
+        assert oracle.sample_gumbel(z, 0.9, seed, pos, row) == int(np.argmax(sc))
