@@ -366,8 +366,8 @@ struct Spin {
     int it = 0;
     __device__ __forceinline__ bool again(const StepArgs& a, Smem* sm, int task) {
         if (sm->abort) return false;
-        if ((++it & 15) == 0 && !spin_check(a, sm, task, &t0)) return false;
-        __nanosleep(32);
+        if ((++it & 63) == 0 && !spin_check(a, sm, task, &t0)) return false;
+        if (it > 64) __nanosleep(32);
         return true;
     }
 };
