@@ -515,9 +515,13 @@ __device__ GemvStage make_gemv(const StepArgs& a, int kind, int l, const LayerPl
             s.src_tag = tag_of(a, l, TAG_GU);
             s.out_tag = tag_of(a, l, TAG_DOWN);
             s.cnt_wait = cnt_stage(l, ST_GU); s.cnt_pub = cnt_stage(l, ST_DOWN);
-            if (p.E > 0) {  // k-chunk j = the Fe columns of union slot j's expert
+            if (p.E > 0) {
+                // one dense GEMV over the union's columns side by side (union slot j holds
+                // columns [j Fe, (j + 1) Fe)): row r of the virtual matrix is the
+                // concatenation of row r of each union expert's [d][Fe] down matrix. The
+                // loader gathers each 2048-column chunk of a row from those matrices.
                 s.moe = 2; s.uni = sm->moe_uni; s.K = sm->moe_nu * p.Fe;
-                s.w0 = lp.exp_down; s.kcw = p.Fe; s.ldw = p.Fe; s.lds = p.hrow;
+                s.w0 = lp.exp_down; s.kcw = KCW; s.ldw = 0; s.lds = p.hrow;
                 return s;
             }
             s.K = p.F; s.w0 = lp.w_down;
@@ -564,10 +568,10 @@ __device__ __forceinline__ const bf16* gemv_row(const GemvStage& s, int r0, int 
     }
     return s.w0 + (size_t)r * s.ldw;
 }
-// element offset of k-chunk k0 within a weight row: the column itself, or for the MoE
-// down projection the start of union slot k0 / Fe's expert matrix
+// element offset of k-chunk k0 within a weight row (not used for the MoE down
+// projection, whose chunks are gathered from several expert matrices)
 __device__ __forceinline__ size_t chunk_base(const GemvStage& s, int k0) {
-    return s.moe == 2 ? (size_t)s.uni[k0 / s.Fe] * s.R * s.Fe : (size_t)k0;
+    return (size_t)k0;
 }
 
 // Shared-memory geometry of one weight slot (8 rows x kc columns of k-chunk k0).
@@ -911,7 +915,19 @@ struct Producer {
                     const uint32_t dst = slot_addr(), bar = full_bar();
                     if (lane == 0 && !pf) mbar_arrive_expect_tx(bar, (uint32_t)(nr * geo.kc * 2));
                     __syncwarp();
-                    if (lane < ncop) {
+                    if (s.moe == 2) {
+                        // MoE down projection: row i's columns [k0, k0 + kc) come from the
+                        // union experts they belong to; lane (i, segment) copies one piece
+                        const int i = lane >> 2;
+                        if (i < nr) {
+                            const int r = r0 + kGroupRows * gi + i;
+                            for (int j = k0 / s.Fe + (lane & 3); j * s.Fe < k0 + geo.kc; j += 4) {
+                                const int c0 = max(k0, j * s.Fe), c1 = min(k0 + geo.kc, (j + 1) * s.Fe);
+                                const bf16* src = s.w0 + ((size_t)s.uni[j] * s.R + r) * s.Fe + (c0 - j * s.Fe);
+                                copy(dst + i * geo.cpitch + (c0 - k0) * 2, src, (uint32_t)((c1 - c0) * 2), bar);
+                            }
+                        }
+                    } else if (lane < ncop) {
                         const int i0 = lane * geo.rpc;
                         const int cnt = min(geo.rpc, nr - i0);
                         const bf16* p0 = gemv_row(s, r0, gi, ngate, i0) + cb;
