@@ -1836,9 +1836,8 @@ struct FinishCols {
 // columns [ch0, ch0 + FinishCols) (left in shared memory by the piece) and write them as
 // this split's partial records, one per row, as tagged words. MULTI: a shared-prefix
 // piece (several rows, one or two column tiles); otherwise one row, one tile, one pass.
-// Non-inlined so the key loop keeps its registers to itself.
 template <int HD, bool MULTI>
-__device__ __noinline__ void attention_finish(int l, Piece pc, int ch0, int NC, int wpt_in) {
+__device__ __forceinline__ void attention_finish(int l, Piece pc, int ch0, int NC, int wpt_in) {
     Ctx c = make_ctx(0);
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
@@ -2512,6 +2511,7 @@ __device__ __noinline__ void moe_route(int l) {
         pw[c.lane + 32] = c.lane + 32 < E ? p1 : -1.f;
         __syncwarp();
         int r0 = 0, r1 = 0;
+#pragma unroll 8
         for (int e = 0; e < E; ++e) {
             const float v = pw[e];
             r0 += (v > p0 || (v == p0 && e < c.lane)) ? 1 : 0;
