@@ -205,15 +205,22 @@ typedef enum mk_option {
 } mk_option;
 MK_API mk_status mk_set_option(mk_handle *h, mk_option opt, int64_t value);
 
-/* Next-token rule from the next step on. temperature == 0 (the default): greedy argmax
- * (lowest index on ties). temperature > 0: a draw from softmax(logits / temperature),
- * taken as argmax_i (logits_i / temperature + g_i) with g_i = -log(-log u_i) standard
- * Gumbel noise; u_i comes from Philox4x32-10 with key = seed (low word first) and counter
- * (token i, positions[b], row b, 0), u = (top 24 bits of word 0 + 0.5) / 2^24. The draw is
- * a function of (seed, position, row, token) only, so a step can be replayed exactly.
- * The logits written by mk_decode_step stay the raw logits. Negative or non-finite
- * temperatures: MK_ERR_INVALID_ARG. mk_decode_step_noalloc is always greedy. */
-MK_API mk_status mk_set_sampling(mk_handle *h, float temperature, uint64_t seed);
+/* Next-token rule from the next step on. Source: the sampling modes of "Cohere,
+ * Megakernel sunum sistemini acik kaynak yapti", section "Sinirlar acikca yazilmis"
+ * (greedy, temperature, a limited top_k; no top_p).
+ *   temperature == 0 (the default): greedy argmax (lowest index on ties); top_k ignored.
+ *   temperature > 0: a draw from softmax(logits / temperature), taken as
+ *     argmax_i (logits_i / temperature + g_i) with g_i = -log(-log u_i) standard Gumbel
+ *     noise; u_i comes from Philox4x32-10 with key = seed (low word first) and counter
+ *     (token i, positions[b], row b, 0), u = (top 24 bits of word 0 + 0.5) / 2^24.
+ *   top_k in 1..32: the draw is limited to the top_k largest logits of the row (the
+ *     larger logit first, the lower index first among equal logits), i.e. softmax
+ *     renormalised over them; top_k 1 is the greedy token. top_k 0: no cut.
+ * The draw is a function of (seed, position, row, token) only, so a step can be replayed
+ * exactly. The logits written by mk_decode_step stay the raw logits. Negative or
+ * non-finite temperatures, or top_k outside 0..32: MK_ERR_INVALID_ARG.
+ * mk_decode_step_noalloc is always greedy. */
+MK_API mk_status mk_set_sampling(mk_handle *h, float temperature, int32_t top_k, uint64_t seed);
 
 /* Shared prefixes (cascade attention) for the next steps of batch `batch`. Source: the
  * prefix cache of "Cohere, Megakernel sunum sistemini acik kaynak yapti", section

@@ -81,6 +81,9 @@ def lib():
         L.or_gumbel.argtypes = [ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
         L.or_gumbel_scores.argtypes = [_f32p, ctypes.c_int32, ctypes.c_float, ctypes.c_uint64,
                                        ctypes.c_int32, ctypes.c_int32, _f32p]
+        L.or_sample_gumbel_topk.restype = ctypes.c_int32
+        L.or_sample_gumbel_topk.argtypes = [_f32p, ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
+                                            ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32]
         L.or_sample_gumbel.restype = ctypes.c_int32
         L.or_sample_gumbel.argtypes = [_f32p, ctypes.c_int32, ctypes.c_float, ctypes.c_uint64,
                                        ctypes.c_int32, ctypes.c_int32]
@@ -156,11 +159,13 @@ class OracleModel:
         self.m = m
 
     def decode_step(self, kv: np.ndarray, tokens, positions, page_table, seq_lens,
-                    nthreads: Optional[int] = None, temperature: float = 0.0, seed: int = 0):
+                    nthreads: Optional[int] = None, temperature: float = 0.0, seed: int = 0,
+                    top_k: int = 0):
         """One decode step; appends into ``kv`` (uint16, pool layout) in place.
         Returns (logits [B, vocab] float32, next_tokens [B] int32). temperature > 0
         samples the next tokens from softmax(logits / T) (Gumbel-max, Philox draws keyed
-        by ``seed``, counter (token, position, row)); else greedy."""
+        by ``seed``, counter (token, position, row)), restricted to the ``top_k`` largest
+        logits when top_k > 0; else greedy."""
         cfg = self.cfg
         assert kv.dtype == np.uint16 and kv.flags.c_contiguous
         num_pages = kv.shape[1]
@@ -178,9 +183,9 @@ class OracleModel:
                                   _ptr(nxt, _i32p), nthreads or default_threads())
         if rc != 0:
             raise ValueError(f"oracle decode_step returned {rc}")
-        if temperature > 0.0:  # Gumbel-max sampling from softmax(logits / T)
+        if temperature > 0.0:  # Gumbel-max sampling from softmax(logits / T), optionally top-k
             for b in range(B):
-                nxt[b] = sample_gumbel(logits[b], temperature, seed, int(positions[b]), b)
+                nxt[b] = sample_gumbel_topk(logits[b], temperature, top_k, seed, int(positions[b]), b)
         return logits, nxt
 
     def forward_full(self, tokens, nthreads: Optional[int] = None) -> np.ndarray:
@@ -268,6 +273,16 @@ def gumbel_scores(logits, temperature: float, seed: int, pos: int, row: int) -> 
     z = np.empty_like(v)
     lib().or_gumbel_scores(_ptr(v, _f32p), v.shape[0], temperature, seed, pos, row, _ptr(z, _f32p))
     return z
+
+
+def sample_gumbel_topk(logits, temperature: float, top_k: int, seed: int, pos: int, row: int) -> int:
+    """A draw from softmax(logits / T) over the top_k largest logits (lower index first
+    among equal logits); top_k 0 or >= vocab: no cut."""
+    v = _c(logits, np.float32)
+    r = int(lib().or_sample_gumbel_topk(_ptr(v, _f32p), v.shape[0], temperature, int(top_k), seed, pos, row))
+    if r < 0:
+        raise MemoryError("or_sample_gumbel_topk")
+    return r
 
 
 def sample_gumbel(logits, temperature: float, seed: int, pos: int, row: int) -> int:

@@ -226,6 +226,43 @@ int32_t or_sample_gumbel(const float *logits, int32_t n, float temperature, uint
     return best;
 }
 
+/* Temperature sampling limited to the top_k largest logits (1 <= top_k <= n): the
+ * candidate set is the top_k tokens in the order (larger logit first, lower index first
+ * among equal logits); the draw is the candidate with the largest logits_i / T + g_i,
+ * the lowest index among equal scores -- a draw from softmax(logits / T) renormalised
+ * over the candidates (Gumbel-max restricted to a subset). Selection: a candidate is a
+ * token with fewer than top_k tokens ahead of it in that order (a count, O(n^2) in the
+ * worst case but fine for the sizes the tests use; tokens below the top_k-th largest
+ * logit are rejected first). */
+int32_t or_sample_gumbel_topk(const float *logits, int32_t n, float temperature, int32_t top_k,
+                              uint64_t seed, int32_t pos, int32_t row) {
+    if (top_k < 1 || top_k >= n) return or_sample_gumbel(logits, n, temperature, seed, pos, row);
+    /* the top_k-th largest logit value (a lower bound for every candidate) */
+    float *tmp = (float *)malloc(sizeof(float) * (size_t)n);
+    if (!tmp) return -1;
+    memcpy(tmp, logits, sizeof(float) * (size_t)n);
+    for (int32_t k = 0; k < top_k; k++) {  /* partial selection sort, descending */
+        int32_t best = k;
+        for (int32_t i = k + 1; i < n; i++)
+            if (tmp[i] > tmp[best]) best = i;
+        const float t = tmp[k]; tmp[k] = tmp[best]; tmp[best] = t;
+    }
+    const float kth = tmp[top_k - 1];
+    free(tmp);
+    int32_t best = -1;
+    float bv = -INFINITY;
+    for (int32_t i = 0; i < n; i++) {
+        if (logits[i] < kth) continue;
+        int32_t ahead = 0;  /* tokens before i in (logit desc, index asc) order */
+        for (int32_t j = 0; j < n && ahead < top_k; j++)
+            if (logits[j] > logits[i] || (logits[j] == logits[i] && j < i)) ahead++;
+        if (ahead >= top_k) continue;
+        const float z = logits[i] / temperature + or_gumbel(seed, i, pos, row);
+        if (best < 0 || z > bv) { bv = z; best = i; }
+    }
+    return best;
+}
+
 /* Greedy: index of the largest value, the lowest index among equal maxima. */
 int32_t or_argmax(const float *v, int32_t n) {
     int32_t best = 0;

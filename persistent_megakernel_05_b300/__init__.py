@@ -117,7 +117,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mk_set_option.restype = ctypes.c_int
     L.mk_set_option.argtypes = [_vp, ctypes.c_int, i64]
     L.mk_set_sampling.restype = ctypes.c_int
-    L.mk_set_sampling.argtypes = [_vp, ctypes.c_float, ctypes.c_uint64]
+    L.mk_set_sampling.argtypes = [_vp, ctypes.c_float, ctypes.c_int32, ctypes.c_uint64]
     L.mk_set_shared_prefix.restype = ctypes.c_int
     L.mk_set_shared_prefix.argtypes = [_vp, i32, _P(i32), _P(i32)]
     L.mk_get_info.restype = ctypes.c_int
@@ -197,8 +197,8 @@ def mk_set_option(handle: int, opt: int, value: int):
     _check(load().mk_set_option(handle, opt, int(value)), "mk_set_option")
 
 
-def mk_set_sampling(handle: int, temperature: float, seed: int):
-    _check(load().mk_set_sampling(handle, float(temperature), int(seed) & (2 ** 64 - 1)),
+def mk_set_sampling(handle: int, temperature: float, seed: int, top_k: int = 0):
+    _check(load().mk_set_sampling(handle, float(temperature), int(top_k), int(seed) & (2 ** 64 - 1)),
            "mk_set_sampling")
 
 
@@ -384,9 +384,10 @@ class DecodeModel:
     def set_option(self, opt: int, value: int):
         mk_set_option(self.handle, opt, value)
 
-    def set_sampling(self, temperature: float, seed: int = 0):
-        """temperature 0: greedy; > 0: draw from softmax(logits / temperature)."""
-        mk_set_sampling(self.handle, temperature, seed)
+    def set_sampling(self, temperature: float, seed: int = 0, top_k: int = 0):
+        """temperature 0: greedy; > 0: draw from softmax(logits / temperature), over the
+        top_k largest logits when top_k > 0."""
+        mk_set_sampling(self.handle, temperature, seed, top_k)
 
     def set_shared_prefix(self, leader=(), shared_pages=()):
         """Rows b with the same leader[b] share logical pages [0, shared_pages[b]) of their

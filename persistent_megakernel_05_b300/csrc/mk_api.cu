@@ -34,6 +34,7 @@ struct mk_handle {
     uint32_t cnt_epoch = 0;         // steps since the counters were last zeroed
     int last_batch = 0;             // batch of the last step (selects the activation format)
     float temperature = 0.f;        // next-token rule: 0 greedy, > 0 Gumbel-max sampling
+    int top_k = 0;                  // sampling over the top_k largest logits (0: all)
     uint64_t seed = 0;
     long long timeout_ns = 1000000000LL;
     int skip_publish = -1;
@@ -237,6 +238,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     const size_t o_attnf = take(sizeof(float) * (size_t)maxB * Hq * hd);
     const size_t o_hf = take(sizeof(float) * (size_t)maxB * hrow);
     const size_t o_am = take(16 * (size_t)C * maxB);  // tagged (value, index) pairs
+    const size_t o_cand = take(16 * (size_t)C * maxB * mk::kMaxSampleTopK);  // top-k sampling lists
     h->counters_words = (size_t)(1 + L * mk::kStagesPerLayer) * mk::kCounterStride;
     h->arrivals_words = (size_t)mk::kCounterStride;
     const size_t o_cnt = take(sizeof(uint32_t) * h->counters_words);
@@ -334,6 +336,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     p.hf = (float*)(base + o_hf);
     p.counters = (uint32_t*)(base + o_cnt);
     p.amax = (uint64_t*)(base + o_am);
+    p.cand = (uint64_t*)(base + o_cand);
     p.arrivals = (uint32_t*)(base + o_arr);
     p.status = (int*)(base + o_status);
     p.kv = nullptr;
@@ -456,6 +459,7 @@ mk_status launch_steps(mk_handle* h, int32_t n_steps, const int32_t* tokens, con
     a.prefetch_slots = h->prefetch_slots;
     a.timeout_ns = h->timeout_ns;
     a.temperature = h->temperature;
+    a.top_k = h->top_k;
     a.seed_lo = (uint32_t)h->seed;
     a.seed_hi = (uint32_t)(h->seed >> 32);
     a.pf_on = h->pf_batch != 0;
@@ -553,9 +557,11 @@ mk_status mk_set_option(mk_handle* h, mk_option opt, int64_t value) {
     return MK_ERR_INVALID_ARG;
 }
 
-mk_status mk_set_sampling(mk_handle* h, float temperature, uint64_t seed) {
+mk_status mk_set_sampling(mk_handle* h, float temperature, int32_t top_k, uint64_t seed) {
     if (!h || !std::isfinite(temperature) || temperature < 0.f) return MK_ERR_INVALID_ARG;
+    if (top_k < 0 || top_k > mk::kMaxSampleTopK) return MK_ERR_INVALID_ARG;
     h->temperature = temperature;
+    h->top_k = top_k;
     h->seed = seed;
     return MK_OK;
 }
@@ -894,6 +900,7 @@ extern "C" mk_status mk_decode_step_noalloc(
     p.hf = (float*)(base + o_hf);
     p.counters = (uint32_t*)(base + o_cnt);
     p.amax = (uint64_t*)(base + o_am);
+    p.cand = nullptr;  // always greedy here
     p.arrivals = (uint32_t*)(base + o_arr);
     p.status = (int*)(base + o_status);
     p.kv = (bf16*)kv_pool;
@@ -912,6 +919,7 @@ extern "C" mk_status mk_decode_step_noalloc(
     a.prefetch_slots = mk::kDefaultPrefetchSlots;
     a.timeout_ns = 1000000000LL;
     a.temperature = 0.f;  // greedy
+    a.top_k = 0;
     a.seed_lo = a.seed_hi = 0;
     a.n_steps = 1;
     a.logits_last = logits;

@@ -62,6 +62,7 @@ constexpr int kTaskRows = 128;                     // <= 16 row groups of 8 per 
 constexpr int kMaxLayers = 128;
 constexpr int kMaxExperts = 64;                    // MoE: experts per layer (one warp routes a row)
 constexpr int kMaxTopK = 16;                       // MoE: experts routed per row
+constexpr int kMaxSampleTopK = 32;                 // sampling: largest top-k cut (one warp lane each)
 constexpr int kCounterStride = 32;                 // u32 words per counter (128 B apart)
 constexpr int kStagesPerLayer = 8;                 // counter slots per layer
 constexpr int kMaxOwnRows = 32;                    // residual rows a CTA owns: ceil(d / CTAs) <= 32
@@ -166,6 +167,7 @@ struct Plan {
     float* hf;
     uint32_t* counters;                 // stage counters, kCounterStride apart
     uint64_t* amax;                     // [C][maxB][2] tagged (value, index as float bits)
+    uint64_t* cand;                     // [C][maxB][kMaxSampleTopK][2] top-k sampling candidates
     uint32_t* arrivals;                 // (unused by the kernel; zeroed with the counters)
     int* status;                        // [0] code, [1] task
     bf16* kv;                           // paged pool base
@@ -188,6 +190,7 @@ struct StepArgs {
     uint32_t epoch;                     // step number mod 2^20, never 0: high bits of every tag
     uint32_t stage_target;              // counter target of every stage: steps since reset * C
     float temperature;                  // 0: greedy; > 0: Gumbel-max sampling
+    int top_k;                          // sampling over the top_k largest logits (0: all)
     uint32_t seed_lo, seed_hi;          // Philox key of the sampling draws
     int skip_publish;                   // task id whose outputs are never written, or -1
     int prefetch_slots;                 // L2 prefetch lead over the loader, in slots (0 = off)
@@ -231,6 +234,8 @@ struct Smem {
     float rstd[kMaxBatch];
     float amax_v[kMaxBatch];
     int amax_i[kMaxBatch];
+    float tk_v[kMaxBatch][kMaxSampleTopK];  // top-k sampling: each row's running top-k logits
+    int tk_i[kMaxBatch][kMaxSampleTopK];
     int pos[kMaxBatch];                    // consumers' positions of their current step
     int ppos[kMaxBatch];                   // the loader's positions of its current step
     int tok[kMaxBatch];                    // the next step's input tokens
@@ -268,6 +273,10 @@ struct Smem {
 };
 
 constexpr int kSmemBytes = 1024 + kStages * kSlotBytes + kScratchBytes + (int)sizeof(Smem);
+// The SM's unified L1 / shared array is split in fixed carveouts; staying within the
+// 164 KB one (with the 1 KB the runtime reserves per block) leaves ~90 KB to L1, which
+// the consumers' saved registers and gain reads depend on.
+static_assert(kSmemBytes + 1024 <= 164 * 1024, "shared memory beyond the 164 KB carveout shrinks L1");
 
 struct Ctx {
     const StepArgs* a;
@@ -1254,6 +1263,105 @@ __device__ __forceinline__ float gumbel_score(const StepArgs& a, float logit, in
 }
 __device__ __forceinline__ int cta_of(const Ctx&) { return blockIdx.x; }
 
+// ---- top-k sampling (the largest top_k logits of a row, then a Gumbel-max draw) ----
+// Order of the candidates: the larger logit first, the lower index first among equal ones.
+__device__ __forceinline__ bool tk_before(float v1, int i1, float v2, int i2) {
+    return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+__device__ __forceinline__ bool topk_sampling(const StepArgs& a) { return a.temperature > 0.f && a.top_k > 0; }
+// A warp's running top-K list (K <= 32): lane j holds entry j, in the order above; unused
+// entries are (-inf, INT_MAX). Every lane offers a candidate (cv, ci) (ignored when
+// !valid); the survivors of the cut by the current K-th entry are inserted one by one.
+__device__ __forceinline__ void tk_offer(float& lv, int& li, int K, float cv, int ci, bool valid) {
+    const int lane = (int)(threadIdx.x & 31);
+    float mv = __shfl_sync(0xffffffffu, lv, K - 1);
+    int mi = __shfl_sync(0xffffffffu, li, K - 1);
+    uint32_t m = __ballot_sync(0xffffffffu, valid && tk_before(cv, ci, mv, mi));
+    while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const float v = __shfl_sync(0xffffffffu, cv, src);
+        const int i = __shfl_sync(0xffffffffu, ci, src);
+        if (!tk_before(v, i, mv, mi)) continue;  // (uniform) the cut rose since the vote
+        const int pos = __popc(__ballot_sync(0xffffffffu, lane < K && tk_before(lv, li, v, i)));
+        const float pv = __shfl_up_sync(0xffffffffu, lv, 1);
+        const int pi = __shfl_up_sync(0xffffffffu, li, 1);
+        if (lane < K) {
+            if (lane > pos) { lv = pv; li = pi; }
+            else if (lane == pos) { lv = v; li = i; }
+        }
+        mv = __shfl_sync(0xffffffffu, lv, K - 1);
+        mi = __shfl_sync(0xffffffffu, li, K - 1);
+    }
+}
+// LM-head epilogue of a top-k sampling step: warp b offers the task's logits of row b to
+// the row's running list (kept in shared memory between tasks).
+__device__ __noinline__ void tk_lm_task(int b, int r0, int n, const float* yout) {
+    const Ctx c = make_ctx(0);
+    const int K = c.a->top_k;
+    float lv = c.lane < K ? c.sm->tk_v[b][c.lane] : -INFINITY;
+    int li = c.lane < K ? c.sm->tk_i[b][c.lane] : 0x7fffffff;
+    for (int r = c.lane; r - c.lane < n; r += 32)
+        tk_offer(lv, li, K, r < n ? yout[r * 8 + b] : -INFINITY, r0 + r, r < n);
+    if (c.lane < K) {
+        c.sm->tk_v[b][c.lane] = lv;
+        c.sm->tk_i[b][c.lane] = li;
+    }
+}
+// The step's draw for row b from every CTA's list (tagged pairs, written after the LM
+// head): warp-wide merge into the row's top-K, then argmax of logit / T + Gumbel noise
+// over it (lowest index on equal scores). Returns the token (lane-uniform).
+__device__ __noinline__ int tk_draw(int b, uint32_t tag, int task) {
+    const Ctx c = make_ctx(0);
+    const StepArgs& a = *c.a;
+    const Plan& p = a.p;
+    const int K = a.top_k;
+    float lv = -INFINITY;
+    int li = 0x7fffffff;
+    // lane j takes entry j of 8 CTAs at a time (one read round per 8 CTAs)
+    for (int ct0 = 0; ct0 < p.C; ct0 += 8) {
+        uint64_t w[8][2];
+        Spin sp;
+        for (;;) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                w[q][0] = w[q][1] = (uint64_t)tag << 32;
+                if (ct0 + q < p.C && c.lane < K)
+                    ll_ld2(p.cand + (((size_t)(ct0 + q) * p.maxB + b) * kMaxSampleTopK + c.lane) * 2, w[q][0], w[q][1]);
+            }
+            int miss = -1;
+#pragma unroll
+            for (int q = 7; q >= 0; --q)
+                if (ll_tag(w[q][0]) != tag || ll_tag(w[q][1]) != tag) miss = q;
+            if (!__any_sync(0xffffffffu, miss >= 0)) break;
+            // each lane waits on its first missing pair alone, then the batch is re-read
+            bool ok = true;
+            if (miss >= 0)
+                ok = ll_wait_pair(p.cand + (((size_t)(ct0 + miss) * p.maxB + b) * kMaxSampleTopK + c.lane) * 2,
+                                  tag, sp, a, c.sm, task);
+            if (!__all_sync(0xffffffffu, ok)) break;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            tk_offer(lv, li, K, ll_val(w[q][0]), __float_as_int(ll_val(w[q][1])),
+                     ct0 + q < p.C && c.lane < K);
+    }
+    const int pos = c.sm->pos[b];
+    float bz = -INFINITY;
+    int bi = 0x7fffffff;
+    if (c.lane < K && li != 0x7fffffff) {
+        bz = gumbel_score(a, lv, li, pos, b);
+        bi = li;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oz = __shfl_xor_sync(0xffffffffu, bz, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (oz > bz || (oz == bz && oi < bi)) { bz = oz; bi = oi; }
+    }
+    return bi == 0x7fffffff ? 0 : bi;
+}
+
 // the small-batch path computes the RMSNorm statistics from its own activation loads
 // when the whole input row is one k-chunk
 __device__ __forceinline__ bool fused_norm_stage(const StepArgs& a, const GemvStage& s) {
@@ -1694,7 +1802,9 @@ __device__ __forceinline__ void yout_epilogue(Ctx& c, const GemvStage& s, int r0
                     const int r = e / B, b = e % B;
                     a.logits[(size_t)b * p.V + r0 + r] = yout[r * 8 + b];
                 }
-            if (c.cw < B) {
+            if (c.cw < B && topk_sampling(a)) {
+                tk_lm_task(c.cw, r0, n, yout);
+            } else if (c.cw < B) {
                 const int b = c.cw;
                 const bool sample = a.temperature > 0.f;
                 const int pos = c.sm->pos[b];
@@ -2385,6 +2495,7 @@ __device__ __forceinline__ void argmax_finish(Ctx& c, int cta) {
     const int task = p.L * 16;
     const uint32_t tag = tag_of(a, p.L, TAG_EMBED);  // layer index L: no other write uses it
     consumer_sync();  // every warp's LM-head epilogue has updated amax_v / amax_i
+    const bool tk = topk_sampling(a);
     if (c.tid == 0 && !c.sm->abort && a.skip_publish != task) {
         if (more) {
             fence_proxy_async_global();
@@ -2394,8 +2505,26 @@ __device__ __forceinline__ void argmax_finish(Ctx& c, int cta) {
             ll_st2(p.amax + ((size_t)cta * p.maxB + b) * 2, c.sm->amax_v[b],
                    __int_as_float(c.sm->amax_i[b]), tag);
     }
+    if (tk && c.cw < a.B && c.lane < a.top_k && !c.sm->abort && a.skip_publish != task) {
+        // top-k sampling: this CTA's list of each row (each writer releases the step's
+        // K/V appends first, as thread 0 does above)
+        if (more) {
+            fence_proxy_async_global();
+            __threadfence();
+        }
+        const int b = c.cw;
+        ll_st2(p.cand + (((size_t)cta * p.maxB + b) * kMaxSampleTopK + c.lane) * 2, c.sm->tk_v[b][c.lane],
+               __int_as_float(c.sm->tk_i[b][c.lane]), tag);
+    }
     if (!more && cta != 0) return;
-    if (c.cw < a.B) {
+    if (tk && c.cw < a.B) {
+        const int b = c.cw;
+        const int tok = tk_draw(b, tag, task);
+        if (c.lane == 0) {
+            c.sm->tok[b] = tok;
+            if (cta == 0) a.next_tokens[(size_t)step * a.B + b] = tok;
+        }
+    } else if (c.cw < a.B) {
         const int b = c.cw;
         float bv = -INFINITY;
         int bi = 0x7fffffff;
@@ -2456,6 +2585,10 @@ __device__ __forceinline__ void argmax_finish(Ctx& c, int cta) {
             c.sm->amax_v[b] = -INFINITY;
             c.sm->amax_i[b] = 0x7fffffff;
         }
+    }
+    for (int i = c.tid; i < kMaxBatch * kMaxSampleTopK; i += kConsumerThreads) {
+        c.sm->tk_v[i / kMaxSampleTopK][i % kMaxSampleTopK] = -INFINITY;
+        c.sm->tk_i[i / kMaxSampleTopK][i % kMaxSampleTopK] = 0x7fffffff;
     }
     consumer_sync();
 }
@@ -2687,6 +2820,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     if (threadIdx.x < kMaxBatch) {
         sm->amax_v[threadIdx.x] = -INFINITY;
         sm->amax_i[threadIdx.x] = 0x7fffffff;
+    }
+    for (int i = threadIdx.x; i < kMaxBatch * kMaxSampleTopK; i += kThreads) {
+        sm->tk_v[i / kMaxSampleTopK][i % kMaxSampleTopK] = -INFINITY;
+        sm->tk_i[i / kMaxSampleTopK][i % kMaxSampleTopK] = 0x7fffffff;
     }
     __syncthreads();
 

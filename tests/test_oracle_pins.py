@@ -494,3 +494,51 @@ def test_sampled_token_is_the_argmax_of_the_scores():
         pos, row, seed = int(rng.integers(0, 1 << 20)), int(rng.integers(0, 8)), int(rng.integers(0, 1 << 62))
         sc = oracle.gumbel_scores(z, 0.9, seed, pos, row)
         assert oracle.sample_gumbel(z, 0.9, seed, pos, row) == int(np.argmax(sc))
+
+
+# ---------------------------------------------------------------- limited top-k sampling
+def test_topk_one_is_the_greedy_token():
+    """k = 1 leaves one candidate, the largest logit (lowest index among equal ones),
+    whatever the temperature and the draw."""
+    rng = np.random.default_rng(31)
+    for t in range(50):
+        z = rng.normal(size=300).astype(np.float32)
+        if t % 5 == 0:
+            z[rng.integers(0, 300, size=3)] = z.max()  # tied maxima
+        for T in (0.3, 1.0, 4.0):
+            assert oracle.sample_gumbel_topk(z, T, 1, t, 1000 + t, 2) == int(np.argmax(z))
+
+
+def test_topk_of_the_whole_vocabulary_is_the_unrestricted_draw():
+    rng = np.random.default_rng(32)
+    for t in range(50):
+        z = rng.normal(size=257).astype(np.float32)
+        for k in (0, 257, 300):
+            assert oracle.sample_gumbel_topk(z, 0.9, k, 5, t, 1) == oracle.sample_gumbel(z, 0.9, 5, t, 1)
+
+
+def test_topk_draws_stay_in_the_candidate_set():
+    """The drawn token has fewer than k tokens ahead of it (larger logit, or equal logit
+    and a lower index); ties at the boundary keep the lower indices."""
+    rng = np.random.default_rng(33)
+    for t in range(200):
+        z = np.round(rng.normal(size=64), 1).astype(np.float32)  # many equal logits
+        k = int(rng.integers(1, 20))
+        i = oracle.sample_gumbel_topk(z, 1.3, k, 77, t, 0)
+        ahead = int(np.sum((z > z[i]) | ((z == z[i]) & (np.arange(64) < i))))
+        assert ahead < k, (k, i, ahead)
+
+
+def test_topk_frequencies_are_the_renormalised_softmax():
+    """Over many counters, draws restricted to the top k follow softmax(z / T) over those
+    k tokens; the tied boundary token with the higher index is never drawn."""
+    z = np.array([0.5, 2.0, 1.0, 1.0, -1.0, 1.5], np.float32)  # order: 1, 5, 2, 3, 0, 4
+    k, T, n = 3, 0.8, 30000
+    counts = np.zeros(len(z))
+    for pos in range(n):
+        counts[oracle.sample_gumbel_topk(z, T, k, 19, pos, 4)] += 1
+    cand = [1, 5, 2]
+    p = np.zeros(len(z))
+    p[cand] = np.exp(z[cand] / T) / np.exp(z[cand] / T).sum()
+    assert counts[3] == 0 and counts[0] == 0 and counts[4] == 0
+    assert np.abs(counts / n - p).max() < 0.012, (counts / n, p)
