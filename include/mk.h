@@ -123,7 +123,10 @@ typedef struct mk_kv_pool {
     int64_t bytes;
 } mk_kv_pool;
 
-/* Creates a handle on `device`: checks the GPU (sm_103, cooperative launch),
+/* Creates a handle on `device`. Source: the interface sentence of the build's target
+ * (a model descriptor plus weight pointers) and "Cohere, Megakernel sunum sistemini acik
+ * kaynak yapti", section "Sinirlar acikca yazilmis" (one model, BF16 weights, batch
+ * 1..8). Checks the GPU (sm_103, cooperative launch),
  * copies the descriptor, records the weight pointers, uploads the RoPE table
  * (cos/sin computed on the host in double), and allocates the step scratch
  * (activations, attention partials, dependency counters, status word; the KV tensor
@@ -134,14 +137,20 @@ typedef struct mk_kv_pool {
 MK_API mk_status mk_create(const mk_model_desc *desc, const mk_weights *weights, int device,
                     mk_handle **out);
 
-/* Allocates the handle's paged KV pool of num_pages pages (one pool per handle; a
+/* Allocates the handle's paged KV pool of num_pages pages. Source: the paged KV cache
+ * of "Cohere, Megakernel sunum sistemini acik kaynak yapti", section "Sinirlar acikca
+ * yazilmis" (pages of 16 tokens here). One pool per handle; a
  * second call fails with MK_ERR_INVALID_ARG until mk_kv_free). The memory is not
  * initialised. Returns MK_ERR_OOM if the allocation fails. */
 MK_API mk_status mk_kv_alloc(mk_handle *h, int32_t num_pages, mk_kv_pool *out);
 MK_API mk_status mk_kv_free(mk_handle *h, mk_kv_pool *pool);
 
 /* One decode step for `batch` sequences (1 <= batch <= max_batch), enqueued on
- * `stream` as a single cooperative kernel launch.
+ * `stream` as a single cooperative kernel launch. Source: "Cohere, Megakernel sunum
+ * sistemini acik kaynak yapti", sections "Megakernel ne demek" (the whole decode pass in
+ * one persistent kernel) and "Sinirlar acikca yazilmis" (decode only, batch 1..8,
+ * continuous batching, ragged lengths, paged KV, sliding window); "Kog AI: standart
+ * GPU'larda 3,000 token/s", on LM-head sampling kept on the GPU.
  *   tokens[batch]       input token of each sequence (0 <= token < vocab)
  *   positions[batch]    tokens already cached = position of the input token
  *   page_table[batch][max_pages_per_seq]  entry i = page holding positions
@@ -182,7 +191,9 @@ MK_API mk_status mk_decode_steps(mk_handle *h, int32_t n_steps, const int32_t *t
                                  int32_t batch, int32_t *next_tokens, float *logits,
                                  void *stream);
 
-/* Waits for `stream`, then reads the device status word. Returns MK_OK or the
+/* Waits for `stream`, then reads the device status word. Source: the error-reporting
+ * half of the build's interface sentence (device-side failures latched, not faulted;
+ * the pages give no mechanism). Returns MK_OK or the
  * latched device error; *failing_task (may be NULL) receives the id of the task
  * that latched it (layer*16 + stage, or -1). */
 MK_API mk_status mk_status_sync(mk_handle *h, void *stream, int32_t *failing_task);
