@@ -123,10 +123,10 @@ typedef struct mk_kv_pool {
     int64_t bytes;
 } mk_kv_pool;
 
-/* Creates a handle on `device`. Source: the interface sentence of the build's target
- * (a model descriptor plus weight pointers) and "Cohere, Megakernel sunum sistemini acik
- * kaynak yapti", section "Sinirlar acikca yazilmis" (one model, BF16 weights, batch
- * 1..8). Checks the GPU (sm_103, cooperative launch),
+/* Creates a handle on `device` for one model (a descriptor plus borrowed weight
+ * pointers). Source: "Cohere, Megakernel sunum sistemini acik kaynak yapti", section
+ * "Sinirlar acikca yazilmis" (one model, BF16 weights, batch 1..8). Checks the GPU
+ * (sm_103, cooperative launch),
  * copies the descriptor, records the weight pointers, uploads the RoPE table
  * (cos/sin computed on the host in double), and allocates the step scratch
  * (activations, attention partials, dependency counters, status word; the KV tensor
@@ -191,9 +191,9 @@ MK_API mk_status mk_decode_steps(mk_handle *h, int32_t n_steps, const int32_t *t
                                  int32_t batch, int32_t *next_tokens, float *logits,
                                  void *stream);
 
-/* Waits for `stream`, then reads the device status word. Source: the error-reporting
- * half of the build's interface sentence (device-side failures latched, not faulted;
- * the pages give no mechanism). Returns MK_OK or the
+/* Waits for `stream`, then reads the device status word (the pages describe no error
+ * mechanism; here device-side failures are latched and the kernel winds down instead of
+ * faulting). Returns MK_OK or the
  * latched device error; *failing_task (may be NULL) receives the id of the task
  * that latched it (layer*16 + stage, or -1). */
 MK_API mk_status mk_status_sync(mk_handle *h, void *stream, int32_t *failing_task);
