@@ -388,7 +388,7 @@ def e2e_loop(S, cfg, steps, warmup):
 
 
 # ------------------------------------------------------------------ the other model configs
-def other_config(mk, local, name, B, ctx, steps, warmup, prefix_pages=0, private_pages=0):
+def other_config(mk, local, name, B, ctx, steps, warmup, prefix_pages=0, private_pages=0, layers=0):
     """One more decode workload on its own seeded weights: B rows at context ~ctx (or
     rows sharing a page-aligned prefix run), greedy tokens fed back on device. Returns
     tokens/s, per-step time, and the achieved GB/s over the algorithmic bytes (a MoE
@@ -396,6 +396,8 @@ def other_config(mk, local, name, B, ctx, steps, warmup, prefix_pages=0, private
     import torch
     import synth
     cfg = synth.CONFIGS[name]
+    if layers:  # profiling only: the same shapes with fewer layers
+        cfg = cfg.with_(name=f"{name}-{layers}l", n_layers=layers)
     dev = f"cuda:{local}"
     seed = {"moe-64x768": 3, "dense-8b": 4 if not prefix_pages else 5}[name]
     W = synth.make_weights(cfg, seed, device=dev)
@@ -578,7 +580,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the MoE and 8B lines")
     ap.add_argument("--layers", type=int, default=0,
-                    help="profiling only: run the 2B shapes with this many layers")
+                    help="profiling only: run every workload's shapes with this many layers")
+    ap.add_argument("--only", default="", choices=["", "moe_b1", "moe_b8", "dense8b_b1", "dense8b_b4_prefix"],
+                    help="profiling only: run just this one of the other workloads (no headline line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -597,6 +601,16 @@ def main():
     mkbuild.build()
     import persistent_megakernel_05_b300 as mk
     torch.cuda.set_device(local)
+    extra_kw = {"moe_b1": dict(name="moe-64x768", B=1, ctx=4096, steps=128),
+                "moe_b8": dict(name="moe-64x768", B=8, ctx=4096, steps=128),
+                "dense8b_b1": dict(name="dense-8b", B=1, ctx=32768, steps=128),
+                "dense8b_b4_prefix": dict(name="dense-8b", B=4, ctx=0, steps=128,
+                                          prefix_pages=1024, private_pages=64)}
+    if args.only:  # profiling only: one of the other workloads, --steps timed steps
+        kw = dict(extra_kw[args.only], steps=args.steps)
+        r = other_config(mk, local, warmup=args.warmup, layers=args.layers, **kw)
+        emit({"only": args.only, "layers": args.layers or None, **r}, rank)
+        return
     cfg = synth.DENSE_2B
     if args.layers:
         cfg = cfg.with_(name=f"dense-2b-{args.layers}l", n_layers=args.layers)
@@ -686,12 +700,8 @@ def main():
         S["model"].close()
         torch.cuda.empty_cache()
         extra = {}
-        for key, kw in (("moe_b1", dict(name="moe-64x768", B=1, ctx=4096, steps=128)),
-                        ("moe_b8", dict(name="moe-64x768", B=8, ctx=4096, steps=128)),
-                        ("dense8b_b1", dict(name="dense-8b", B=1, ctx=32768, steps=128)),
-                        ("dense8b_b4_prefix", dict(name="dense-8b", B=4, ctx=0, steps=128,
-                                                   prefix_pages=1024, private_pages=64))):
-            extra[key] = other_config(mk, local, warmup=args.warmup, **kw)
+        for key, kw in extra_kw.items():
+            extra[key] = other_config(mk, local, warmup=args.warmup, layers=args.layers, **kw)
             extra[key]["frac_of_measured_peak"] = round(extra[key]["hbm_gbs"] / peak, 4)
         out["other_configs"] = extra
         W = synth.make_weights(cfg, 1, device=f"cuda:{local}")
