@@ -8,8 +8,9 @@ Checked here, on two consecutive calls each (the second one finds the array hold
 first call's contents): the result matches the CPU oracle at the parity bar (logits,
 tokens where the oracle's margin is clear, K/V appends at the oracle's addresses and
 within 1 BF16 ulp), at batch 1 and 3 (tagged-word hand-off, which relies on the
-per-call clearing of the array) and batch 8 (counters); and it matches the handle-based
-mk_decode_step on the same inputs.
+per-call clearing of the array) and batch 8 (counters), for a small dense model, a small
+MoE and the 2B shapes cut to two layers; and it matches the handle-based mk_decode_step on
+the same inputs.
 
 This file is collected last on purpose: if it fails, a run that stops at the first
 failure has already run every other test.
@@ -79,16 +80,27 @@ class _NoAllocPair:
         self.model.close()
 
 
-@pytest.mark.parametrize("B", [1, 3, 8])
-def test_noalloc_matches_the_oracle_on_two_consecutive_calls(B):
+# a small MoE (8 experts of width 128, top-2) and the 2B shapes cut to two layers, with
+# max_batch 2 and 1,024 positions so that their scratch fits the static array
+_TINY_MOE = synth.ModelConfig("tiny-moe", n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=2,
+                              head_dim=64, ffn_dim=0, vocab=4096, n_experts=8, top_k=2,
+                              expert_ffn_dim=128, max_positions=512)
+_DENSE_2B_SMALL = synth.DENSE_2B.with_(n_layers=2, max_batch=2, max_positions=1024)
+_CASES = [(synth.TINY, 1), (synth.TINY, 3), (synth.TINY, 8), (_TINY_MOE, 1), (_TINY_MOE, 3),
+          (_DENSE_2B_SMALL, 1), (_DENSE_2B_SMALL, 2)]
+
+
+@pytest.mark.parametrize("cfg,B", _CASES, ids=[f"{c.name}-B{b}" for c, b in _CASES])
+def test_noalloc_matches_the_oracle_on_two_consecutive_calls(cfg, B):
     from persistent_megakernel_05_b300 import build
     build.build()
-    cfg = synth.TINY
-    npages = 64
-    pair = _NoAllocPair(cfg, seed=21 + B, num_pages=npages, kv_seed=4)
     rng = np.random.default_rng(21 + B)
     pos = np.array([3, 15, 16, 40, 77, 100, 129, 200], np.int32)[:B]
+    if cfg.d_model > 256:
+        pos = pos + 700  # 45+ pages per row: the attention runs split over several CTAs
     pages = [int(p) // 16 + 2 for p in pos]
+    npages = max(64, sum(pages) + 4)
+    pair = _NoAllocPair(cfg, seed=21 + B, num_pages=npages, kv_seed=4)
     pt = synth.random_page_tables(rng, npages, pages, max(pages))
     toks = synth.random_tokens(rng, cfg.vocab, B)
     for call in range(2):
