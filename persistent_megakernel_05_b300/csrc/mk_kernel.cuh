@@ -102,7 +102,8 @@ enum ProfSection { PS_OTHER = 0, PS_G_DATA = 1, PS_G_SLOTS = 2, PS_G_EPI = 3, PS
                    PS_A_POST = 30, PS_A_FINISH = 31, PS_M_ML = 32, PS_M_W = 33, PS_M_O = 34,
                    PS_A_END = 35, PS_EMBED = 36, PS_ARGMAX = 37, PS_A_LWAIT = 38, PS_G_SWAIT = 39,
                    PS_MOE_ROUTE = 40, PS_L_ISSUE = 41, PS_L_BLOCK = 42, PS_L_DEP = 43,
-                   PS_L_SLOTS = 44, PS_L_NBLOCK = 45, PS_T_RET = 46, PS_T_CALL = 47, PS_TOTAL = 63 };
+                   PS_L_SLOTS = 44, PS_L_NBLOCK = 45, PS_T_RET = 46, PS_T_CALL = 47,
+                   PS_TOTAL_NS = 62, PS_TOTAL = 63 };
 // loader sections (lane 0 of the loader; MK_PROF builds): cycles issuing, cycles waiting
 // for a free ring slot, cycles waiting on a routing / step dependency, slots issued,
 // slots that found the ring full
@@ -583,29 +584,18 @@ __device__ __forceinline__ size_t chunk_base(const GemvStage& s, int k0) {
     return (size_t)k0;
 }
 
-// Shared-memory geometry of one weight slot (8 rows x kc columns of k-chunk k0).
-// When a chunk is a whole weight row, rpc consecutive rows travel in one contiguous copy
-// of up to 8 KB; otherwise each row segment is its own copy. Copies are
-// 16 B apart so that 8 rows read by ldmatrix fall into distinct (or at most 2-way
-// shared) bank groups.
+// Shared-memory geometry of one weight slot (8 rows x kc columns of k-chunk k0). Each
+// row segment travels in its own copy; rows are kc * 2 + 16 bytes apart, so the 8 rows
+// that one ldmatrix reads at the same column start in 8 different 16-byte bank groups
+// (kc is a multiple of 64, so the pitch is 16 modulo 128).
 struct SlotGeom {
-    int kc, rpc, rpc_log2, cpitch, rowb;  // rowb = kc * 2 (bytes of one row segment)
-    __device__ __forceinline__ int row_off(int r) const {
-        return (r >> rpc_log2) * cpitch + (r & (rpc - 1)) * rowb;
-    }
+    int kc, pitch;
+    __device__ __forceinline__ int row_off(int r) const { return r * pitch; }
 };
 __device__ __forceinline__ SlotGeom slot_geom(const GemvStage& s, int k0) {
     SlotGeom g;
     g.kc = min(s.kcw, s.K - k0);
-    int lg = 0;
-    if (g.kc == s.ldw) {
-        const int r = 4096 / g.kc;
-        lg = r >= 8 ? 3 : r >= 4 ? 2 : r >= 2 ? 1 : 0;
-    }
-    g.rpc_log2 = lg;
-    g.rpc = 1 << lg;
-    g.rowb = g.kc * 2;
-    g.cpitch = g.rpc * g.rowb + 16;
+    g.pitch = g.kc * 2 + 16;
     return g;
 }
 
@@ -920,7 +910,6 @@ struct Producer {
                 for (int gi = 0; gi < ng; ++gi) {
                     if (!acquire_slot(s.task_id)) return false;
                     const int nr = group_rows(s, n, gi, ngate);
-                    const int ncop = (nr + geo.rpc - 1) >> geo.rpc_log2;
                     const uint32_t dst = slot_addr(), bar = full_bar();
                     if (lane == 0 && !pf) mbar_arrive_expect_tx(bar, (uint32_t)(nr * geo.kc * 2));
                     __syncwarp();
@@ -933,22 +922,12 @@ struct Producer {
                             for (int j = k0 / s.Fe + (lane & 3); j * s.Fe < k0 + geo.kc; j += 4) {
                                 const int c0 = max(k0, j * s.Fe), c1 = min(k0 + geo.kc, (j + 1) * s.Fe);
                                 const bf16* src = s.w0 + ((size_t)s.uni[j] * s.R + r) * s.Fe + (c0 - j * s.Fe);
-                                copy(dst + i * geo.cpitch + (c0 - k0) * 2, src, (uint32_t)((c1 - c0) * 2), bar);
+                                copy(dst + i * geo.pitch + (c0 - k0) * 2, src, (uint32_t)((c1 - c0) * 2), bar);
                             }
                         }
-                    } else if (lane < ncop) {
-                        const int i0 = lane * geo.rpc;
-                        const int cnt = min(geo.rpc, nr - i0);
-                        const bf16* p0 = gemv_row(s, r0, gi, ngate, i0) + cb;
-                        const bf16* p1 = gemv_row(s, r0, gi, ngate, i0 + cnt - 1) + cb;
-                        const uint32_t d0 = dst + lane * geo.cpitch;
-                        if (p1 == p0 + (size_t)(cnt - 1) * s.ldw) {
-                            copy(d0, p0, (uint32_t)(cnt * geo.kc * 2), bar);
-                        } else {  // the rows straddle two weight tensors (q|k|v)
-                            for (int i = 0; i < cnt; ++i)
-                                copy(d0 + i * geo.kc * 2, gemv_row(s, r0, gi, ngate, i0 + i) + cb,
-                                     (uint32_t)(geo.kc * 2), bar);
-                        }
+                    } else if (lane < nr) {
+                        copy(dst + lane * geo.pitch, gemv_row(s, r0, gi, ngate, lane) + cb,
+                             (uint32_t)(geo.kc * 2), bar);
                     }
                     if (trace_slots(s) && !pf) MK_TRACE_P(*this, TR_S_ISSUE, seq);
                     ++seq;
@@ -2710,6 +2689,7 @@ __device__ __forceinline__ void consumer_run(Ctx& c, int cta) {
     if (c.tid < 64) c.sm->prof[c.tid] = 0;
     consumer_sync();
     const long long t_start = clock64();
+    const uint64_t ns_start = globaltimer();  // with the cycle count: the SM clock of the run
     if (c.tid == 0) c.sm->prof_pt = t_start;
 #endif
     const int nsteps = MULTI ? c.a->n_steps : 1;
@@ -2742,7 +2722,10 @@ __device__ __forceinline__ void consumer_run(Ctx& c, int cta) {
         if (c.sm->abort) break;
     }
 #ifdef MK_PROF
-    if (c.tid == 0) c.sm->prof[PS_TOTAL] += clock64() - t_start;
+    if (c.tid == 0) {
+        c.sm->prof[PS_TOTAL] += clock64() - t_start;
+        c.sm->prof[PS_TOTAL_NS] += globaltimer() - ns_start;
+    }
     consumer_sync();
     if (c.tid < 64 && cta < kProfCtas) g_mk_prof[cta][c.tid] += c.sm->prof[c.tid];
 #endif
