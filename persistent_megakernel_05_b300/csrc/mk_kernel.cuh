@@ -46,12 +46,12 @@ __device__ __forceinline__ bool idle_warp(int w) { return w == 4 || w == 8; }
 __device__ __forceinline__ int consumer_index(int w) { return w - 1 - (w > 4) - (w > 8); }
 constexpr int kDefaultPrefetchSlots = 0;          // L2 prefetch lead (slots); 0 = off
 
-// Shared-memory ring depth. Four 33 KB slots keep HBM streaming (132 KB in flight per
-// SM) and leave ~90 KB of the SM's unified L1/shared array to L1: the consumers' saved
-// registers at calls and the norm-gain reads then hit L1 instead of waiting on L2.
-// Measured at 2B batch 1: 6 slots 1.107, 5 slots 1.106, 4 slots 1.070, 3 slots 1.135
-// ms/step (alternating runs on one box).
-constexpr int kStages = 4;
+// Shared-memory ring depth. Five 33 KB slots (165 KB in flight per SM) with the scratch
+// and the shared state fit the 196 KB carveout, which leaves ~60 KB of the SM's unified
+// L1/shared array to L1 for the consumers' saved registers and the norm-gain reads.
+// Measured (alternating runs on one box), ms/step: 2B batch 1: 4 slots 1.033, 5 slots
+// 1.019, 6 slots 1.095; 2B batch 8: 2.667, 2.582, 2.602; MoE batch 1: 1.228, 1.225, 1.267.
+constexpr int kStages = 5;
 constexpr int KCW = 2048;                          // GEMV k-chunk: columns of a weight slot
 constexpr int kGroupRows = 8;                      // weight rows per ring slot
 constexpr int kSlotBytes = 33 * 1024;              // >= 8 * (2 * KCW + 16), multiple of 1024
@@ -275,9 +275,9 @@ struct Smem {
 
 constexpr int kSmemBytes = 1024 + kStages * kSlotBytes + kScratchBytes + (int)sizeof(Smem);
 // The SM's unified L1 / shared array is split in fixed carveouts; staying within the
-// 164 KB one (with the 1 KB the runtime reserves per block) leaves ~90 KB to L1, which
+// 196 KB one (with the 1 KB the runtime reserves per block) leaves ~60 KB to L1, which
 // the consumers' saved registers and gain reads depend on.
-static_assert(kSmemBytes + 1024 <= 164 * 1024, "shared memory beyond the 164 KB carveout shrinks L1");
+static_assert(kSmemBytes + 1024 <= 196 * 1024, "shared memory beyond the 196 KB carveout shrinks L1");
 
 struct Ctx {
     const StepArgs* a;
