@@ -2581,13 +2581,15 @@ __device__ __noinline__ void moe_route(int l) {
     Ctx c = make_ctx(0);
     const StepArgs& a = *c.a;
     const Plan& p = a.p;
-    const int E = p.E, task = l * 16 + ST_ROUTE;
-    float* sel = c.scratch;  // [B][64]: routing weight by expert id, -1 = not routed
-    // Every warp routes a row (warp w takes row w mod B; only the first B warps write).
-    // A lone routing warp next to warps parked at a CTA barrier ran ~8x slower.
-    if (!c.sm->abort) {
-        const int b = c.cw % a.B;
-        const bool writer = c.cw < a.B;
+    const int E = p.E, B = a.B, task = l * 16 + ST_ROUTE;
+    float* sel = c.scratch;  // [B][64]: routing weight by expert id, -1 = not routed (B > 1)
+    // Warp b routes row b; the other warps go straight to the barrier. (Routing the rows
+    // redundantly on every warp tripled the issue load of the three schedulers the
+    // consumers share: MoE batch 1 took 1.228 ms per step that way, 1.126 ms this way.)
+    // The code is kept compact (loops not unrolled): it runs once per layer, so its
+    // instructions are fetched cold each time.
+    if (!c.sm->abort && c.cw < B) {
+        const int b = c.cw;
         const uint32_t tag = tag_of(a, l, TAG_ROUTE);
         const uint64_t* row = p.route + (size_t)b * E;
         float v0 = -INFINITY, v1 = -INFINITY;
@@ -2613,7 +2615,6 @@ __device__ __noinline__ void moe_route(int l) {
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         p0 /= z;
         p1 /= z;
-        // (a shuffle-chain selection ran several times slower here than standalone)
         float* pw = c.scratch + 8 * 64 + c.cw * 64;             // this warp's p, by expert
         int* ids = reinterpret_cast<int*>(c.scratch + 16 * 64) + c.cw * kMaxTopK;
         // Top-k by rank: an expert's rank is the number of experts ahead of it (larger p,
@@ -2623,11 +2624,15 @@ __device__ __noinline__ void moe_route(int l) {
         pw[c.lane + 32] = c.lane + 32 < E ? p1 : -1.f;
         __syncwarp();
         int r0 = 0, r1 = 0;
-#pragma unroll 8
-        for (int e = 0; e < E; ++e) {
-            const float v = pw[e];
-            r0 += (v > p0 || (v == p0 && e < c.lane)) ? 1 : 0;
-            r1 += (v > p1 || (v == p1 && e < c.lane + 32)) ? 1 : 0;
+#pragma unroll 1
+        for (int e = 0; e < E; e += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(pw + e);
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                r0 += (vv[q] > p0 || (vv[q] == p0 && e + q < c.lane)) ? 1 : 0;
+                r1 += (vv[q] > p1 || (vv[q] == p1 && e + q < c.lane + 32)) ? 1 : 0;
+            }
         }
         const int topk = p.topk;
         const bool t0 = c.lane < E && r0 < topk, t1 = c.lane + 32 < E && r1 < topk;
@@ -2635,35 +2640,51 @@ __device__ __noinline__ void moe_route(int l) {
         if (t1) ids[r1] = c.lane + 32;
         __syncwarp();
         float picked = 0.f;
+#pragma unroll 1
         for (int r = 0; r < topk; ++r) picked += pw[ids[r]];
-        if (writer) {
-            sel[b * 64 + c.lane] = (c.lane < E && t0) ? p0 / picked : -1.f;
-            sel[b * 64 + c.lane + 32] = (c.lane + 32 < E && t1) ? p1 / picked : -1.f;
+        const float w0 = t0 ? p0 / picked : -1.f, w1 = t1 ? p1 / picked : -1.f;
+        if (B == 1) {  // the union is this row's route, in ascending expert id
+            const uint32_t m0 = __ballot_sync(0xffffffffu, t0), m1 = __ballot_sync(0xffffffffu, t1);
+            const uint32_t below = (1u << c.lane) - 1u;
+            const int s0 = __popc(m0 & below), s1 = __popc(m0) + __popc(m1 & below);
+            if (t0) { c.sm->moe_uni[s0] = c.lane; c.sm->moe_w[0][s0] = w0; }
+            if (t1) { c.sm->moe_uni[s1] = c.lane + 32; c.sm->moe_w[0][s1] = w1; }
+            if (c.lane == 0) {
+                c.sm->moe_nu = __popc(m0) + __popc(m1);
+                if (blockIdx.x == 0) p.moe_union[l] = __popc(m0) + __popc(m1);
+            }
+        } else {
+            sel[b * 64 + c.lane] = w0;
+            sel[b * 64 + c.lane + 32] = w1;
         }
     }
     consumer_sync();
-    if (c.cw == 0) {
-        // union over the rows, ascending expert id: slot = rank among the routed ids
-        bool in0 = false, in1 = false;
-        for (int b = 0; b < a.B; ++b) {
-            in0 = in0 || sel[b * 64 + c.lane] >= 0.f;
-            in1 = in1 || sel[b * 64 + c.lane + 32] >= 0.f;
+    if (B > 1) {
+        if (c.cw == 0) {
+            // union over the rows, ascending expert id: slot = rank among the routed ids
+            bool in0 = false, in1 = false;
+#pragma unroll 1
+            for (int b = 0; b < B; ++b) {
+                in0 = in0 || sel[b * 64 + c.lane] >= 0.f;
+                in1 = in1 || sel[b * 64 + c.lane + 32] >= 0.f;
+            }
+            const uint32_t m0 = __ballot_sync(0xffffffffu, in0), m1 = __ballot_sync(0xffffffffu, in1);
+            const uint32_t below = (1u << c.lane) - 1u;
+            const int s0 = __popc(m0 & below), s1 = __popc(m0) + __popc(m1 & below);
+            if (in0) c.sm->moe_uni[s0] = c.lane;
+            if (in1) c.sm->moe_uni[s1] = c.lane + 32;
+#pragma unroll 1
+            for (int b = 0; b < B; ++b) {  // (rows b >= B are never read)
+                if (in0) c.sm->moe_w[b][s0] = fmaxf(sel[b * 64 + c.lane], 0.f);
+                if (in1) c.sm->moe_w[b][s1] = fmaxf(sel[b * 64 + c.lane + 32], 0.f);
+            }
+            if (c.lane == 0) {
+                c.sm->moe_nu = __popc(m0) + __popc(m1);
+                if (blockIdx.x == 0) p.moe_union[l] = __popc(m0) + __popc(m1);
+            }
         }
-        const uint32_t m0 = __ballot_sync(0xffffffffu, in0), m1 = __ballot_sync(0xffffffffu, in1);
-        const uint32_t below = (1u << c.lane) - 1u;
-        const int s0 = __popc(m0 & below), s1 = __popc(m0) + __popc(m1 & below);
-        if (in0) c.sm->moe_uni[s0] = c.lane;
-        if (in1) c.sm->moe_uni[s1] = c.lane + 32;
-        for (int b = 0; b < kMaxBatch; ++b) {
-            if (in0) c.sm->moe_w[b][s0] = b < a.B ? fmaxf(sel[b * 64 + c.lane], 0.f) : 0.f;
-            if (in1) c.sm->moe_w[b][s1] = b < a.B ? fmaxf(sel[b * 64 + c.lane + 32], 0.f) : 0.f;
-        }
-        if (c.lane == 0) {
-            c.sm->moe_nu = __popc(m0) + __popc(m1);
-            if (blockIdx.x == 0) p.moe_union[l] = __popc(m0) + __popc(m1);
-        }
+        consumer_sync();
     }
-    consumer_sync();
     MK_PROF_MARK(c, PS_MOE_ROUTE);
     if (l == 1) MK_TRACE_C(c, TR_R_DONE, 0);
     if (c.tid == 0) {
