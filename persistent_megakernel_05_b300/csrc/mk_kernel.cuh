@@ -2092,8 +2092,12 @@ __device__ __noinline__ void attention_merge(int l, int b, int g, int split, int
     if (l == 0 || l == 1) MK_TRACE_C(c, TR_A_MERGED, 0);
 }
 
-template <int HD, bool MULTI>
+// PK (one row, G <= 4): the B columns are n = 2 h + part, the BF16 hi (part 0) and lo
+// (part 1) halves of head h's q (and P) side by side, so one MMA covers both halves where
+// the general path issues one per half; each lane then owns one head (t) instead of two.
+template <int HD, bool MULTI, bool PK>
 __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) {
+    static_assert(!(MULTI && PK), "packed columns hold one row's heads");
     Ctx c = make_ctx(seq);
     const SeqSpan sp = pc.sp;
     const int b = pc.b, g = pc.g, u = pc.u, n = pc.n;
@@ -2189,7 +2193,7 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
     if (l == 1) MK_TRACE_C(c, TR_Q_SYNCED, 0);
     // q^T (after RoPE) as the B operand: column gq of this warp's tile, k = head dims;
     // hi/lo split. b0b1 of k-step s holds dims 16s + 2t, +1; b2b3 holds 16s + 8 + 2t, +1.
-    const int qcol = tile * 8 + gq;
+    const int qcol = PK ? (gq >> 1) : tile * 8 + gq;
     const float2* rq = MULTI ? rs + (qcol < NC ? qcol / G : 0) * (HD / 2) : rs;
     uint32_t qa[NKS][2], ql[NKS][2];
 #pragma unroll
@@ -2212,6 +2216,7 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
                 }
             }
             split_bf16x2(v0, v1, qa[s][hh], ql[s][hh]);
+            if (PK && (gq & 1)) qa[s][hh] = ql[s][hh];  // column 2 h + 1: the lo half
         }
     // the new token's K (after RoPE) and V, rounded to BF16 (warp 0 also splices them)
     if (has_last && c.cw == 0) {
@@ -2281,7 +2286,7 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
                     __syncwarp();
                 }
                 // S^T = K q^T for both pages: A = K rows (keys) via ldmatrix, B = q^T; four
-                // accumulator chains (page A / B x hi / lo)
+                // accumulator chains (page A / B x hi / lo; PK: page A / B x even / odd k-step)
                 float shA[4] = {0.f, 0.f, 0.f, 0.f}, slA[4] = {0.f, 0.f, 0.f, 0.f};
                 float shB[4] = {0.f, 0.f, 0.f, 0.f}, slB[4] = {0.f, 0.f, 0.f, 0.f};
                 {
@@ -2293,15 +2298,60 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
                         uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
                         ldmatrix_x4(kbA + off, a0, a1, a2, a3);
                         ldmatrix_x4(kbB + off, b0, b1, b2, b3);  // (page B may be past the piece: masked)
-                        mma_16816(shA, a0, a1, a2, a3, qa[s][0], qa[s][1]);
-                        mma_16816(shB, b0, b1, b2, b3, qa[s][0], qa[s][1]);
-                        mma_16816(slA, a0, a1, a2, a3, ql[s][0], ql[s][1]);
-                        mma_16816(slB, b0, b1, b2, b3, ql[s][0], ql[s][1]);
+                        if (PK) {
+                            mma_16816(s & 1 ? slA : shA, a0, a1, a2, a3, qa[s][0], qa[s][1]);
+                            mma_16816(s & 1 ? slB : shB, b0, b1, b2, b3, qa[s][0], qa[s][1]);
+                        } else {
+                            mma_16816(shA, a0, a1, a2, a3, qa[s][0], qa[s][1]);
+                            mma_16816(shB, b0, b1, b2, b3, qa[s][0], qa[s][1]);
+                            mma_16816(slA, a0, a1, a2, a3, ql[s][0], ql[s][1]);
+                            mma_16816(slB, b0, b1, b2, b3, ql[s][0], ql[s][1]);
+                        }
                     }
                 }
                 // scores of keys A+g, A+g+8, B+g, B+g+8 (index 4 * page + 2 * (g + 8) + head)
                 auto valid = [&](int key) { return key >= lo && key <= pos; };
                 const bool okB = hasB;
+                uint32_t ph[2][2], pl[2][2];  // [page][b0b1 | b2b3]
+                if (PK) {
+                    // this lane's head t: D columns 2t (hi) and 2t + 1 (lo), both k-step chains
+                    float sc[4];
+                    sc[0] = valid(keyA + gq) ? ((shA[0] + slA[0]) + (shA[1] + slA[1])) * p.scale : -INFINITY;
+                    sc[1] = valid(keyA + gq + 8) ? ((shA[2] + slA[2]) + (shA[3] + slA[3])) * p.scale : -INFINITY;
+                    sc[2] = okB && valid(keyB + gq) ? ((shB[0] + slB[0]) + (shB[1] + slB[1])) * p.scale : -INFINITY;
+                    sc[3] = okB && valid(keyB + gq + 8) ? ((shB[2] + slB[2]) + (shB[3] + slB[3])) * p.scale : -INFINITY;
+                    float mb = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+                    const float m_new = fmaxf(m_run[0], mb);
+                    float corr = 1.f, pv[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (m_new != -INFINITY) {
+                        corr = expf(m_run[0] - m_new);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) pv[k] = expf(sc[k] - m_new);
+                    }
+                    m_run[0] = m_new;
+                    l_run[0] = l_run[0] * corr + ((pv[0] + pv[1]) + (pv[2] + pv[3]));
+#pragma unroll
+                    for (int mt = 0; mt < NMT; ++mt) {
+                        oacc[mt][0] *= corr; oacc[mt][1] *= corr; oacc[mt][2] *= corr; oacc[mt][3] *= corr;
+                    }
+                    // P^T as the B operand: column gq = (head gq / 2, half gq % 2)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) pbuf[(gq + 8 * k) * 5 + t] = pv[k];
+                    __syncwarp();
+                    const int hq = gq >> 1;
+#pragma unroll
+                    for (int pg = 0; pg < 2; ++pg) {
+                        uint32_t h0, l0, h1, l1;
+                        split_bf16x2(pbuf[(16 * pg + 2 * t) * 5 + hq], pbuf[(16 * pg + 2 * t + 1) * 5 + hq], h0, l0);
+                        split_bf16x2(pbuf[(16 * pg + 2 * t + 8) * 5 + hq], pbuf[(16 * pg + 2 * t + 9) * 5 + hq], h1, l1);
+                        ph[pg][0] = (gq & 1) ? l0 : h0;
+                        ph[pg][1] = (gq & 1) ? l1 : h1;
+                    }
+                    __syncwarp();
+                } else {
                 float sc[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -2337,13 +2387,13 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
                     pbuf[key * 9 + 2 * t + 1] = pv[2 * k + 1];
                 }
                 __syncwarp();
-                uint32_t ph[2][2], pl[2][2];  // [page][b0b1 | b2b3]
 #pragma unroll
                 for (int pg = 0; pg < 2; ++pg) {
                     split_bf16x2(pbuf[(16 * pg + 2 * t) * 9 + gq], pbuf[(16 * pg + 2 * t + 1) * 9 + gq], ph[pg][0], pl[pg][0]);
                     split_bf16x2(pbuf[(16 * pg + 2 * t + 8) * 9 + gq], pbuf[(16 * pg + 2 * t + 9) * 9 + gq], ph[pg][1], pl[pg][1]);
                 }
                 __syncwarp();
+                }
                 // keys 2t, 2t+1 / 2t+8, 2t+9 of each page's V^T: zero the invalid ones
                 auto vmask = [&](int k0) {
                     return (valid(k0) ? 0x0000ffffu : 0u) | (valid(k0 + 1) ? 0xffff0000u : 0u);
@@ -2362,9 +2412,9 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
                     a0 &= mloA; a1 &= mloA; a2 &= mhiA; a3 &= mhiA;
                     b0 &= mloB; b1 &= mloB; b2 &= mhiB; b3 &= mhiB;
                     mma_16816(oacc[mt], a0, a1, a2, a3, ph[0][0], ph[0][1]);
-                    mma_16816(oacc[mt], a0, a1, a2, a3, pl[0][0], pl[0][1]);
+                    if (!PK) mma_16816(oacc[mt], a0, a1, a2, a3, pl[0][0], pl[0][1]);
                     mma_16816(oacc[mt], b0, b1, b2, b3, ph[1][0], ph[1][1]);
-                    mma_16816(oacc[mt], b0, b1, b2, b3, pl[1][0], pl[1][1]);
+                    if (!PK) mma_16816(oacc[mt], b0, b1, b2, b3, pl[1][0], pl[1][1]);
                 }
             }
             release_at(c, c.seq + j);
@@ -2390,6 +2440,16 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
     const int ncl = MULTI ? min(8, NC) : 1;  // one pass for one row (G columns <= kFC)
     for (int ch0 = 0; ch0 < ncl; ch0 += kFC) {
         consumer_sync();  // the key loop's P buffers / the previous pass are done with it
+        if (PK) {  // head t: the hi and lo columns of its D summed
+            if (t < G) {
+                if (gq == 0) { ws_m[c.cw * 8 + t] = m_run[0]; ws_l[c.cw * 8 + t] = l_run[0]; }
+#pragma unroll
+                for (int mt = 0; mt < NMT; ++mt) {
+                    ws_o[(c.cw * kFC + t) * OS + 16 * mt + gq] = oacc[mt][0] + oacc[mt][1];
+                    ws_o[(c.cw * kFC + t) * OS + 16 * mt + gq + 8] = oacc[mt][2] + oacc[mt][3];
+                }
+            }
+        } else {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int h = 2 * t + hh;
@@ -2401,6 +2461,7 @@ __device__ __noinline__ uint32_t attention_piece(uint32_t seq, int l, Piece pc) 
                     ws_o[(c.cw * kFC + h - ch0) * OS + 16 * mt + gq + 8] = oacc[mt][2 + hh];
                 }
             }
+        }
         }
         MK_PROF_MARK(c, PS_A_POST);
         attention_finish<HD, MULTI>(l, pc, ch0, NC, wpt);
@@ -2418,8 +2479,9 @@ __device__ __noinline__ uint32_t attention_stage(uint32_t seq, int l, int cta) {
     // every piece first writes its partial record; then each split merges its slice
     auto piece = [&](const Piece& pc) {
         MK_TRACE_C(c, TR_PIECE, (uint32_t)(pc.b * 256 + pc.g));
-        if (pc.prefix) c.seq = attention_piece<HD, true>(c.seq, l, pc);
-        else c.seq = attention_piece<HD, false>(c.seq, l, pc);
+        if (pc.prefix) c.seq = attention_piece<HD, true, false>(c.seq, l, pc);
+        else if (c.a->p.G <= 4) c.seq = attention_piece<HD, false, true>(c.seq, l, pc);
+        else c.seq = attention_piece<HD, false, false>(c.seq, l, pc);
     };
     auto merge = [&](const Piece& pc) {
         if (pc.prefix) return;  // a shared prefix's records are merged by each row's own CTAs
