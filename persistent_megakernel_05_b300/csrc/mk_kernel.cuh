@@ -67,6 +67,8 @@ constexpr int kCounterStride = 32;                 // u32 words per counter (128
 constexpr int kStagesPerLayer = 8;                 // counter slots per layer
 constexpr int kMaxOwnRows = 32;                    // residual rows a CTA owns: ceil(d / CTAs) <= 32
 constexpr int kMaxSplitsG = 1184;                  // splits (<= CTAs) x G (<= 8): merge staging
+constexpr int kPieceCache = 4;                     // attention pieces a CTA caches per layer class
+constexpr int kPieceWords = 16;                    // 32-bit words of one cached piece (>= sizeof(Piece) / 4)
 
 // ---- optional timeline trace (compile with -DMK_TRACE; no code otherwise) ----
 #ifdef MK_TRACE
@@ -255,6 +257,11 @@ struct Smem {
     StepArgs args;
     __align__(16) LayerPlan lp[2];  // consumers' copies of the plans of layers l (l & 1) and l + 1
     __align__(16) LayerPlan lpl[2]; // the loader's copies (it runs ahead of the consumers)
+    // the consumers' attention pieces of the current step, per layer class (full / sliding
+    // window): computed at the first layer of each class, reused by the others
+    int pc_tag[2];                     // cstep * 2 + class + 1 the pieces below belong to; 0: none
+    int pc_n[2];                       // pieces (-1: more than the cache holds)
+    __align__(16) int pc_words[2][kPieceCache * kPieceWords];
     // MoE routing of the current layer, written by the consumers, read by the loader too
     volatile int moe_ready;            // step * kMaxLayers + layer + 1 whose routing is below
     int moe_nu;                        // experts in the union of the batch rows' routes
@@ -663,6 +670,7 @@ struct Piece {
     int nrec;        // records the row's merge reads (prefix pieces + its own)
     bool prefix;     // a shared-prefix piece: writes records for every row, merges nothing
 };
+static_assert(sizeof(Piece) <= 4 * kPieceWords && alignof(Piece) <= 4, "a cached piece fits its words");
 
 // Calls f(piece) for each attention piece of this CTA. Work items are (row b, kv head g)
 // with np(b) pages each, plus one item per (active prefix group, g). When there are no
@@ -2492,8 +2500,35 @@ __device__ __noinline__ uint32_t attention_stage(uint32_t seq, int l, int cta) {
         for_each_group_piece(*c.a, c.sm->pos, l, cta, piece);
         for_each_group_piece(*c.a, c.sm->pos, l, cta, merge);
     } else {
-        for_each_row_piece(*c.a, c.sm->pos, l, cta, piece);
-        for_each_row_piece(*c.a, c.sm->pos, l, cta, merge);
+        // The partition depends only on the step's positions and on whether the layer
+        // slides, so it is computed once per step and layer class and kept in shared memory.
+        const Plan& p = c.a->p;
+        const int cls = (p.window > 0 && ((p.sliding_mask[l >> 5] >> (l & 31)) & 1u)) ? 1 : 0;
+        const int want = c.sm->cstep * 2 + cls + 1;
+        Piece* cached = reinterpret_cast<Piece*>(c.sm->pc_words[cls]);
+        if (c.sm->pc_tag[cls] != want) {
+            int k = 0;
+            for_each_row_piece(*c.a, c.sm->pos, l, cta, [&](const Piece& pc) {
+                if (k < kPieceCache && c.tid == 0) cached[k] = pc;
+                ++k;
+            });
+            consumer_sync();  // (every thread has read the previous tag)
+            if (c.tid == 0) {
+                c.sm->pc_n[cls] = k <= kPieceCache ? k : -1;
+                c.sm->pc_tag[cls] = want;
+            }
+            consumer_sync();
+        }
+        const int np = c.sm->pc_n[cls];
+        if (np < 0) {
+            for_each_row_piece(*c.a, c.sm->pos, l, cta, piece);
+            for_each_row_piece(*c.a, c.sm->pos, l, cta, merge);
+        } else {
+#pragma unroll 1
+            for (int i = 0; i < np; ++i) piece(cached[i]);
+#pragma unroll 1
+            for (int i = 0; i < np; ++i) merge(cached[i]);
+        }
     }
     // larger batches: every CTA counts its (possibly empty) share of the merges
     if (!tagged(*c.a)) publish(c, cnt_stage(l, ST_ATTN), l * 16 + ST_ATTN);
@@ -2863,6 +2898,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         sm->moe_ready = 0;
         sm->step_ready = 0;
         sm->cstep = 0;
+        sm->pc_tag[0] = sm->pc_tag[1] = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm->full[s]), 1);
             mbar_init(smem_u32(&sm->empty[s]), kConsumerWarps);
