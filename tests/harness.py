@@ -120,8 +120,14 @@ def check_kv(pair: Pair):
         rms = np.sqrt(np.mean(ov ** 2, axis=-1, keepdims=True))
         small = np.abs(gv - ov) <= SMALL * rms
         bad = (ulp > 1) & ~small
-        assert not bad.any(), (f"{int(bad.sum())} K/V elements differ by more than 1 BF16 ulp and more "
-                               f"than 1/4096 of their row's RMS (max {int(ulp[bad].max())} ulp)")
+        if bad.any():
+            rows = np.argwhere(g_changed)  # (layer, page, K/V, head, slot) of each written row
+            where = [f"(layer, page, kv, head, slot) {tuple(int(v) for v in rows[r])} dim {int(d)}: "
+                     f"gpu {gv[r, d]:.6g} oracle {ov[r, d]:.6g} row rms {rms[r, 0]:.3g}"
+                     for r, d in np.argwhere(bad)[:6]]
+            raise AssertionError(f"{int(bad.sum())} K/V elements differ by more than 1 BF16 ulp and more "
+                                 f"than 1/4096 of their row's RMS (max {int(ulp[bad].max())} ulp); "
+                                 + "; ".join(where))
         KV_STATS["elements"] += int(ulp.size)
         KV_STATS["ulp0"] += int((ulp == 0).sum())
         KV_STATS["ulp1"] += int((ulp == 1).sum())
