@@ -84,13 +84,22 @@ class Twin:
         return [{"k": np.zeros((0, cfg.n_kv_heads, cfg.head_dim)),
                  "v": np.zeros((0, cfg.n_kv_heads, cfg.head_dim))} for _ in range(cfg.n_layers)]
 
-    def step(self, cache, token: int, pos: int):
+    def step(self, cache, token: int, pos: int, appended=None):
         """Appends the step's K/V rows to ``cache`` (which must hold exactly ``pos`` rows)
-        and returns the logits (float64 [vocab])."""
+        and returns the logits (float64 [vocab]).
+
+        The step's own BF16-rounded K/V rows are also kept in ``self.own_appends`` (one
+        (K, V) pair of [kv heads, head_dim] arrays per layer). ``appended``, if given,
+        holds one such pair per layer from another implementation of the same step: the
+        cache then stores those rows instead of the step's own, so every later layer
+        runs from that implementation's rounding of the current token's K/V (the current
+        token attends to its own key and value, so one BF16 rounding that falls the
+        other way in an early layer shifts every later layer's input)."""
         cfg = self.cfg
         hd, Hq, Hkv = cfg.head_dim, cfg.n_q_heads, cfg.n_kv_heads
         G = Hq // Hkv
         x = self.embed[token].copy()
+        self.own_appends = []
         for l, L in enumerate(self.layers):
             c = cache[l]
             assert c["k"].shape[0] == pos
@@ -98,8 +107,12 @@ class Twin:
             q = self.rope((L["wq"] @ xn).reshape(Hq, hd), pos)
             k = self.rope((L["wk"] @ xn).reshape(Hkv, hd), pos)
             v = (L["wv"] @ xn).reshape(Hkv, hd)
-            c["k"] = np.concatenate([c["k"], round_to_bf16(k)[None]], 0)
-            c["v"] = np.concatenate([c["v"], round_to_bf16(v)[None]], 0)
+            kr, vr = round_to_bf16(k), round_to_bf16(v)
+            self.own_appends.append((kr, vr))
+            if appended is not None:
+                kr, vr = appended[l]
+            c["k"] = np.concatenate([c["k"], kr[None]], 0)
+            c["v"] = np.concatenate([c["v"], vr[None]], 0)
             slides = cfg.sliding_window > 0 and cfg.layer_is_sliding()[l]
             lo = max(0, pos - cfg.sliding_window + 1) if slides else 0
             o = np.empty((Hq, hd))
