@@ -308,7 +308,7 @@ MK_API mk_status mk_decode_step_noalloc(const mk_model_desc *desc, const mk_weig
  * step ran; they are overwritten by the next step. The element size is
  * *bytes / (max_batch * width): 8 bytes when the element is a tagged word (low 32 bits
  * the fp32 value, high 32 bits the tag of the write that produced it; QKV always, the
- * others after a step with batch <= 4), else 4 bytes of plain fp32.
+ * others after a step with batch <= 2), else 4 bytes of plain fp32.
  * Layouts (row b at b*width elements):
  *   MK_BUF_X     residual stream after the last layer (input of the final norm),
  *                [max_batch][d_model], permuted columns (below)

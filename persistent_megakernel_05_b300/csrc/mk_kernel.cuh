@@ -18,7 +18,7 @@
 //     wait. It has the SM's scheduler 0 to itself (warps 4 and 8 only exit), so busy
 //     consumer warps never starve it of issue slots;
 //   * eight consumer warps (warps 1-3, 5-7, 9-10 on schedulers 1-3) compute: exact fp32
-//     CUDA-core GEMV for batches up to 4, BF16 mma.sync GEMV tiles above (activations
+//     CUDA-core GEMV for batches up to 2, BF16 mma.sync GEMV tiles above (activations
 //     split hi + lo), flash-decode attention on mma.sync with keys in the M dimension and
 //     online softmax, fused epilogues (RoPE + KV append, residual add, SwiGLU, partial
 //     argmax); warp 11 optionally prefetches the loader's future reads into L2.
@@ -210,9 +210,13 @@ struct StepArgs {
 };
 
 // Up to this batch size the activations between stages travel as tagged words (one
-// read latency per hand-off, no fence); above it, as fp32 behind counters, because a
-// tagged word doubles the bytes every CTA reads and the registers a poll holds.
-constexpr int kMaxTaggedBatch = 4;
+// read latency per hand-off, no fence) and the GEMVs run on the CUDA cores; above it the
+// activations travel as fp32 behind counters (a tagged word doubles the bytes every CTA
+// reads and the registers a poll holds) and the GEMVs run on mma.sync tiles, which read
+// those fp32 rows. From 3 rows on that pair is faster: 8B shapes at 4 rows 1.845 -> 1.447
+// ms per step for 8 layers, 2B shapes at 4 rows -1.4 %, 3 rows unchanged; at 2 rows the
+// tensor-core GEMV is a third slower.
+constexpr int kMaxTaggedBatch = 2;
 __device__ __forceinline__ bool tagged(const StepArgs& a) { return a.B <= kMaxTaggedBatch; }
 
 // counter slots (batches above kMaxTaggedBatch)
@@ -1352,7 +1356,7 @@ __device__ __noinline__ int tk_draw(int b, uint32_t tag, int task) {
 // the small-batch path computes the RMSNorm statistics from its own activation loads
 // when the whole input row is one k-chunk
 __device__ __forceinline__ bool fused_norm_stage(const StepArgs& a, const GemvStage& s) {
-    return a.B <= 4 && s.K <= KCW;
+    return a.B <= kMaxTaggedBatch && s.K <= KCW;
 }
 
 // a consumer warp waits for ring slot `q` to be full; warp-uniform result. Fast path:
@@ -1394,7 +1398,7 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[8 * BP], int l
     return v[0];
 }
 
-// Small batches (B <= 4): exact fp32 CUDA-core dot products. Each lane owns one 8-column
+// Small batches (B <= kMaxTaggedBatch): exact fp32 CUDA-core dot products. Each lane owns one 8-column
 // piece of the k-chunk (a 16 B read of every row), with the piece's activations in
 // registers. Each slot's 8 x BP partial sums are reduced across the warp at once (one
 // value per lane, or per group of lanes, at the end) and added to this warp's partials
@@ -1734,7 +1738,7 @@ __device__ __forceinline__ void gemv_mma(Ctx& c, const GemvStage& s, int r0, int
 }
 
 // Epilogues from the staged outputs yout[vrow][8] (vrow = 8 * group + row; GU: up rows
-// start at vrow 8 * ngate): the LM head at every batch, every stage above 4 rows.
+// start at vrow 8 * ngate): the LM head at every batch, every stage above kMaxTaggedBatch rows.
 __device__ __forceinline__ void yout_epilogue(Ctx& c, const GemvStage& s, int r0, int r1,
                                               const float* yout) {
     const StepArgs& a = *c.a;
@@ -1861,15 +1865,10 @@ __device__ __noinline__ uint32_t gemv_task_mma(uint32_t seq, int kind, int layer
 }
 __device__ __forceinline__ uint32_t gemv_task_call(uint32_t seq, int kind, int layer, int r0, int r1) {
     const int B = make_ctx(seq).a->B;
-    if (B > 4) return gemv_task_mma(seq, kind, layer, r0, r1);
-    if (kind == G_LM) {
-        if (B == 1) return gemv_task_fma_lm<1>(seq, r0, r1);
-        if (B == 2) return gemv_task_fma_lm<2>(seq, r0, r1);
-        return gemv_task_fma_lm<4>(seq, r0, r1);
-    }
-    if (B == 1) return gemv_task_fma<1>(seq, kind, layer, r0, r1);
-    if (B == 2) return gemv_task_fma<2>(seq, kind, layer, r0, r1);
-    return gemv_task_fma<4>(seq, kind, layer, r0, r1);
+    static_assert(kMaxTaggedBatch == 2, "the CUDA-core GEMV is instantiated for 1 and 2 rows");
+    if (B > kMaxTaggedBatch) return gemv_task_mma(seq, kind, layer, r0, r1);
+    if (kind == G_LM) return B == 1 ? gemv_task_fma_lm<1>(seq, r0, r1) : gemv_task_fma_lm<2>(seq, r0, r1);
+    return B == 1 ? gemv_task_fma<1>(seq, kind, layer, r0, r1) : gemv_task_fma<2>(seq, kind, layer, r0, r1);
 }
 
 
