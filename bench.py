@@ -338,48 +338,33 @@ def timed_region(one, warmup, steps, dist):
 
 
 def e2e_loop(S, cfg, steps, warmup):
-    """End to end through the public API: every step copies its inputs from pinned
-    host memory, runs mk_decode_step, and reads the next tokens back to the host
-    (which feeds them to the following step). Returns the wall time (s) of the timed
-    steps and the bytes copied each way per step."""
-    import torch
+    """End to end through the public API with HOST buffers: every step calls
+    mk_decode_step_host, which packs the step's inputs into one host-to-device copy, runs
+    the step, and returns the device status word and the next tokens in one
+    device-to-host copy; the host feeds the tokens to the following step. Returns the
+    wall time (s) of the timed steps and the bytes copied each way per step."""
+    import numpy as np
     model = S["model"]
     B = S["B"]
-    dev = S["pos"].device
-    pt_host = torch.tensor(S["pt_host"], dtype=torch.int32).pin_memory()
+    pt_host = np.ascontiguousarray(S["pt_host"], dtype=np.int32)
     maxp = pt_host.shape[1]
-    h_tok = torch.zeros(B, dtype=torch.int32).pin_memory()
-    h_pos = torch.zeros(B, dtype=torch.int32).pin_memory()
-    h_sl = torch.zeros(B, dtype=torch.int32).pin_memory()
-    h_next = torch.zeros(B, dtype=torch.int32).pin_memory()
-    d_tok = torch.empty(B, dtype=torch.int32, device=dev)
-    d_pos = torch.empty(B, dtype=torch.int32, device=dev)
-    d_sl = torch.empty(B, dtype=torch.int32, device=dev)
-    d_pt = torch.empty((B, maxp), dtype=torch.int32, device=dev)
-    d_next = torch.empty(B, dtype=torch.int32, device=dev)
+    h_tok = np.zeros(B, dtype=np.int32)
+    h_pos = np.zeros(B, dtype=np.int32)
+    h_sl = np.zeros(B, dtype=np.int32)
+    h_next = np.zeros(B, dtype=np.int32)
     h_tok[0] = S["tok0"]
-    h2d = (h_tok.numel() + h_pos.numel() + h_sl.numel() + pt_host.numel()) * 4
-    d2h = h_next.numel() * 4
+    h2d = (3 * B + B * maxp) * 4        # tokens, positions, seq_lens, page table: one copy
+    d2h = (4 + B) * 4                   # status word (+ 2 spare ints) and next tokens: one copy
 
     def one(t):
         p = CTX + (t % CYCLE)
-        h_pos.fill_(p)
-        h_sl.fill_(p + 1)
-        d_tok.copy_(h_tok, non_blocking=True)
-        d_pos.copy_(h_pos, non_blocking=True)
-        d_sl.copy_(h_sl, non_blocking=True)
-        d_pt.copy_(pt_host, non_blocking=True)
-        model.step(d_tok, d_pos, d_pt, d_sl, d_next, None)
-        h_next.copy_(d_next, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        h_tok.copy_(h_next)
+        h_pos.fill(p)
+        h_sl.fill(p + 1)
+        model.step_host(h_tok, h_pos, pt_host, h_sl, h_next)
+        h_tok[:] = h_next
 
     for t in range(warmup):
         one(t)
-    code, task = model.status()
-    if code != 0:
-        raise RuntimeError(f"e2e warm-up failed: status {code}")
-    torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
         one(warmup + i)
@@ -714,7 +699,7 @@ def main():
         val = whole_job_value(world, S["B"], e2e_steps, 1000.0 * wall)
         out["e2e"] = {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                      "path": "pinned host inputs -> cudaMemcpyAsync -> mk_decode_step -> next token to host, sync every step"}
+                      "path": "host arrays -> mk_decode_step_host (one H2D copy of the packed inputs, the step, one D2H copy of status + next tokens, synchronous) -> next token fed back"}
     # CPU baseline: the oracle on the host cores (rank 0, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu:
         W_cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in W.items() if k != "layers"}

@@ -171,6 +171,24 @@ MK_API mk_status mk_decode_step(mk_handle *h, const int32_t *tokens, const int32
                          const int32_t *seq_lens, int32_t batch, int32_t *next_tokens,
                          float *logits, void *stream);
 
+/* One decode step from and to HOST memory, synchronous: the call a serving loop makes
+ * when its tokens live on the host. The arguments mean what they mean for
+ * mk_decode_step, with every pointer in host memory (pageable or pinned). The inputs
+ * are packed into a pinned staging buffer the handle owns and reach the device in ONE
+ * host-to-device copy; the step runs on `stream`; the device status word and the next
+ * tokens come back in ONE device-to-host copy (the logits, when `logits` is not NULL,
+ * in a second one); the call returns once they are in the caller's arrays.
+ * The handle grows its staging buffers on the first call that needs more room (the
+ * logits buffer, max_batch * vocab fp32, on the first call that asks for logits);
+ * mk_destroy frees them. Calls on one handle must not overlap (the staging is shared).
+ * Returns host-side argument errors, MK_ERR_OOM if staging cannot be allocated, else
+ * the step's device status (MK_OK or the latched error, as mk_status_sync reports). */
+MK_API mk_status mk_decode_step_host(mk_handle *h, const int32_t *tokens,
+                                     const int32_t *positions, const int32_t *page_table,
+                                     int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                     int32_t batch, int32_t *next_tokens, float *logits,
+                                     void *stream);
+
 /* n_steps consecutive decode steps of the same rows as ONE launch (the token of each
  * step is fed back on the device). Source: "Kog AI: standart GPU'larda 3,000 token/s",
  * on kernel boundaries and on sampling kept on the GPU.

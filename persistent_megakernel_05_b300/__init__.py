@@ -34,7 +34,7 @@ MK_OPT_PREFETCH_SLOTS = 3
 ABI_SYMBOLS = ("mk_create", "mk_kv_alloc", "mk_kv_free", "mk_decode_step", "mk_status_sync",
                "mk_status_reset", "mk_set_option", "mk_get_info", "mk_debug_buffer",
                "mk_status_string", "mk_destroy", "mk_decode_step_noalloc", "mk_set_sampling",
-               "mk_set_shared_prefix", "mk_decode_steps")
+               "mk_set_shared_prefix", "mk_decode_steps", "mk_decode_step_host")
 MK_NOALLOC_SCRATCH_BYTES = 8 << 20
 MK_BUF_X, MK_BUF_QKV, MK_BUF_ATTN, MK_BUF_H, MK_BUF_ROUTE, MK_BUF_MOE_UNION = 1, 2, 3, 4, 5, 6
 
@@ -108,6 +108,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mk_kv_free.argtypes = [_vp, _P(mk_kv_pool)]
     L.mk_decode_step.restype = ctypes.c_int
     L.mk_decode_step.argtypes = [_vp, _vp, _vp, _vp, i32, _vp, i32, _vp, _vp, _vp]
+    L.mk_decode_step_host.restype = ctypes.c_int
+    L.mk_decode_step_host.argtypes = [_vp, _vp, _vp, _vp, i32, _vp, i32, _vp, _vp, _vp]
     L.mk_decode_steps.restype = ctypes.c_int
     L.mk_decode_steps.argtypes = [_vp, i32, _vp, _vp, _vp, i32, _vp, i32, _vp, _vp, _vp]
     L.mk_status_sync.restype = ctypes.c_int
@@ -172,6 +174,15 @@ def mk_decode_step(handle: int, tokens: int, positions: int, page_table: int,
     """Raw call with device addresses (ints). Returns the mk_status code."""
     return load().mk_decode_step(handle, tokens, positions, page_table, max_pages_per_seq,
                                  seq_lens, batch, next_tokens, logits, stream)
+
+
+def mk_decode_step_host(handle: int, tokens: int, positions: int, page_table: int,
+                        max_pages_per_seq: int, seq_lens: int, batch: int, next_tokens: int,
+                        logits: Optional[int], stream: Optional[int] = None) -> int:
+    """Raw call with HOST addresses (ints); synchronous. Returns the mk_status code (the
+    step's device status when the call itself succeeded)."""
+    return load().mk_decode_step_host(handle, tokens, positions, page_table, max_pages_per_seq,
+                                      seq_lens, batch, next_tokens, logits, stream)
 
 
 def mk_decode_steps(handle: int, n_steps: int, tokens: int, positions: int, page_table: int,
@@ -353,6 +364,25 @@ class DecodeModel:
                               next_tokens.data_ptr(),
                               logits.data_ptr() if logits is not None else None, s.cuda_stream)
         _check(code, "mk_decode_step")
+
+    def step_host(self, tokens, positions, page_table, seq_lens, next_tokens, logits=None,
+                  stream=None):
+        """One decode step from and to host memory (numpy arrays, C-contiguous: int32
+        inputs and next_tokens, fp32 logits [B][vocab] or None); returns when next_tokens
+        (and logits) hold the step's results. Raises on a host or device error."""
+        import numpy as np
+        import torch
+        for a in (tokens, positions, page_table, seq_lens, next_tokens):
+            assert isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous
+        if logits is not None:
+            assert logits.dtype == np.float32 and logits.flags.c_contiguous
+        B = tokens.shape[0]
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        code = mk_decode_step_host(self.handle, tokens.ctypes.data, positions.ctypes.data,
+                                   page_table.ctypes.data, page_table.shape[1], seq_lens.ctypes.data,
+                                   B, next_tokens.ctypes.data,
+                                   logits.ctypes.data if logits is not None else None, s.cuda_stream)
+        _check(code, "mk_decode_step_host")
 
     def steps(self, n_steps, tokens, positions, page_table, seq_lens, next_tokens, logits=None,
               stream=None):

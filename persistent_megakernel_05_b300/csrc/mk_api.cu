@@ -46,6 +46,11 @@ struct mk_handle {
     int hd = 0;
     int64_t weight_bytes = 0;
     size_t counters_words = 0, arrivals_words = 0;
+    // mk_decode_step_host: pinned host staging and its device twin, grown on demand
+    void* host_stage = nullptr;     // [tokens | positions | seq_lens | page_table], then the outputs
+    void* dev_stage = nullptr;      // the same inputs on the device
+    size_t stage_bytes = 0;         // capacity of both input areas
+    float* dev_logits = nullptr;    // [max_batch][vocab] fp32, allocated on first use
 };
 
 namespace {
@@ -138,6 +143,9 @@ void free_handle(mk_handle* h) {
     if (h->d_layers) cudaFree(h->d_layers);
     if (h->d_gains) cudaFree(h->d_gains);
     if (h->d_rope) cudaFree(h->d_rope);
+    if (h->host_stage) cudaFreeHost(h->host_stage);
+    if (h->dev_stage) cudaFree(h->dev_stage);
+    if (h->dev_logits) cudaFree(h->dev_logits);
     delete h;
 }
 
@@ -243,7 +251,9 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* weights, int de
     h->arrivals_words = (size_t)mk::kCounterStride;
     const size_t o_cnt = take(sizeof(uint32_t) * h->counters_words);
     const size_t o_arr = take(sizeof(uint32_t) * h->arrivals_words);
-    const size_t o_status = take(sizeof(int) * 4);
+    // status word (2 ints, 2 spare), then the next tokens of mk_decode_step_host, so that
+    // one device-to-host copy returns both
+    const size_t o_status = take(sizeof(int) * (4 + mk::kMaxBatch));
     h->block_bytes = off;
     if (cudaMalloc(&h->block, h->block_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -504,6 +514,69 @@ mk_status mk_decode_steps(mk_handle* h, int32_t n_steps, const int32_t* tokens,
                         batch, next_tokens, logits, stream);
 }
 
+
+mk_status mk_decode_step_host(mk_handle* h, const int32_t* tokens, const int32_t* positions,
+                              const int32_t* page_table, int32_t max_pages_per_seq,
+                              const int32_t* seq_lens, int32_t batch, int32_t* next_tokens,
+                              float* logits, void* stream) {
+    if (!h || !tokens || !positions || !page_table || !seq_lens || !next_tokens)
+        return MK_ERR_INVALID_ARG;
+    if (batch < 1 || batch > h->desc.max_batch || max_pages_per_seq < 1) return MK_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    const size_t nb = (size_t)batch;
+    const size_t in_bytes = sizeof(int32_t) * (3 * nb + nb * (size_t)max_pages_per_seq);
+    const size_t out_bytes = sizeof(int32_t) * (4 + mk::kMaxBatch);
+    if (in_bytes > h->stage_bytes) {
+        if (h->host_stage) cudaFreeHost(h->host_stage);
+        if (h->dev_stage) cudaFree(h->dev_stage);
+        h->host_stage = h->dev_stage = nullptr;
+        h->stage_bytes = 0;
+        if (cudaHostAlloc(&h->host_stage, in_bytes + out_bytes, cudaHostAllocDefault) != cudaSuccess ||
+            cudaMalloc(&h->dev_stage, in_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            if (h->host_stage) cudaFreeHost(h->host_stage);
+            if (h->dev_stage) cudaFree(h->dev_stage);
+            h->host_stage = h->dev_stage = nullptr;
+            return MK_ERR_OOM;
+        }
+        h->stage_bytes = in_bytes;
+    }
+    if (logits && !h->dev_logits &&
+        cudaMalloc(&h->dev_logits, sizeof(float) * (size_t)h->desc.max_batch * h->desc.vocab) != cudaSuccess) {
+        cudaGetLastError();
+        h->dev_logits = nullptr;
+        return MK_ERR_OOM;
+    }
+    // pack the inputs; one host-to-device copy
+    int32_t* hs = static_cast<int32_t*>(h->host_stage);
+    std::memcpy(hs, tokens, sizeof(int32_t) * nb);
+    std::memcpy(hs + nb, positions, sizeof(int32_t) * nb);
+    std::memcpy(hs + 2 * nb, seq_lens, sizeof(int32_t) * nb);
+    std::memcpy(hs + 3 * nb, page_table, sizeof(int32_t) * nb * (size_t)max_pages_per_seq);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(h->dev_stage, hs, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_INTERNAL;
+    }
+    const int32_t* ds = static_cast<const int32_t*>(h->dev_stage);
+    const mk_status ls = launch_steps(h, 1, ds, ds + nb, ds + 3 * nb, max_pages_per_seq, ds + 2 * nb, batch,
+                                      h->plan.status + 4, logits ? h->dev_logits : nullptr, stream);
+    if (ls != MK_OK) {
+        cudaStreamSynchronize(st);  // the copy must finish before the staging is reused
+        return ls;
+    }
+    // the status word and the next tokens in one device-to-host copy
+    int32_t* ho = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(h->host_stage) + h->stage_bytes);
+    if (cudaMemcpyAsync(ho, h->plan.status, sizeof(int32_t) * (4 + nb), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        (logits && cudaMemcpyAsync(logits, h->dev_logits, sizeof(float) * nb * (size_t)h->desc.vocab,
+                                   cudaMemcpyDeviceToHost, st) != cudaSuccess) ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return MK_ERR_INTERNAL;
+    }
+    std::memcpy(next_tokens, ho + 4, sizeof(int32_t) * nb);
+    return (mk_status)ho[0];
+}
 
 mk_status mk_status_sync(mk_handle* h, void* stream, int32_t* failing_task) {
     if (!h) return MK_ERR_INVALID_ARG;
