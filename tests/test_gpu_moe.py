@@ -1,7 +1,7 @@
 """GPU parity of the MoE layers (softmax top-k routing over the router logits, routed
 experts' SwiGLU, routing-weighted sum; "Kog Inference Engine" MoE paragraphs) against the
-CPU oracle, through the C ABI, at batch 1 (tagged-word hand-off) and batch 8 (fp32 +
-counters, union of the rows' routes)."""
+CPU oracle, through the C ABI, at batch 1 and 2 (tagged-word hand-off) and batches 3 and 8
+(fp32 + counters), over the union of the rows' routes."""
 import numpy as np
 import pytest
 import torch
@@ -51,9 +51,9 @@ def test_tiny_moe_prompt_then_greedy(gain_noise):
     pair.close()
 
 
-@pytest.mark.parametrize("B", [3, 8])
+@pytest.mark.parametrize("B", [2, 3, 8])
 def test_tiny_moe_batch_ragged(B):
-    """Batch 3 (tagged words) and 8 (fp32 + counters): each row routes on its own; the
+    """Batch 2 (tagged words), 3 and 8 (fp32 + counters): each row routes on its own; the
     expert stages run over the union of the rows' routes."""
     cfg = TINY_MOE
     pair = Pair(cfg, seed=12, num_pages=96, kv_seed=3)

@@ -65,7 +65,8 @@ def test_8b_shapes_batch4_one_group_two_column_tiles():
 
 
 @pytest.mark.parametrize("B,groups", [
-    (3, [((0, 1, 2), 4)]),                       # tagged words, one tile (6 columns)
+    (2, [((0, 1), 4)]),                          # tagged words, one tile (4 columns)
+    (3, [((0, 1, 2), 4)]),                       # fp32 + counters, one tile (6 columns)
     (6, [((0, 2, 3), 4), ((1, 5), 3)]),          # fp32 + counters; row 4 alone
     (8, [((0, 1, 2, 3, 4, 5, 6, 7), 5)]),        # 16 columns of head dim 64
 ])

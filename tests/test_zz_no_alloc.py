@@ -7,10 +7,10 @@ the KV pool.
 Checked here, on two consecutive calls each (the second one finds the array holding the
 first call's contents): the result matches the CPU oracle at the parity bar (logits,
 tokens where the oracle's margin is clear, K/V appends at the oracle's addresses and
-within 1 BF16 ulp), at batch 1 and 3 (tagged-word hand-off, which relies on the
-per-call clearing of the array) and batch 8 (counters), for a small dense model, a small
-MoE and the 2B shapes cut to two layers; and it matches the handle-based mk_decode_step on
-the same inputs.
+within 1 BF16 ulp), at batch 1 and 2 (tagged-word hand-off, which relies on the
+per-call clearing of the array) and batch 3 and 8 (counters), for a small dense model, a
+small MoE and the 2B shapes cut to two layers; and it matches the handle-based
+mk_decode_step on the same inputs.
 
 This file is collected last on purpose: if it fails, a run that stops at the first
 failure has already run every other test.
