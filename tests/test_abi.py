@@ -27,6 +27,21 @@ def test_header_declares_the_abi():
     assert sorted(declared_symbols()) == sorted(mk.ABI_SYMBOLS)
 
 
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++17")])
+def test_header_compiles_as_plain_c_and_cpp(tmp_path, lang, std):
+    """The ABI header is usable from C (no C++ or torch types leak into it)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / "use_mk.c"
+    src.write_text('#include "mk.h"\nint main(void) { return (int)sizeof(mk_model_desc) > 0 ? 0 : 1; }\n')
+    subprocess.run([cc, "-x", lang, std, "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o", str(tmp_path / "use_mk.o")],
+                   check=True)
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_symbols():
         assert hasattr(lib, name), name
@@ -67,6 +82,7 @@ def test_host_side_argument_errors_need_no_gpu(lib):
     # valid shape, but null weight pointers
     assert lib.mk_create(ctypes.byref(d), ctypes.byref(w), 0, ctypes.byref(h)) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_decode_step(None, None, None, None, 1, None, 1, None, None, None) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_decode_step_host(None, None, None, None, 1, None, 1, None, None, None) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_kv_alloc(None, 4, None) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_status_reset(None) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_set_option(None, mk.MK_OPT_TIMEOUT_NS, 10**9) == mk.MK_ERR_INVALID_ARG
