@@ -113,6 +113,32 @@ def test_bad_page_latches_error_then_reset_recovers():
     pair.close()
 
 
+def test_full_batch_at_the_last_position_then_one_past():
+    """Every row of a full batch (max_batch rows) at the last position the model allows
+    (max_positions - 1) matches the oracle; one row one position further latches
+    MK_ERR_INVALID_ARG (the RoPE table ends there), and the handle recovers after reset."""
+    cfg = synth.TINY.with_(max_positions=64)
+    B, per = cfg.max_batch, 4
+    pair = Pair(cfg, seed=16, num_pages=B * per + 2, kv_seed=3)
+    rng = np.random.default_rng(16)
+    pt = synth.random_page_tables(rng, B * per + 2, [per] * B, per)
+    pos = np.full(B, cfg.max_positions - 1, np.int32)
+    toks = synth.random_tokens(rng, cfg.vocab, B)
+    g_lg, g_nx, o_lg, o_nx = pair.step(toks, pos, pt)
+    check_logits(g_lg, g_nx, o_lg, o_nx, what="last position")
+    assert check_kv(pair) == B * cfg.n_layers * 2 * cfg.n_kv_heads
+    g = pair.gpu
+    dev = "cuda"
+    past = torch.tensor(pos, device=dev)
+    past[3] += 1
+    nxt = torch.zeros(B, dtype=torch.int32, device=dev)
+    g.step(torch.tensor(g_nx, device=dev), past, torch.tensor(pt, device=dev), past + 1, nxt)
+    assert g.status()[0] == mk.MK_ERR_INVALID_ARG
+    g.reset()
+    assert g.status()[0] == mk.MK_OK
+    pair.close()
+
+
 def test_bad_step_inputs_latch_invalid():
     cfg, pair = _small_model()
     g = pair.gpu
